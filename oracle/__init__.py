@@ -1,0 +1,185 @@
+"""CPU oracle for the W4A16 skinny GEMM and the int4 lm_head greedy verify.
+
+TEST INFRASTRUCTURE ONLY.  The tests, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` are the only callers.  The product library
+never imports, links or runs anything here, and this package imports nothing
+from the product package.
+
+The arithmetic lives in ``oracle.c`` (plain C, built with gcc, OpenMP over
+output rows only, ``-ffp-contract=off``); this module only marshals numpy
+arrays through ctypes and composes the three steps of the verify:
+logits -> argmax -> first-mismatch comparison.
+
+Sources, by page and section:
+  * "qwen-warp, llamAmpere ..." -- "qwen-warp: keep the activations in bf16"
+    (nibble format, level = nibble - 8, fp32 group scale after each
+    128-column group) and "What each one calls the same answer" (greedy
+    acceptance is argmax equality over the verify rows).
+  * "swift-qwen3.8-rtx3090" -- "Body, heads and drafter" (keep drafts up to the
+    first disagreement; a restricted draft head is a slice of lm_head rows).
+  * "OpenJet engine" -- "How it works" (verify over T = 1 + n_draft rows),
+    "How it gets its speed" (restricted draft vocabulary).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from dataclasses import dataclass
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_lib = None
+
+_u16p = np.ctypeslib.ndpointer(dtype=np.uint16, flags="C_CONTIGUOUS")
+_u32p = np.ctypeslib.ndpointer(dtype=np.uint32, flags="C_CONTIGUOUS")
+_i32p = np.ctypeslib.ndpointer(dtype=np.int32, flags="C_CONTIGUOUS")
+_f32p = np.ctypeslib.ndpointer(dtype=np.float32, flags="C_CONTIGUOUS")
+_f64p = np.ctypeslib.ndpointer(dtype=np.float64, flags="C_CONTIGUOUS")
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into ``oracle/_build/liboracle.so`` (gcc, OpenMP)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + ".%d.tmp" % os.getpid()
+    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-ffp-contract=off", "-fno-fast-math",
+           "-fPIC", "-shared", "-Wall", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    lib = ctypes.CDLL(build())
+    c_int = ctypes.c_int
+    lib.or_w4a16_gemm.restype = c_int
+    lib.or_w4a16_gemm.argtypes = [_u16p, _u32p, _u16p, c_int, c_int, c_int,
+                                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    lib.or_lmhead_logits.restype = c_int
+    lib.or_lmhead_logits.argtypes = [_u16p, _u32p, _u16p, c_int, c_int, ctypes.c_void_p,
+                                     c_int, c_int, ctypes.c_void_p, ctypes.c_void_p]
+    lib.or_argmax.restype = c_int
+    lib.or_argmax.argtypes = [_f32p, c_int, c_int, ctypes.c_void_p, _i32p,
+                              ctypes.c_void_p, ctypes.c_void_p]
+    lib.or_verify.restype = c_int
+    lib.or_verify.argtypes = [_i32p, ctypes.c_void_p, c_int, ctypes.POINTER(ctypes.c_int32),
+                              ctypes.POINTER(ctypes.c_int32)]
+    _lib = lib
+    return lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def w4a16_gemm(x, Wq, scales, T, K, N, want64=False):
+    """Return (y32 [T][N] float32, ybf [T][N] uint16 bf16 bits[, y64]).
+
+    y[t][n] = sum_g scale[n][g] * sum_{k in g} (nibble(n,k) - 8) * x[t][k],
+    fp32 group sums in ascending k, then round-to-nearest-even to bf16.
+    """
+    lib = _load()
+    x = _c(x, np.uint16).reshape(-1)
+    Wq = _c(Wq, np.uint32).reshape(-1)
+    scales = _c(scales, np.uint16).reshape(-1)
+    y32 = np.empty((T, N), np.float32)
+    ybf = np.empty((T, N), np.uint16)
+    y64 = np.empty((T, N), np.float64) if want64 else None
+    rc = lib.or_w4a16_gemm(x, Wq, scales, T, K, N, _ptr(y32), _ptr(y64), _ptr(ybf))
+    if rc != 0:
+        raise ValueError("oracle w4a16_gemm rejected its arguments")
+    return (y32, ybf, y64) if want64 else (y32, ybf)
+
+
+def lmhead_logits(x, Wq, scales, K, T, V, rows=None, want64=False):
+    """fp32 logits [T][n_rows] of the rows listed in ``rows`` (None: all V)."""
+    lib = _load()
+    x = _c(x, np.uint16).reshape(-1)
+    Wq = _c(Wq, np.uint32).reshape(-1)
+    scales = _c(scales, np.uint16).reshape(-1)
+    rows_a = None if rows is None else _c(rows, np.int32)
+    n_rows = V if rows is None else int(rows_a.size)
+    l32 = np.empty((T, n_rows), np.float32)
+    l64 = np.empty((T, n_rows), np.float64) if want64 else None
+    rc = lib.or_lmhead_logits(x, Wq, scales, K, T, _ptr(rows_a), n_rows, V, _ptr(l32), _ptr(l64))
+    if rc != 0:
+        raise ValueError("oracle lmhead_logits rejected its arguments")
+    return (l32, l64) if want64 else l32
+
+
+def argmax(logits, ids=None):
+    """Row argmax with lowest token id on ties.
+
+    Returns (a, best, second): token ids, the top value and the runner-up value.
+    """
+    lib = _load()
+    logits = _c(logits, np.float32)
+    T, n = logits.shape
+    ids_a = None if ids is None else _c(ids, np.int32)
+    a = np.empty(T, np.int32)
+    best = np.empty(T, np.float32)
+    second = np.empty(T, np.float32)
+    rc = lib.or_argmax(logits, T, n, _ptr(ids_a), a, _ptr(best), _ptr(second))
+    if rc != 0:
+        raise ValueError("oracle argmax rejected its arguments (non-finite logits?)")
+    return a, best, second
+
+
+def verify(a, drafts):
+    """(accept_len, next_token) for one block: first mismatch, then a[accept_len]."""
+    lib = _load()
+    a = _c(a, np.int32)
+    d = _c(drafts, np.int32) if len(drafts) else None
+    if a.size != (0 if d is None else d.size) + 1:
+        raise ValueError("verify needs len(a) == n_draft + 1")
+    acc = ctypes.c_int32()
+    nxt = ctypes.c_int32()
+    rc = lib.or_verify(a, _ptr(d), 0 if d is None else d.size, ctypes.byref(acc), ctypes.byref(nxt))
+    if rc != 0:
+        raise ValueError("oracle verify rejected its arguments")
+    return int(acc.value), int(nxt.value)
+
+
+@dataclass
+class VerifyResult:
+    accept_len: np.ndarray   # [n_streams] int32
+    next_token: np.ndarray   # [n_streams] int32
+    a: np.ndarray            # [T] argmax token id per row
+    margin: np.ndarray       # [T] best - runner-up logit per row (fp32)
+    logits: np.ndarray       # [T][n_rows] fp32
+
+
+def lmhead_verify(x, Wq, scales, K, V, drafts, n_streams=1, vocab_map=None):
+    """The whole greedy verify: logits -> argmax -> per-stream first mismatch.
+
+    x holds n_streams blocks of (1 + n_draft) rows; drafts is
+    [n_streams][n_draft].  With vocab_map the candidate rows are
+    Wq[vocab_map[j]] and every id returned is a token id.
+    """
+    drafts = np.asarray(drafts, np.int32).reshape(n_streams, -1)
+    n_draft = drafts.shape[1]
+    rows_per = n_draft + 1
+    T = n_streams * rows_per
+    logits = lmhead_logits(x, Wq, scales, K, T, V, rows=vocab_map)
+    a, best, second = argmax(logits, ids=vocab_map)
+    acc = np.empty(n_streams, np.int32)
+    nxt = np.empty(n_streams, np.int32)
+    for s in range(n_streams):
+        acc[s], nxt[s] = verify(a[s * rows_per:(s + 1) * rows_per], drafts[s])
+    margin = (best.astype(np.float64) - second.astype(np.float64))
+    return VerifyResult(acc, nxt, a, margin, logits)
+
