@@ -1,0 +1,541 @@
+#!/usr/bin/env python
+"""Benchmark of the W4A16 verify hot path on GB300.
+
+One step = one speculative verify pass of a 27B-class decoder's weight read at
+T = 4 (1 + 3 drafts): the three decode GEMMs (fused QKV 5120->10240, fused
+gate+up 5120->34816, down 17408->5120) and the int4 lm_head pass with greedy
+verification over V = 248,320 (the "mtp_T4" workload).  The metric is
+algorithmic HBM bytes per second (weights + scales read once, activations
+read, outputs written).  Inputs are seeded synthetic data with the shapes of
+that model; the step streams 820 MB, more than the 129 MB L2, so every kernel
+reads its weights from HBM.
+
+Usage: python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+                       [--ncu-case head|gemm] [--breakdown]
+One JSON line on stdout (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import gen  # noqa: E402
+
+METRIC = "W4A16 skinny-GEMM + lm_head verify HBM GB/s (frac of 8 TB/s), T=1..32"
+NOMINAL_HBM_GBS = 8000.0
+WORKLOAD = "mtp_T4"
+T_STEP = 4
+N_DRAFT = 3
+
+
+# ----------------------------------------------------------------------------
+# helpers
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def kernel_source_digest():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_verify_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it
+    was taken on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    digest = kernel_source_digest()
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 3 and not line.startswith("#") and parts[0] == kernel and parts[1] == digest:
+                return int(parts[2])
+    return None
+
+
+class ClockSampler:
+    """Samples the SM clock and the clock-event reasons of one GPU through
+    NVML (read-only queries) every few milliseconds on a host thread."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, torch, device, period_s=0.002):
+        self.samples = []
+        self.period = period_s
+        self.max_mhz = None
+        self.ok = False
+        self._stop = threading.Event()
+        self._thread = None
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            prop = torch.cuda.get_device_properties(device)
+            bus = b"%08x:%02x:%02x.0" % (prop.pci_domain_id, prop.pci_bus_id, prop.pci_device_id)
+            h = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(h)) != 0:
+                return
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = int(mx.value)
+            self.nv, self.h = nv, h
+            self.ok = True
+        except Exception:
+            self.ok = False
+
+    def _run(self):
+        clk = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(clk)) == 0:
+                r = 0
+                if self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h, ctypes.byref(rs)) == 0:
+                    r = int(rs.value)
+                self.samples.append((time.perf_counter(), int(clk.value), r))
+            time.sleep(self.period)
+
+    def start(self):
+        if self.ok:
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
+
+    def stop(self):
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join()
+
+    def summary(self, t0=None, t1=None):
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0,
+                    "source": "nvml unavailable"}
+        sel = [s for s in self.samples if (t0 is None or s[0] >= t0) and (t1 is None or s[0] <= t1)]
+        window = "timed region"
+        if not sel:          # region shorter than the sampling period: nearest samples
+            mid = (t0 + t1) / 2 if t0 is not None else self.samples[-1][0]
+            sel = sorted(self.samples, key=lambda s: abs(s[0] - mid))[:3]
+            window = "nearest samples to the timed region"
+        mhz = float(np.median([s[1] for s in sel]))
+        bits = 0
+        for s in sel:
+            bits |= s[2]
+        reasons = [name for bit, name in self.REASONS.items() if bits & bit]
+        return {"sm_mhz": mhz, "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples": len(sel), "source": "nvml, " + window}
+
+
+# ----------------------------------------------------------------------------
+# workload
+
+
+class Workload:
+    """Device-resident inputs of the mtp_T4 step (seeded, synthetic)."""
+
+    def __init__(self, torch, device, seed=2):
+        rng = np.random.default_rng(seed)
+        self.T = T_STEP
+        self.gemms = []
+        dev = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a).view(dt)).to(device)
+        self.host = {}
+        for label, K, N in gen.GEMM_SHAPES:
+            Wq, sc = gen.weights(rng, N, K)
+            x = gen.activations(rng, self.T, K)
+            self.host[label] = (x, Wq, sc)
+            self.gemms.append(dict(label=label, K=K, N=N, x=dev(x, np.int16), Wq=dev(Wq, np.int32),
+                                   sc=dev(sc, np.int16),
+                                   y=torch.empty((self.T, N), dtype=torch.bfloat16, device=device),
+                                   bytes=gen.gemm_bytes(self.T, K, N)))
+        V, K = gen.VOCAB, gen.HIDDEN
+        Wq, sc = gen.weights(rng, V, K)
+        x = gen.activations(rng, self.T, K)
+        drafts = rng.integers(0, V, size=N_DRAFT).astype(np.int32)
+        self.host["head"] = (x, Wq, sc, drafts)
+        self.head = dict(V=V, K=K, x=dev(x, np.int16), Wq=dev(Wq, np.int32), sc=dev(sc, np.int16),
+                         drafts=torch.from_numpy(drafts).to(device),
+                         acc=torch.zeros(1, dtype=torch.int32, device=device),
+                         nxt=torch.zeros(1, dtype=torch.int32, device=device),
+                         bytes=gen.lmhead_bytes(V, K, self.T, n_streams=1, n_draft=N_DRAFT))
+        self.bytes_per_step = sum(g["bytes"] for g in self.gemms) + self.head["bytes"]
+        self.launches_per_step = len(self.gemms) + 1
+
+    def step(self, sv, stream, head_events=None):
+        for g in self.gemms:
+            sv.w4a16_gemm(g["x"], g["Wq"], g["sc"], y=g["y"], stream=stream)
+        h = self.head
+        if head_events is not None:
+            head_events[0].record(stream)
+        sv.lmhead_verify(h["x"], h["Wq"], h["sc"], h["drafts"], accept_len=h["acc"],
+                         next_token=h["nxt"], stream=stream)
+        if head_events is not None:
+            head_events[1].record(stream)
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle timing (the cpu_baseline leg and the reference arm)
+
+
+def oracle_sample_step(oracle, host, rows_frac):
+    """Run the oracle on a bounded sample of one step: the first
+    rows_frac of every GEMM's output rows and of the lm_head rows, with the
+    same x.  Returns (algorithmic bytes of the sample, seconds)."""
+    t0 = time.perf_counter()
+    nbytes = 0
+    for label, K, N in gen.GEMM_SHAPES:
+        x, Wq, sc = host[label]
+        n = max(1, int(N * rows_frac))
+        oracle.w4a16_gemm(x, Wq[:n], sc[:n], T_STEP, K, n)
+        nbytes += gen.gemm_bytes(T_STEP, K, n)
+    x, Wq, sc, drafts = host["head"]
+    V, K = Wq.shape[0], Wq.shape[1] * 8
+    n = max(1, int(V * rows_frac))
+    lg = oracle.lmhead_logits(x, Wq[:n], sc[:n], K, T_STEP, n)
+    a, _, _ = oracle.argmax(lg)
+    oracle.verify(a, drafts)
+    nbytes += gen.lmhead_bytes(n, K, T_STEP, n_streams=1, n_draft=N_DRAFT)
+    return nbytes, time.perf_counter() - t0
+
+
+def host_only_workload(seed=2):
+    rng = np.random.default_rng(seed)
+    host = {}
+    for label, K, N in gen.GEMM_SHAPES:
+        Wq, sc = gen.weights(rng, N, K)
+        x = gen.activations(rng, T_STEP, K)
+        host[label] = (x, Wq, sc)
+    V, K = gen.VOCAB, gen.HIDDEN
+    Wq, sc = gen.weights(rng, V, K)
+    x = gen.activations(rng, T_STEP, K)
+    drafts = rng.integers(0, V, size=N_DRAFT).astype(np.int32)
+    host["head"] = (x, Wq, sc, drafts)
+    return host
+
+
+def cpu_baseline(host, budget_s=12.0):
+    import oracle
+    oracle.build()
+    # size the sample: calibrate on 1% of the rows, then fill the budget
+    nb, dt = oracle_sample_step(oracle, host, 0.01)
+    frac = min(1.0, max(0.01, 0.01 * budget_s / max(dt, 1e-3) / 2))
+    nb, dt = oracle_sample_step(oracle, host, frac)
+    return {"value": nb / dt / 1e9, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": "%.1f%% of the output rows of each of the 3 GEMMs and of the 248,320 "
+                      "lm_head rows (T=4), one pass, %.1f s" % (100 * frac, dt)}
+
+
+# ----------------------------------------------------------------------------
+# arms
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the CPU oracle as it stands, timed on the host cores
+    (rank 0 only), on bounded samples of the same workload."""
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    host = host_only_workload()
+    budget_total = 150.0
+    nb, dt = oracle_sample_step(oracle, host, 0.002)
+    per_step = budget_total / max(1, args.steps + args.warmup)
+    frac = min(1.0, max(0.0005, 0.002 * per_step / max(dt, 1e-4)))
+    for _ in range(args.warmup):
+        oracle_sample_step(oracle, host, frac)
+    tot_b, tot_t = 0, 0.0
+    for _ in range(args.steps):
+        b, t = oracle_sample_step(oracle, host, frac)
+        tot_b += b
+        tot_t += t
+    value = tot_b / tot_t / 1e9
+    sample = ("%.2f%% of the output rows of each GEMM and of the lm_head rows per step (T=4)"
+              % (100 * frac))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * tot_t / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "T": T_STEP, "n_draft": N_DRAFT,
+                       "gemms": [list(s) for s in gen.GEMM_SHAPES], "V": gen.VOCAB,
+                       "K_head": gen.HIDDEN, "l2": "oracle on host cores"},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.num_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import speculative_verify_gb300 as sv
+
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    sv.load()
+    wl = Workload(torch, device)
+    stream = torch.cuda.current_stream(device)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    # warm-up (and the first call's scratch allocation)
+    for _ in range(args.warmup):
+        wl.step(sv, stream)
+    torch.cuda.synchronize()
+    assert sv.last_device_error() == 0
+
+    sampler = ClockSampler(torch, device)
+    sampler.start()
+    # keep the GPU busy ~0.3 s before timing so clocks settle (untimed)
+    t_pre = time.perf_counter()
+    while time.perf_counter() - t_pre < 0.3:
+        wl.step(sv, stream)
+        torch.cuda.synchronize()
+
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    head_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    t_host0 = time.perf_counter()
+    ev0.record(stream)
+    for i in range(args.steps):
+        wl.step(sv, stream, head_events=head_ev[i])
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t_host1 = time.perf_counter()
+    barrier()
+    sampler.stop()
+    ms = ev0.elapsed_time(ev1)
+    head_ms = float(np.mean([a.elapsed_time(b) for a, b in head_ev]))
+    if dist is not None:
+        t = torch.tensor([ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    assert sv.last_device_error() == 0
+
+    # end to end through the public API with host buffers: per step the
+    # activations and drafts go host->device from pinned memory, the verify
+    # result comes back, and the host waits for it (as a decode loop must).
+    pinned_in = []
+    for g in wl.gemms:
+        pinned_in.append((g["x"], g["x"].cpu().pin_memory()))
+    h = wl.head
+    pinned_in.append((h["x"], h["x"].cpu().pin_memory()))
+    pinned_in.append((h["drafts"], h["drafts"].cpu().pin_memory()))
+    out_host = torch.empty(2, dtype=torch.int32).pin_memory()
+    h2d = sum(p.numel() * p.element_size() for _, p in pinned_in)
+    d2h = out_host.numel() * out_host.element_size()
+    e2e_steps = max(1, min(args.steps, 200))
+    barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        for d, p in pinned_in:
+            d.copy_(p, non_blocking=True)
+        wl.step(sv, stream)
+        out_host[0:1].copy_(h["acc"], non_blocking=True)
+        out_host[1:2].copy_(h["nxt"], non_blocking=True)
+        stream.synchronize()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    breakdown = per_kernel_breakdown(torch, sv, device, stream) if args.breakdown else None
+
+    if rank != 0:
+        return
+    peak, peak_kind = measured_peaks()
+    ms_per_step = ms / args.steps
+    value = world * wl.bytes_per_step * args.steps / (ms * 1e-3) / 1e9
+    achieved = wl.head["bytes"] / (head_ms * 1e-3) / 1e9
+    clocks = sampler.summary(t_host0, t_host1)
+    cpu = cpu_baseline(wl.host) if (world == 1 and not args.no_cpu_baseline) else None
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 x int4 -> fp32",
+        "data": "synthetic (seeded; shapes of a 27B-class decoder)",
+        "config": {"workload": WORKLOAD, "T": T_STEP, "n_draft": N_DRAFT,
+                   "gemms": [list(s) for s in gen.GEMM_SHAPES], "V": gen.VOCAB,
+                   "K_head": gen.HIDDEN, "bytes_per_step": wl.bytes_per_step,
+                   "l2": "inputs larger than L2 (820 MB streamed per step; each weight set is "
+                         "evicted by the others before it is read again)",
+                   "parallelism": "replicas" if world > 1 else "1 GPU"},
+        "frac_of_8TBps": value / world / NOMINAL_HBM_GBS,
+        "frac_of_measured_copy": value / world / peak,
+        "roofline": {"kernel": "lmhead_verify (w4a16_stream_kernel<1,true>)", "bound": "hbm",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind
+                     if peak_kind == "measured" else "fallback",
+                     "algorithmic_bytes_per_launch": wl.head["bytes"],
+                     "avg_launch_ms": head_ms,
+                     "traffic": recorded_traffic("lmhead_verify_T4")},
+        "clocks": clocks,
+        "e2e": {"value": wl.bytes_per_step / (e2e_ms * 1e-3) / 1e9 * world, "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms, "steps": e2e_steps},
+        "gpu_launches": wl.launches_per_step * args.steps,
+        "cpu_baseline": cpu,
+    }
+    if breakdown is not None:
+        line["breakdown"] = breakdown
+    print(json.dumps(line), flush=True)
+
+
+def per_kernel_breakdown(torch, sv, device, stream, reps=50):
+    """GB/s of each kernel alone at each T, averaged over back-to-back launches
+    that rotate through enough weight copies to exceed L2 twice."""
+    out = []
+    rng = np.random.default_rng(99)
+    l2 = 129 * 2 ** 20
+    dev = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a).view(dt)).to(device)
+    cases = []
+    for label, K, N in gen.GEMM_SHAPES:
+        for T in (1, 4, 8, 32):
+            cases.append(("gemm", label, K, N, T))
+    for T, S in ((1, 1), (4, 1), (8, 1), (32, 4)):
+        cases.append(("head", "lm_head", gen.HIDDEN, gen.VOCAB, (T, S)))
+    cases.append(("head_map", "restricted", gen.HIDDEN, gen.VOCAB, (4, 1)))
+    for kind, label, K, N, T in cases:
+        if kind == "gemm":
+            wbytes = N * K // 2
+            copies = max(2, int(np.ceil(2 * l2 / wbytes)))
+            Wq, sc = gen.weights(rng, N, K)
+            Ws = [(dev(Wq, np.int32), dev(sc, np.int16)) for _ in range(copies)]
+            x = dev(gen.activations(rng, T, K), np.int16)
+            y = torch.empty((T, N), dtype=torch.bfloat16, device=device)
+            fn = lambda i: sv.w4a16_gemm(x, Ws[i % copies][0], Ws[i % copies][1], y=y, stream=stream)
+            nbytes = gen.gemm_bytes(T, K, N)
+        else:
+            Tt, S = T
+            n_draft = Tt // S - 1
+            Wq, sc = gen.weights(rng, N, K)
+            Ws = [(dev(Wq, np.int32), dev(sc, np.int16)) for _ in range(2)]
+            copies = 2
+            x = dev(gen.activations(rng, Tt, K), np.int16)
+            drafts = torch.zeros((S, n_draft), dtype=torch.int32, device=device)
+            vm = dev(gen.vocab_map(rng, N, gen.DRAFT_VOCAB), np.int32) if kind == "head_map" else None
+            fn = lambda i: sv.lmhead_verify_batched(x, Ws[i % copies][0], Ws[i % copies][1], drafts,
+                                                    vocab_map=vm, stream=stream)
+            n_map = gen.DRAFT_VOCAB if vm is not None else 0
+            nbytes = gen.lmhead_bytes(N, K, Tt, n_map=n_map, n_streams=S, n_draft=n_draft)
+            T = Tt
+        for i in range(5):
+            fn(i)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(reps):
+            fn(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / reps
+        gbs = nbytes / (us * 1e-6) / 1e9
+        out.append({"kernel": kind, "shape": label, "K": K, "N": N, "T": T, "us": round(us, 2),
+                    "GB/s": round(gbs, 1), "frac_8TBps": round(gbs / NOMINAL_HBM_GBS, 3)})
+        del Ws
+        torch.cuda.empty_cache()
+    return out
+
+
+def run_ncu_case(args):
+    """A small, fixed workload for ncu captures: a few launches of one kernel."""
+    import torch
+    import speculative_verify_gb300 as sv
+    sv.load()
+    device = torch.device("cuda", 0)
+    rng = np.random.default_rng(5)
+    dev = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a).view(dt)).to(device)
+    if args.ncu_case == "head":
+        V, K, T = gen.VOCAB, gen.HIDDEN, T_STEP
+        Wq, sc = gen.weights(rng, V, K)
+        Wd, sd = dev(Wq, np.int32), dev(sc, np.int16)
+        x = dev(gen.activations(rng, T, K), np.int16)
+        drafts = torch.zeros(T - 1, dtype=torch.int32, device=device)
+        for _ in range(3):
+            sv.lmhead_verify(x, Wd, sd, drafts)
+    else:
+        label, K, N = gen.GEMM_SHAPES[1]
+        Wq, sc = gen.weights(rng, N, K)
+        Wd, sd = dev(Wq, np.int32), dev(sc, np.int16)
+        x = dev(gen.activations(rng, T_STEP, K), np.int16)
+        for _ in range(3):
+            sv.w4a16_gemm(x, Wd, sd)
+    torch.cuda.synchronize()
+    assert sv.last_device_error() == 0
+    print(json.dumps({"ncu_case": args.ncu_case, "ok": True}))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--breakdown", action="store_true", help="also time each kernel alone at T=1..32")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ncu-case", choices=["head", "gemm"], default=None)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.ncu_case:
+        run_ncu_case(args)
+        return
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    run_ours(args, rank, world, local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,153 @@
+/*
+ * specverify.h -- C ABI of the GB300 (sm_103a) W4A16 weight-read library:
+ * a group-128 dequantizing skinny GEMM and an int4 lm_head pass with fused
+ * greedy speculative verification.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  * All array arguments are DEVICE pointers owned by the caller, 16-byte
+ *    aligned, row-major and densely packed:
+ *      x       [T][K]         bf16 bits (sv_bf16)
+ *      Wq      [rows][K/8]    uint32; column k = 8w + i of a row is nibble i
+ *                             (bits 4i..4i+3) of word w; level = nibble - 8
+ *      scales  [rows][K/128]  bf16 bits, one per row and 128-column group
+ *      y       [T][N]         bf16 bits
+ *    Format source: page "qwen-warp, llamAmpere ..." (ai.satyajit.si),
+ *    section "qwen-warp: keep the activations in bf16": eight nibbles per
+ *    uint32 word along K, one bf16 scale per 128 columns, level = nibble - 8,
+ *    the group scale applied in fp32 after each group's accumulate.
+ *  * K is a multiple of 128; 1 <= T <= 32.
+ *  * Every call is enqueued on `stream` (NULL = the legacy default stream)
+ *    and returns before the GPU has run it.  It performs no host<->device
+ *    copy and no synchronisation.  Results are valid once the stream has
+ *    been synchronised.
+ *  * A call returns SV_OK or a negative status.  On any error nothing is
+ *    launched and no output is touched.
+ *  * The library keeps one small scratch area per device (split-tile fp32
+ *    partial sums, completion counters, the argmax keys; under 6 MB),
+ *    created with cudaMalloc by the first call on that device (so make that
+ *    first call outside CUDA-graph capture) and reused afterwards.  Calls
+ *    on one device must therefore be ordered with respect to each other
+ *    (same stream, or synchronised streams); overlapping calls race on it.
+ *  * Problems found by a kernel at run time (a vocab_map id outside [0, V),
+ *    an internal wait that timed out) never trap: the kernel finishes and
+ *    sets a sticky per-device error word, read with sv_last_device_error.
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t sv_bf16;                  /* raw bf16 bits */
+typedef struct CUstream_st *sv_stream;     /* a cudaStream_t */
+
+enum sv_status {
+    SV_OK = 0,
+    SV_ERR_NULL = -1,    /* a required pointer is NULL                     */
+    SV_ERR_SHAPE = -2,   /* a size is out of range or inconsistent         */
+    SV_ERR_ALIGN = -3,   /* a pointer is not 16-byte aligned               */
+    SV_ERR_CUDA = -4,    /* a CUDA runtime call or the launch failed       */
+    SV_ERR_NOMEM = -5,   /* the per-device scratch area could not be made  */
+    SV_ERR_DEVICE = -6   /* the current device is not sm_103 / sm_100      */
+};
+
+/* Bits of the sticky device error word. */
+#define SV_DEVERR_BAD_MAP_ID  0x1   /* a vocab_map entry outside [0, V) was skipped */
+#define SV_DEVERR_TIMEOUT     0x2   /* a pipeline wait gave up; outputs are invalid */
+
+/*
+ * w4a16_gemm -- y[t][n] = bf16_rne( sum_g float(scales[n][g]) *
+ *                          sum_{k in group g} (q(n,k) - 8) * float(x[t][k]) )
+ * with fp32 products and sums; every packed weight byte and scale is read
+ * from HBM once per call whatever T is ("read once per cycle regardless of
+ * T": page "OpenJet engine", section "How it gets its speed").  Summation
+ * order differs from a sequential loop (groups may be split across thread
+ * blocks and added in a fixed order), so results agree with a sequential
+ * fp32 sum to within fp32 rounding before the final bf16 rounding; they
+ * are deterministic from run to run.
+ *   x [T][K], Wq [N][K/8], scales [N][K/128], y [T][N] (written).
+ *   Errors: SV_ERR_NULL, SV_ERR_SHAPE (T outside 1..32, K < 128 or
+ *   K % 128 != 0, N < 1), SV_ERR_ALIGN, SV_ERR_CUDA, SV_ERR_NOMEM.
+ */
+int w4a16_gemm(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales,
+               int T, int K, int N, sv_bf16 *y, sv_stream stream);
+
+/*
+ * lmhead_verify -- one int4 lm_head pass over the T = 1 + n_draft verify
+ * rows with on-device greedy verification.
+ *   logit[t][v] = sum_g float(scales[v][g]) * sum_{k in g} (q(v,k)-8)*x[t][k]
+ *   in fp32 (never rounded to bf16, never written to memory);
+ *   a[t] = argmax over candidate v of logit[t][v], lowest token id on ties;
+ *   accept_len = first i in [0, n_draft) with drafts[i] != a[i], else n_draft;
+ *   next_token = a[accept_len]  (the model's own token at the first
+ *   disagreement, or the bonus token when every draft was accepted).
+ * Sources: page "qwen-warp, llamAmpere ..." section "What each one calls the
+ * same answer" (greedy acceptance is an argmax equality over the verify
+ * rows); page "swift-qwen3.8-rtx3090" section "Body, heads and drafter"
+ * (drafts are kept up to the first one the model disagrees with); page
+ * "OpenJet engine" section "How it works" (lm_head and verification run on
+ * the device and only the accepted tokens go back to the host).
+ *   Candidates: all rows 0..V-1 when vocab_map == NULL (n_map ignored);
+ *   otherwise rows vocab_map[0..n_map-1] of the V-row head, and every id
+ *   compared or returned is a token id (vocab_map[j]), ties going to the
+ *   lowest token id whatever the map order.  A draft outside the map can
+ *   never match (page "swift-qwen3.8-rtx3090": every miss of the draft
+ *   vocabulary is a rejection).
+ *   x [1+n_draft][K]; Wq [V][K/8]; scales [V][K/128]; drafts [n_draft]
+ *   int32 (may be NULL when n_draft == 0); vocab_map [n_map] int32 or NULL;
+ *   accept_len, next_token: one int32 each (written).
+ *   Errors: SV_ERR_NULL, SV_ERR_SHAPE (n_draft outside 0..31, K as above,
+ *   V < 1, n_map outside 1..V with a map), SV_ERR_ALIGN, SV_ERR_CUDA,
+ *   SV_ERR_NOMEM.
+ */
+int lmhead_verify(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, int K,
+                  const int32_t *drafts, int n_draft,
+                  const int32_t *vocab_map, int n_map, int V,
+                  int32_t *accept_len, int32_t *next_token, sv_stream stream);
+
+/*
+ * lmhead_verify_batched -- n_streams independent verify blocks in ONE pass
+ * over the head (page "qwen-warp, llamAmpere ...", section "What makes each
+ * one a 3090 engine": four sequences with three drafts each share one weight
+ * read).  Block s owns rows s*(1+n_draft) .. s*(1+n_draft)+n_draft of x and
+ * drafts[s][0..n_draft-1]; accept_len[s], next_token[s] as in lmhead_verify.
+ *   Requires n_streams >= 1 and T = n_streams*(1+n_draft) <= 32.
+ */
+int lmhead_verify_batched(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales,
+                          int K, const int32_t *drafts, int n_draft, int n_streams,
+                          const int32_t *vocab_map, int n_map, int V,
+                          int32_t *accept_len, int32_t *next_token, sv_stream stream);
+
+/*
+ * lmhead_argmax -- the same pass without the draft comparison: for each of
+ * the T rows of x, ids[t] = the argmax token id (lowest id on ties) and
+ * vals[t] = its fp32 logit.  This is the greedy step of a restricted draft
+ * head (page "OpenJet engine", section "How it gets its speed": the draft
+ * head scores a fixed id list; page "swift-qwen3.8-rtx3090": the draft head
+ * is the lm_head restricted to the draft vocabulary).
+ *   ids [T] int32, vals [T] float (written).  vals may be NULL.
+ */
+int lmhead_argmax(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, int K,
+                  int T, const int32_t *vocab_map, int n_map, int V,
+                  int32_t *ids, float *vals, sv_stream stream);
+
+/* A static, human-readable name for a status code. */
+const char *sv_status_string(int status);
+
+/*
+ * sv_last_device_error -- *out = the sticky device error word of the
+ * current device (SV_DEVERR_* bits), then clears it.  Synchronises the
+ * device (it reads device memory with a blocking copy).  Returns SV_OK,
+ * SV_ERR_NULL or SV_ERR_CUDA.
+ */
+int sv_last_device_error(int32_t *out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECVERIFY_H */

@@ -72,10 +72,17 @@ def _load():
     lib.or_argmax.argtypes = [_f32p, c_int, c_int, ctypes.c_void_p, _i32p,
                               ctypes.c_void_p, ctypes.c_void_p]
     lib.or_verify.restype = c_int
+    lib.or_num_threads.restype = c_int
+    lib.or_num_threads.argtypes = []
     lib.or_verify.argtypes = [_i32p, ctypes.c_void_p, c_int, ctypes.POINTER(ctypes.c_int32),
                               ctypes.POINTER(ctypes.c_int32)]
     _lib = lib
     return lib
+
+
+def num_threads() -> int:
+    """Threads the oracle's OpenMP regions use."""
+    return int(_load().or_num_threads())
 
 
 def _ptr(a):

@@ -46,6 +46,7 @@
 #include <stdlib.h>
 #include <string.h>
 #include <math.h>
+#include <omp.h>
 
 #define OR_OK 0
 #define OR_EINVAL (-1)
@@ -263,4 +264,16 @@ int or_verify(const int32_t *a, const int32_t *drafts, int n_draft,
     *accept_len = i;
     *next_token = a[i];
     return OR_OK;
+}
+
+/* Number of threads an OpenMP region of this library uses. */
+int or_num_threads(void)
+{
+    int n = 1;
+#pragma omp parallel
+    {
+#pragma omp single
+        n = omp_get_num_threads();
+    }
+    return n;
 }

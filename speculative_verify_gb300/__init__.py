@@ -1,0 +1,231 @@
+"""Python binding of the C ABI in ``include/specverify.h``.
+
+Argument marshalling only: every step of the GEMM and of the verify runs in
+the sm_103a kernels of ``libspecverify.so``.  Tensors are torch CUDA tensors
+(torch supplies device memory and streams); each call passes their
+``data_ptr()`` and the current CUDA stream through ctypes.  There is no CPU
+fallback: if the library is missing the import of the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+from . import build as _build
+
+SV_OK = 0
+STATUS = {0: "SV_OK", -1: "SV_ERR_NULL", -2: "SV_ERR_SHAPE", -3: "SV_ERR_ALIGN",
+          -4: "SV_ERR_CUDA", -5: "SV_ERR_NOMEM", -6: "SV_ERR_DEVICE"}
+DEVERR_BAD_MAP_ID = 0x1
+DEVERR_TIMEOUT = 0x2
+
+_lib = None
+
+
+class SpecVerifyError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__("%s failed: %s (%d): %s" % (fn, STATUS.get(status, "?"), status,
+                                                     status_string(status)))
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(path: str | None = None):
+    """Load libspecverify.so (building it first only if asked via
+    SPECVERIFY_AUTOBUILD=1) and declare the C signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or _build.LIB_PATH
+    if not os.path.exists(path):
+        if os.environ.get("SPECVERIFY_AUTOBUILD") == "1":
+            _build.build()
+        else:
+            raise RuntimeError("libspecverify.so is not built (%s); run "
+                               "speculative_verify_gb300.build.build() or __graft_entry__.build()" % path)
+    lib = ctypes.CDLL(path)
+    vp, ci = ctypes.c_void_p, ctypes.c_int
+    lib.w4a16_gemm.argtypes = [vp, vp, vp, ci, ci, ci, vp, vp]
+    lib.w4a16_gemm.restype = ci
+    lib.lmhead_verify.argtypes = [vp, vp, vp, ci, vp, ci, vp, ci, ci, vp, vp, vp]
+    lib.lmhead_verify.restype = ci
+    lib.lmhead_verify_batched.argtypes = [vp, vp, vp, ci, vp, ci, ci, vp, ci, ci, vp, vp, vp]
+    lib.lmhead_verify_batched.restype = ci
+    lib.lmhead_argmax.argtypes = [vp, vp, vp, ci, ci, vp, ci, ci, vp, vp, vp]
+    lib.lmhead_argmax.restype = ci
+    lib.sv_status_string.argtypes = [ci]
+    lib.sv_status_string.restype = ctypes.c_char_p
+    lib.sv_last_device_error.argtypes = [ctypes.POINTER(ctypes.c_int32)]
+    lib.sv_last_device_error.restype = ci
+    _lib = lib
+    return lib
+
+
+def header_symbols() -> list[str]:
+    """Every function the public header declares."""
+    hdr = os.path.join(_build.INCLUDE, "specverify.h")
+    text = open(hdr).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)
+
+
+def status_string(status: int) -> str:
+    return load().sv_status_string(int(status)).decode()
+
+
+# --------------------------------------------------------------------------
+# torch-facing wrappers
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _check(fn, rc):
+    if rc != SV_OK:
+        raise SpecVerifyError(fn, rc)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _bits16(t, name):
+    torch = _torch()
+    if t.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
+        raise TypeError("%s must hold bf16 values (bfloat16, or int16/uint16 raw bits)" % name)
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError("%s must be a contiguous CUDA tensor" % name)
+    return t
+
+
+def _words(t, name):
+    torch = _torch()
+    if t.dtype not in (torch.int32, torch.uint32):
+        raise TypeError("%s must be int32/uint32 packed nibble words" % name)
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError("%s must be a contiguous CUDA tensor" % name)
+    return t
+
+
+def _i32(t, name):
+    torch = _torch()
+    if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+        raise TypeError("%s must be a contiguous int32 CUDA tensor" % name)
+    return t
+
+
+def w4a16_gemm(x, Wq, scales, y=None, stream=None):
+    """y[T][N] (bf16) = W4A16 group-128 GEMM of x[T][K] with Wq[N][K/8] and
+    scales[N][K/128]; see ``w4a16_gemm`` in include/specverify.h."""
+    torch = _torch()
+    _bits16(x, "x"), _words(Wq, "Wq"), _bits16(scales, "scales")
+    T, K = x.shape
+    N = Wq.shape[0]
+    if Wq.shape[1] * 8 != K or tuple(scales.shape) != (N, K // 128):
+        raise ValueError("shape mismatch: x %s, Wq %s, scales %s" % (tuple(x.shape), tuple(Wq.shape),
+                                                                      tuple(scales.shape)))
+    if y is None:
+        y = torch.empty((T, N), dtype=torch.bfloat16, device=x.device)
+    _bits16(y, "y")
+    _check("w4a16_gemm", load().w4a16_gemm(_ptr(x), _ptr(Wq), _ptr(scales), T, K, N, _ptr(y),
+                                           _stream(stream)))
+    return y
+
+
+def lmhead_verify_batched(x, Wq, scales, drafts, vocab_map=None, accept_len=None,
+                          next_token=None, stream=None):
+    """One head pass for n_streams verify blocks: drafts is [n_streams][n_draft]
+    int32, x is [n_streams*(1+n_draft)][K].  Returns (accept_len, next_token),
+    int32 CUDA tensors of n_streams entries."""
+    torch = _torch()
+    _bits16(x, "x"), _words(Wq, "Wq"), _bits16(scales, "scales")
+    T, K = x.shape
+    V = Wq.shape[0]
+    if drafts.dim() != 2:
+        raise ValueError("drafts must be [n_streams][n_draft]")
+    S, n_draft = drafts.shape
+    if S * (n_draft + 1) != T:
+        raise ValueError("x must have n_streams * (1 + n_draft) rows")
+    if Wq.shape[1] * 8 != K or tuple(scales.shape) != (V, K // 128):
+        raise ValueError("shape mismatch between x, Wq and scales")
+    if n_draft:
+        _i32(drafts, "drafts")
+    if vocab_map is not None:
+        _i32(vocab_map, "vocab_map")
+    if accept_len is None:
+        accept_len = torch.empty(S, dtype=torch.int32, device=x.device)
+    if next_token is None:
+        next_token = torch.empty(S, dtype=torch.int32, device=x.device)
+    n_map = 0 if vocab_map is None else vocab_map.numel()
+    _check("lmhead_verify_batched", load().lmhead_verify_batched(
+        _ptr(x), _ptr(Wq), _ptr(scales), K, _ptr(drafts) if n_draft else None, n_draft, S,
+        _ptr(vocab_map), n_map, V, _ptr(accept_len), _ptr(next_token), _stream(stream)))
+    return accept_len, next_token
+
+
+def lmhead_verify(x, Wq, scales, drafts, vocab_map=None, accept_len=None, next_token=None,
+                  stream=None):
+    """Greedy verify of one block of 1 + n_draft rows (drafts: [n_draft] int32).
+    Returns (accept_len, next_token) as one-element int32 CUDA tensors."""
+    torch = _torch()
+    _bits16(x, "x"), _words(Wq, "Wq"), _bits16(scales, "scales")
+    T, K = x.shape
+    V = Wq.shape[0]
+    n_draft = drafts.numel()
+    if T != n_draft + 1:
+        raise ValueError("x must have 1 + n_draft rows")
+    if Wq.shape[1] * 8 != K or tuple(scales.shape) != (V, K // 128):
+        raise ValueError("shape mismatch between x, Wq and scales")
+    if n_draft:
+        _i32(drafts, "drafts")
+    if vocab_map is not None:
+        _i32(vocab_map, "vocab_map")
+    if accept_len is None:
+        accept_len = torch.empty(1, dtype=torch.int32, device=x.device)
+    if next_token is None:
+        next_token = torch.empty(1, dtype=torch.int32, device=x.device)
+    n_map = 0 if vocab_map is None else vocab_map.numel()
+    _check("lmhead_verify", load().lmhead_verify(
+        _ptr(x), _ptr(Wq), _ptr(scales), K, _ptr(drafts) if n_draft else None, n_draft,
+        _ptr(vocab_map), n_map, V, _ptr(accept_len), _ptr(next_token), _stream(stream)))
+    return accept_len, next_token
+
+
+def lmhead_argmax(x, Wq, scales, vocab_map=None, ids=None, vals=None, stream=None):
+    """Per-row argmax token id (lowest id on ties) and its fp32 logit."""
+    torch = _torch()
+    _bits16(x, "x"), _words(Wq, "Wq"), _bits16(scales, "scales")
+    T, K = x.shape
+    V = Wq.shape[0]
+    if Wq.shape[1] * 8 != K or tuple(scales.shape) != (V, K // 128):
+        raise ValueError("shape mismatch between x, Wq and scales")
+    if vocab_map is not None:
+        _i32(vocab_map, "vocab_map")
+    if ids is None:
+        ids = torch.empty(T, dtype=torch.int32, device=x.device)
+    if vals is None:
+        vals = torch.empty(T, dtype=torch.float32, device=x.device)
+    n_map = 0 if vocab_map is None else vocab_map.numel()
+    _check("lmhead_argmax", load().lmhead_argmax(
+        _ptr(x), _ptr(Wq), _ptr(scales), K, T, _ptr(vocab_map), n_map, V, _ptr(ids), _ptr(vals),
+        _stream(stream)))
+    return ids, vals
+
+
+def last_device_error() -> int:
+    """The sticky device error word (SV_DEVERR_* bits), cleared by the read."""
+    out = ctypes.c_int32(0)
+    _check("sv_last_device_error", load().sv_last_device_error(ctypes.byref(out)))
+    return int(out.value)

@@ -1,0 +1,291 @@
+// specverify.cu -- the C ABI declared in include/specverify.h: argument
+// checks, the per-device scratch area, launch configuration and dispatch to
+// the sm_103a stream kernel (w4a16_stream.cuh).
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+
+#include "specverify.h"
+#include "w4a16_stream.cuh"
+
+namespace sv {
+namespace {
+
+constexpr int MAX_DEVICES = 64;
+
+struct DeviceState {
+    bool ready = false;
+    int sms = 0;
+    int smem_optin = 0;
+    float *part = nullptr;
+    unsigned *ctr = nullptr;
+    unsigned long long *keys = nullptr;
+    unsigned *done = nullptr;
+    int *err = nullptr;
+};
+
+DeviceState g_state[MAX_DEVICES];
+std::mutex g_mu;
+
+template <int NT, bool HEAD>
+cudaError_t raise_smem_limit(int bytes)
+{
+    return cudaFuncSetAttribute(w4a16_stream_kernel<NT, HEAD>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+// Scratch layout (one cudaMalloc): part [sms][2][PART_FLOATS] fp32, then
+// ctr [sms], keys [TMAX], done, err.  All counters start (and are left) at 0.
+int device_state(DeviceState **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_CUDA;
+    if (dev < 0 || dev >= MAX_DEVICES) return SV_ERR_DEVICE;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState &st = g_state[dev];
+    if (!st.ready) {
+        cudaDeviceProp prop;
+        if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return SV_ERR_CUDA;
+        if (prop.major != 10) return SV_ERR_DEVICE;
+        int optin = 0;
+        if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            return SV_ERR_CUDA;
+        const size_t part_bytes = static_cast<size_t>(prop.multiProcessorCount) * 2 * PART_FLOATS * sizeof(float);
+        const size_t ctr_bytes = static_cast<size_t>(prop.multiProcessorCount) * sizeof(unsigned);
+        const size_t keys_bytes = TMAX * sizeof(unsigned long long);
+        const size_t total = part_bytes + ctr_bytes + keys_bytes + 2 * sizeof(unsigned) + 256;
+        uint8_t *base = nullptr;
+        if (cudaMalloc(&base, total) != cudaSuccess) {
+            cudaGetLastError();
+            return SV_ERR_NOMEM;
+        }
+        if (cudaMemset(base, 0, total) != cudaSuccess) {
+            cudaFree(base);
+            return SV_ERR_CUDA;
+        }
+        size_t off = 0;
+        st.part = reinterpret_cast<float *>(base + off);
+        off += part_bytes;
+        off = (off + 255) & ~static_cast<size_t>(255);
+        st.keys = reinterpret_cast<unsigned long long *>(base + off);
+        off += keys_bytes;
+        st.ctr = reinterpret_cast<unsigned *>(base + off);
+        off += ctr_bytes;
+        st.done = reinterpret_cast<unsigned *>(base + off);
+        off += sizeof(unsigned);
+        st.err = reinterpret_cast<int *>(base + off);
+        cudaError_t e = cudaSuccess;
+        e = e != cudaSuccess ? e : raise_smem_limit<1, false>(optin);
+        e = e != cudaSuccess ? e : raise_smem_limit<2, false>(optin);
+        e = e != cudaSuccess ? e : raise_smem_limit<4, false>(optin);
+        e = e != cudaSuccess ? e : raise_smem_limit<1, true>(optin);
+        e = e != cudaSuccess ? e : raise_smem_limit<2, true>(optin);
+        e = e != cudaSuccess ? e : raise_smem_limit<4, true>(optin);
+        if (e != cudaSuccess) {
+            cudaFree(base);
+            return SV_ERR_CUDA;
+        }
+        st.sms = prop.multiProcessorCount;
+        st.smem_optin = optin;
+        st.ready = true;
+    }
+    *out = &st;
+    return SV_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+template <int NT>
+struct Layout {
+    int stage_bytes;
+    int fixed_bytes;
+};
+
+template <int NT>
+Layout<NT> layout_for(int T)
+{
+    using C = Cfg<NT>;
+    Layout<NT> l;
+    l.stage_bytes = (ROWS * C::WSTR + T * C::XSTR + 127) & ~127;
+    l.fixed_bytes = C::RED_FLOATS * 4 + TMAX * 8 + 16;   // + 16 bytes of barriers per stage
+    return l;
+}
+
+template <int NT, bool HEAD>
+int launch(Params p, const DeviceState &st, cudaStream_t stream)
+{
+    const Layout<NT> l = layout_for<NT>(p.T);
+    int nst = (st.smem_optin - l.fixed_bytes) / (l.stage_bytes + 16);
+    if (nst > 6) nst = 6;
+    if (nst < 2) return SV_ERR_SHAPE;
+    p.nst = nst;
+    p.stage_bytes = l.stage_bytes;
+    const int smem = nst * l.stage_bytes + l.fixed_bytes + nst * 16;
+    long long B = st.sms;
+    if (B > p.U) B = p.U;
+    p.part = st.part;
+    p.ctr = st.ctr;
+    p.keys = st.keys;
+    p.done = st.done;
+    p.err = st.err;
+    w4a16_stream_kernel<NT, HEAD><<<static_cast<unsigned>(B), NTHREADS, smem, stream>>>(p);
+    return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+template <bool HEAD>
+int dispatch(Params &p, const DeviceState &st, cudaStream_t stream)
+{
+    if (p.T <= 8) return launch<1, HEAD>(p, st, stream);
+    if (p.T <= 16) return launch<2, HEAD>(p, st, stream);
+    return launch<4, HEAD>(p, st, stream);
+}
+
+int check_common(const void *x, const void *Wq, const void *scales, int T, int K)
+{
+    if (!x || !Wq || !scales) return SV_ERR_NULL;
+    if (T < 1 || T > TMAX || K < 128 || (K % 128) != 0) return SV_ERR_SHAPE;
+    if (!aligned16(x) || !aligned16(Wq) || !aligned16(scales)) return SV_ERR_ALIGN;
+    return SV_OK;
+}
+
+int head_call(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, int K, int T,
+              const int32_t *vocab_map, int n_map, int V, int mode, const int32_t *drafts,
+              int n_draft, int n_streams, int32_t *accept_len, int32_t *next_token,
+              int32_t *ids, float *vals, cudaStream_t stream)
+{
+    int rc = check_common(x, Wq, scales, T, K);
+    if (rc != SV_OK) return rc;
+    if (V < 1) return SV_ERR_SHAPE;
+    if (vocab_map) {
+        if (n_map < 1 || n_map > V) return SV_ERR_SHAPE;
+        if (!aligned4(vocab_map)) return SV_ERR_ALIGN;
+    }
+    if (mode == 0) {
+        if (!accept_len || !next_token) return SV_ERR_NULL;
+        if (n_draft > 0 && !drafts) return SV_ERR_NULL;
+        if ((drafts && !aligned4(drafts)) || !aligned4(accept_len) || !aligned4(next_token))
+            return SV_ERR_ALIGN;
+    } else {
+        if (!ids) return SV_ERR_NULL;
+        if (!aligned4(ids) || (vals && !aligned4(vals))) return SV_ERR_ALIGN;
+    }
+    DeviceState *st = nullptr;
+    rc = device_state(&st);
+    if (rc != SV_OK) return rc;
+    Params p{};
+    p.x = x;
+    p.Wq = Wq;
+    p.scales = scales;
+    p.map = vocab_map;
+    p.T = T;
+    p.K = K;
+    p.G = K / 128;
+    p.n_rows = vocab_map ? n_map : V;
+    p.V = V;
+    const long long tiles = (static_cast<long long>(p.n_rows) + ROWS - 1) / ROWS;
+    p.U = tiles * p.G;
+    p.mode = mode;
+    p.drafts = drafts;
+    p.n_draft = n_draft;
+    p.n_streams = n_streams;
+    p.accept_len = accept_len;
+    p.next_token = next_token;
+    p.ids = ids;
+    p.vals = vals;
+    return dispatch<true>(p, *st, stream);
+}
+
+}  // namespace
+}  // namespace sv
+
+extern "C" {
+
+int w4a16_gemm(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, int T, int K, int N,
+               sv_bf16 *y, sv_stream stream)
+{
+    using namespace sv;
+    int rc = check_common(x, Wq, scales, T, K);
+    if (rc != SV_OK) return rc;
+    if (!y) return SV_ERR_NULL;
+    if (N < 1) return SV_ERR_SHAPE;
+    if (!aligned16(y)) return SV_ERR_ALIGN;
+    DeviceState *st = nullptr;
+    rc = device_state(&st);
+    if (rc != SV_OK) return rc;
+    Params p{};
+    p.x = x;
+    p.Wq = Wq;
+    p.scales = scales;
+    p.T = T;
+    p.K = K;
+    p.G = K / 128;
+    p.n_rows = N;
+    p.V = N;
+    const long long tiles = (static_cast<long long>(N) + ROWS - 1) / ROWS;
+    p.U = tiles * p.G;
+    p.y = y;
+    return dispatch<false>(p, *st, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int lmhead_verify_batched(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, int K,
+                          const int32_t *drafts, int n_draft, int n_streams,
+                          const int32_t *vocab_map, int n_map, int V, int32_t *accept_len,
+                          int32_t *next_token, sv_stream stream)
+{
+    if (n_draft < 0 || n_draft > 31 || n_streams < 1) return SV_ERR_SHAPE;
+    const long long T = static_cast<long long>(n_streams) * (n_draft + 1);
+    if (T > sv::TMAX) return SV_ERR_SHAPE;
+    return sv::head_call(x, Wq, scales, K, static_cast<int>(T), vocab_map, n_map, V, 0, drafts,
+                         n_draft, n_streams, accept_len, next_token, nullptr, nullptr,
+                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+int lmhead_verify(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, int K,
+                  const int32_t *drafts, int n_draft, const int32_t *vocab_map, int n_map, int V,
+                  int32_t *accept_len, int32_t *next_token, sv_stream stream)
+{
+    return lmhead_verify_batched(x, Wq, scales, K, drafts, n_draft, 1, vocab_map, n_map, V,
+                                 accept_len, next_token, stream);
+}
+
+int lmhead_argmax(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, int K, int T,
+                  const int32_t *vocab_map, int n_map, int V, int32_t *ids, float *vals,
+                  sv_stream stream)
+{
+    return sv::head_call(x, Wq, scales, K, T, vocab_map, n_map, V, 1, nullptr, 0, 0, nullptr,
+                         nullptr, ids, vals, reinterpret_cast<cudaStream_t>(stream));
+}
+
+const char *sv_status_string(int status)
+{
+    switch (status) {
+    case SV_OK: return "ok";
+    case SV_ERR_NULL: return "a required pointer is NULL";
+    case SV_ERR_SHAPE: return "a size is out of range or inconsistent";
+    case SV_ERR_ALIGN: return "a pointer is not suitably aligned";
+    case SV_ERR_CUDA: return "a CUDA call or kernel launch failed";
+    case SV_ERR_NOMEM: return "the per-device scratch area could not be allocated";
+    case SV_ERR_DEVICE: return "the current device is not a compute capability 10.x GPU";
+    default: return "unknown status";
+    }
+}
+
+int sv_last_device_error(int32_t *out)
+{
+    using namespace sv;
+    if (!out) return SV_ERR_NULL;
+    DeviceState *st = nullptr;
+    int rc = device_state(&st);
+    if (rc != SV_OK) return rc;
+    int v = 0;
+    if (cudaMemcpy(&v, st->err, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return SV_ERR_CUDA;
+    if (cudaMemset(st->err, 0, sizeof v) != cudaSuccess) return SV_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return SV_ERR_CUDA;
+    *out = v;
+    return SV_OK;
+}
+
+}  // extern "C"

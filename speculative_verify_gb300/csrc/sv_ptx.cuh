@@ -1,0 +1,192 @@
+// sv_ptx.cuh -- thin inline-PTX wrappers used by the sm_103a kernels:
+// mbarriers, 1-D bulk (TMA) copies global -> shared, L2 cache policies,
+// the bf16 tensor-core MMA and the int4 -> bf16x2 dequantisation.
+#pragma once
+
+#include <cstdint>
+
+namespace sv {
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------- mbarrier
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// Make barrier initialisation visible to the async (bulk-copy) proxy.
+__device__ __forceinline__ void fence_barrier_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;"
+                 ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for the phase with the given parity to complete, giving up after
+// `limit_ns` nanoseconds.  Returns false on time-out; the caller records the
+// error and carries on, so no thread ever waits without bound.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// ---------------------------------------------------------------- L2 policies
+
+__device__ __forceinline__ uint64_t policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_last()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// ---------------------------------------------------------------- bulk copy
+
+// 1-D bulk copy of `bytes` (multiple of 16; both addresses 16-byte aligned)
+// from global memory into this CTA's shared memory, completing on `bar`.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                         uint32_t bar, uint64_t policy)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+                 " [%0], [%1], %2, [%3], %4;"
+                 ::"r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(policy) : "memory");
+}
+
+// ---------------------------------------------------------------- named barriers
+
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ---------------------------------------------------------------- shared loads
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
+// ---------------------------------------------------------------- global loads
+
+__device__ __forceinline__ uint16_t ldg_u16(const uint16_t *p)
+{
+    uint16_t v;
+    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t h)
+{
+    return __uint_as_float(static_cast<uint32_t>(h) << 16);
+}
+
+// ---------------------------------------------------------------- dequant
+
+// Two nibbles -> two bf16 levels.  v holds nibble a in bits 0..3 and nibble
+// b in bits 16..19 (other bits ignored).  OR-ing a nibble into the mantissa
+// of bf16 128.0 (0x4300, where the bf16 spacing is exactly 1) gives 128 + n;
+// one packed fma with 1.0 and -136.0 gives n - 8 exactly.  Result: low half
+// = level(a), high half = level(b).
+__device__ __forceinline__ uint32_t dequant2(uint32_t v)
+{
+    uint32_t q, r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(q) : "r"(v), "r"(0x000F000Fu), "r"(0x43004300u));
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(q), "r"(0x3F803F80u), "r"(0xC308C308u));
+    return r;
+}
+
+// ---------------------------------------------------------------- tensor core
+
+// D (16x8 fp32) += A (16x16 bf16, row) * B (16x8 bf16, col).
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0,
+                                               uint32_t b1)
+{
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+                 "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// ---------------------------------------------------------------- argmax keys
+
+// 64-bit key that orders (value, token id) by value, then by LOWER id:
+// high word = order-preserving map of the fp32 bits (-0 folded onto +0, NaN
+// below everything), low word = 0xFFFFFFFF - id.  Key 0 means "no candidate".
+__device__ __forceinline__ unsigned long long make_key(float v, uint32_t id)
+{
+    uint32_t u = __float_as_uint(v);
+    if (v == 0.0f) u = 0u;
+    uint32_t o = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    if (v != v) o = 0u;
+    return (static_cast<unsigned long long>(o) << 32) |
+           static_cast<unsigned long long>(0xFFFFFFFFu - id);
+}
+
+__device__ __forceinline__ float key_value(unsigned long long k)
+{
+    uint32_t o = static_cast<uint32_t>(k >> 32);
+    uint32_t u = (o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o;
+    return __uint_as_float(u);
+}
+
+__device__ __forceinline__ int32_t key_id(unsigned long long k)
+{
+    return static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(k & 0xFFFFFFFFull));
+}
+
+__device__ __forceinline__ unsigned long long shfl_xor_u64(unsigned long long v, int m)
+{
+    uint32_t lo = static_cast<uint32_t>(v), hi = static_cast<uint32_t>(v >> 32);
+    lo = __shfl_xor_sync(0xFFFFFFFFu, lo, m);
+    hi = __shfl_xor_sync(0xFFFFFFFFu, hi, m);
+    return (static_cast<unsigned long long>(hi) << 32) | lo;
+}
+
+}  // namespace sv

@@ -1,0 +1,111 @@
+"""The C ABI without a GPU: the library builds for sm_103a, loads, exports
+every function the header declares, and rejects bad arguments with the
+documented status before touching CUDA."""
+import ctypes
+
+import pytest
+
+import speculative_verify_gb300 as sv
+from speculative_verify_gb300 import build as svbuild
+
+
+@pytest.fixture(scope="module")
+def lib():
+    svbuild.build()
+    return sv.load()
+
+
+def _has_gpu():
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:
+        return False
+
+
+def test_library_exports_every_header_symbol(lib):
+    names = sv.header_symbols()
+    assert set(names) >= {"w4a16_gemm", "lmhead_verify", "lmhead_verify_batched",
+                          "lmhead_argmax", "sv_status_string", "sv_last_device_error"}
+    for name in names:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code, name in sv.STATUS.items():
+        s = sv.status_string(code)
+        assert isinstance(s, str) and s
+    assert sv.status_string(12345) == "unknown status"
+
+
+def test_binding_has_same_names_as_abi():
+    for name in ("w4a16_gemm", "lmhead_verify", "lmhead_verify_batched", "lmhead_argmax"):
+        assert callable(getattr(sv, name))
+
+
+# Fake, never-dereferenced addresses.  Every call below must fail argument
+# checking before any CUDA call; skipped where a GPU is present so that a
+# checking bug could never turn into a launch on fake pointers.
+A = ctypes.c_void_p(0x10000)          # 16-byte aligned
+A2 = ctypes.c_void_p(0x20000)
+A3 = ctypes.c_void_p(0x30000)
+MIS = ctypes.c_void_p(0x10008)        # 8-byte aligned only
+NUL = None
+
+nogpu = pytest.mark.skipif(_has_gpu(), reason="fake-pointer checks run only where no GPU exists")
+
+
+@nogpu
+@pytest.mark.parametrize("args,code", [
+    ((NUL, A, A2, 1, 512, 64, A3, None), -1),
+    ((A, NUL, A2, 1, 512, 64, A3, None), -1),
+    ((A, A, NUL, 1, 512, 64, A3, None), -1),
+    ((A, A2, A3, 1, 512, 64, NUL, None), -1),
+    ((A, A2, A3, 0, 512, 64, A, None), -2),
+    ((A, A2, A3, 33, 512, 64, A, None), -2),
+    ((A, A2, A3, 1, 500, 64, A, None), -2),
+    ((A, A2, A3, 1, 0, 64, A, None), -2),
+    ((A, A2, A3, 1, 512, 0, A, None), -2),
+    ((MIS, A2, A3, 1, 512, 64, A, None), -3),
+    ((A, MIS, A3, 1, 512, 64, A, None), -3),
+    ((A, A2, A3, 1, 512, 64, MIS, None), -3),
+])
+def test_gemm_rejects_bad_arguments(lib, args, code):
+    assert lib.w4a16_gemm(*args) == code
+
+
+@nogpu
+@pytest.mark.parametrize("kw,code", [
+    (dict(n_draft=32), -2),
+    (dict(n_draft=-1), -2),
+    (dict(n_streams=0), -2),
+    (dict(n_streams=9, n_draft=3), -2),         # T = 36 > 32
+    (dict(V=0), -2),
+    (dict(vmap=A, n_map=0), -2),
+    (dict(vmap=A, n_map=5000, V=4096), -2),
+    (dict(drafts=NUL), -1),
+    (dict(acc=NUL), -1),
+    (dict(nxt=NUL), -1),
+    (dict(K=100), -2),
+    (dict(x=MIS), -3),
+    (dict(vmap=ctypes.c_void_p(0x10002), n_map=10), -3),
+])
+def test_verify_rejects_bad_arguments(lib, kw, code):
+    a = dict(x=A, W=A2, s=A3, K=512, drafts=A, n_draft=3, n_streams=1, vmap=NUL, n_map=0,
+             V=4096, acc=A, nxt=A2)
+    a.update(kw)
+    rc = lib.lmhead_verify_batched(a["x"], a["W"], a["s"], a["K"], a["drafts"], a["n_draft"],
+                                   a["n_streams"], a["vmap"], a["n_map"], a["V"], a["acc"],
+                                   a["nxt"], None)
+    assert rc == code
+
+
+@nogpu
+def test_argmax_rejects_bad_arguments(lib):
+    assert lib.lmhead_argmax(A, A2, A3, 512, 4, NUL, 0, 4096, NUL, NUL, None) == -1
+    assert lib.lmhead_argmax(A, A2, A3, 512, 40, NUL, 0, 4096, A, NUL, None) == -2
+    assert lib.lmhead_argmax(A, A2, A3, 512, 4, NUL, 0, 4096, ctypes.c_void_p(0x10001), NUL, None) == -3
+
+
+def test_last_device_error_rejects_null(lib):
+    assert lib.sv_last_device_error(None) == -1

@@ -1,0 +1,335 @@
+"""GPU parity: the sm_103a kernels, called through the C ABI, against the CPU
+oracle on the same seeded inputs.
+
+Tolerances.  GEMM: |y_gpu - y_oracle| <= 1e-2 * max_n |y_oracle[t][n]| for
+every row t (the bound the build is specified to), and the tighter
+|y_gpu - y32| <= 2^-8 |y32| + 1e-5 * max|row| (bf16 rounding of the same fp32
+sum, plus fp32 reordering).  Verify: argmax ids, accept_len and next_token are
+bit-exact wherever the oracle's top-1 fp32 margin of the deciding rows exceeds
+1e-3; rows with a smaller margin are logged and only checked for validity.
+"""
+import numpy as np
+import pytest
+
+import gen
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+MARGIN = 1e-3
+
+
+@pytest.fixture(scope="module")
+def sv():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import speculative_verify_gb300 as m
+    from speculative_verify_gb300 import build
+    build.build()
+    m.load()
+    assert m.last_device_error() == 0
+    return m
+
+
+def dev_bits16(a):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
+
+
+def dev_words(a):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int32)).cuda()
+
+
+def dev_i32(a):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+
+
+def to_f32(t_bf16):
+    return gen.bf16_bits_to_f32(t_bf16.view(torch.int16).cpu().numpy().view(np.uint16))
+
+
+def assert_gemm_close(y_gpu_bits, y32):
+    yg = gen.bf16_bits_to_f32(y_gpu_bits).astype(np.float64)
+    y32 = y32.astype(np.float64)
+    rowmax = np.abs(y32).max(axis=1, keepdims=True)
+    err = np.abs(yg - y32)
+    assert np.all(err <= 1e-2 * rowmax), "north-star tolerance violated: max rel %.3g" % (
+        (err / np.maximum(rowmax, 1e-30)).max())
+    assert np.all(err <= 2.0 ** -8 * np.abs(y32) + 1e-5 * rowmax)
+
+
+# --------------------------------------------------------------------------
+# dequantisation and layout on the GPU
+
+
+def test_gpu_one_hot_pins_nibble_order_and_page_constant(sv, oracle):
+    """Every nibble value in every position of a word, through the GPU GEMM:
+    x = e_k gives y[n] = (nibble - 8) * s exactly (page: 0x4300 | n is 128+n,
+    minus 136 is n - 8, all sixteen exact)."""
+    K, N = 256, 18
+    W = K // 8
+    Wq = np.empty((N, W), np.uint32)
+    lv = np.empty((N, K), np.int64)
+    for n in range(16):                          # rows 0..15: every nibble = n
+        Wq[n, :] = int(("%x" % n) * 8, 16)
+        lv[n, :] = n - 8
+    Wq[16, :] = 0xFEDCBA98
+    lv[16, :] = np.tile(np.arange(8), W)
+    Wq[17, :] = 0x76543210
+    lv[17, :] = np.tile(np.arange(8) - 8, W)
+    s = gen.f32_to_bf16_bits(np.array([[2.0 ** -(n % 5), 2.0 ** (n % 3)] for n in range(N)], np.float32))
+    sval = gen.bf16_bits_to_f32(s).astype(np.float64)
+    one = gen.f32_to_bf16_bits(np.float32(1.0))
+    for k0 in range(0, K, 32):
+        x = np.zeros((32, K), np.uint16)
+        x[np.arange(32), k0 + np.arange(32)] = one
+        y = sv.w4a16_gemm(dev_bits16(x), dev_words(Wq), dev_bits16(s))
+        torch.cuda.synchronize()
+        got = to_f32(y).astype(np.float64)
+        ks = k0 + np.arange(32)
+        expect = (lv[:, ks] * sval[:, ks // 128]).T
+        assert np.array_equal(got, expect)
+
+
+# --------------------------------------------------------------------------
+# GEMM parity
+
+
+@pytest.mark.parametrize("T,K,N", [
+    (1, 512, 1024),      # the tiny configuration
+    (1, 128, 1),
+    (2, 128, 64),
+    (3, 1152, 1000),     # ragged last tile, 9 groups
+    (4, 5120, 200),
+    (8, 2048, 777),
+    (9, 640, 130),       # two n8 token tiles
+    (13, 1280, 321),
+    (16, 384, 64),
+    (32, 1280, 321),     # four n8 token tiles
+    (32, 17408, 70),
+])
+def test_gemm_matches_oracle(sv, oracle, T, K, N):
+    rng = np.random.default_rng(7000 + 31 * T + K + N)
+    Wq, sc = gen.weights(rng, N, K)
+    x = gen.activations(rng, T, K)
+    y32, ybf = oracle.w4a16_gemm(x, Wq, sc, T, K, N)
+    y = sv.w4a16_gemm(dev_bits16(x), dev_words(Wq), dev_bits16(sc))
+    torch.cuda.synchronize()
+    yg = y.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert_gemm_close(yg, y32)
+    # same call again: identical bits (fixed reduction order)
+    y2 = sv.w4a16_gemm(dev_bits16(x), dev_words(Wq), dev_bits16(sc))
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("T", [1, 4, 8, 32])
+@pytest.mark.parametrize("label,K,N", gen.GEMM_SHAPES)
+def test_gemm_full_size_sampled_rows(sv, oracle, label, K, N, T):
+    """Full decode shapes in the launch configuration the benchmark times; the
+    oracle recomputes 640 sampled output rows (and the last tile)."""
+    rng = np.random.default_rng({"qkv": 1, "gate_up": 2, "down": 3}[label] * 100 + T)
+    Wq, sc = gen.weights(rng, N, K)
+    x = gen.activations(rng, T, K)
+    y = sv.w4a16_gemm(dev_bits16(x), dev_words(Wq), dev_bits16(sc))
+    torch.cuda.synchronize()
+    yg = y.view(torch.int16).cpu().numpy().view(np.uint16)
+    rows = np.unique(np.concatenate([rng.choice(N, 576, replace=False), np.arange(N - 64, N)]))
+    y32, _ = oracle.w4a16_gemm(x, Wq[rows], sc[rows], T, K, rows.size)
+    assert_gemm_close(yg[:, rows], y32)
+    assert sv.last_device_error() == 0
+
+
+# --------------------------------------------------------------------------
+# lm_head verify parity
+
+
+def check_verify(res, acc_gpu, nxt_gpu, a_gpu, n_draft, n_streams, vm=None):
+    """Bit-exact where the deciding rows have margin > 1e-3; else log and check
+    that the GPU's choice is one of the near-tied candidates."""
+    rows_per = n_draft + 1
+    acc_gpu = np.asarray(acc_gpu)
+    nxt_gpu = np.asarray(nxt_gpu)
+    for s in range(n_streams):
+        acc = int(res.accept_len[s])
+        deciding = range(s * rows_per, s * rows_per + acc + 1)
+        if all(res.margin[t] > MARGIN for t in deciding):
+            assert int(acc_gpu[s]) == acc, (s, int(acc_gpu[s]), acc)
+            assert int(nxt_gpu[s]) == int(res.next_token[s])
+        else:
+            print("stream %d: near-tie among deciding rows, margins %s" % (
+                s, [float(res.margin[t]) for t in deciding]))
+    if a_gpu is not None:
+        for t in range(len(res.a)):
+            if res.margin[t] > MARGIN:
+                assert int(a_gpu[t]) == int(res.a[t]), (t, int(a_gpu[t]), int(res.a[t]))
+            else:
+                lgt = res.logits[t]
+                ids = np.arange(lgt.size) if vm is None else vm
+                j = np.where(ids == int(a_gpu[t]))[0]
+                assert j.size == 1 and lgt[j[0]] >= lgt.max() - MARGIN
+
+
+def run_head_case(sv, oracle, seed, V, K, n_draft, n_streams=1, n_map=0, mismatch=None):
+    rng = np.random.default_rng(seed)
+    Wq, sc = gen.weights(rng, V, K)
+    T = n_streams * (n_draft + 1)
+    x = gen.activations(rng, T, K)
+    vm = gen.vocab_map(rng, V, n_map) if n_map else None
+    logits = oracle.lmhead_logits(x, Wq, sc, K, T, V, rows=vm)
+    a, best, second = oracle.argmax(logits, ids=vm)
+    drafts = np.zeros((n_streams, n_draft), np.int32)
+    for s in range(n_streams):
+        p = int(rng.integers(0, n_draft + 1)) if mismatch is None else mismatch[s]
+        drafts[s] = gen.drafts_with_mismatch(rng, a[s * (n_draft + 1):(s + 1) * (n_draft + 1)], p, V,
+                                             pool=vm)
+    res = oracle.lmhead_verify(x, Wq, sc, K, V, drafts, n_streams=n_streams, vocab_map=vm)
+    dx, dW, ds = dev_bits16(x), dev_words(Wq), dev_bits16(sc)
+    dvm = None if vm is None else dev_i32(vm)
+    if n_streams == 1:
+        acc, nxt = sv.lmhead_verify(dx, dW, ds, dev_i32(drafts[0]), vocab_map=dvm)
+    else:
+        acc, nxt = sv.lmhead_verify_batched(dx, dW, ds, dev_i32(drafts), vocab_map=dvm)
+    ids, vals = sv.lmhead_argmax(dx, dW, ds, vocab_map=dvm)
+    torch.cuda.synchronize()
+    ids = ids.cpu().numpy()
+    vals = vals.cpu().numpy()
+    check_verify(res, acc.cpu().numpy(), nxt.cpu().numpy(), ids, n_draft, n_streams, vm)
+    # argmax values: the fp32 logit of the chosen id, within fp32 reordering
+    lim = 1e-4 * np.abs(res.logits).max()
+    for t in range(T):
+        ids_all = np.arange(res.logits.shape[1]) if vm is None else vm
+        j = np.where(ids_all == ids[t])[0][0]
+        assert abs(float(vals[t]) - float(res.logits[t, j])) <= lim
+    assert sv.last_device_error() == 0
+    return res, acc.cpu().numpy(), nxt.cpu().numpy()
+
+
+def test_verify_tiny_configuration(sv, oracle):
+    """V=4096, K=512, drafts = oracle argmax of rows 0 and 1, then a different
+    token: accept_len 2, next_token = argmax of row 2."""
+    rng = np.random.default_rng(0)
+    V, K, n_draft = 4096, 512, 3
+    Wq, sc = gen.weights(rng, V, K)
+    x = gen.activations(rng, n_draft + 1, K)
+    lg = oracle.lmhead_logits(x, Wq, sc, K, n_draft + 1, V)
+    a, _, _ = oracle.argmax(lg)
+    drafts = np.array([a[0], a[1], gen.token_not(rng, V, int(a[2]))], np.int32)
+    res = oracle.lmhead_verify(x, Wq, sc, K, V, drafts)
+    assert res.accept_len[0] == 2 and res.next_token[0] == a[2]
+    acc, nxt = sv.lmhead_verify(dev_bits16(x), dev_words(Wq), dev_bits16(sc), dev_i32(drafts))
+    torch.cuda.synchronize()
+    check_verify(res, acc.cpu().numpy(), nxt.cpu().numpy(), None, n_draft, 1)
+
+
+@pytest.mark.parametrize("V,K,n_draft,n_streams,n_map", [
+    (4096, 512, 3, 1, 0),
+    (1000, 640, 0, 1, 0),        # plain greedy, ragged vocabulary
+    (777, 128, 7, 1, 0),
+    (3000, 1024, 7, 4, 0),       # 4 streams x 8 rows = 32
+    (2500, 1152, 2, 3, 0),
+    (5000, 768, 3, 1, 1234),     # restricted
+    (5000, 768, 0, 1, 1),        # single-entry map
+    (6000, 512, 3, 2, 4000),
+])
+def test_verify_matches_oracle(sv, oracle, V, K, n_draft, n_streams, n_map):
+    run_head_case(sv, oracle, 900 + V + K + n_draft, V, K, n_draft, n_streams, n_map)
+
+
+def test_identity_map_equals_full_head_and_map_order_is_irrelevant(sv, oracle):
+    """An identity map is the full head bit for bit (same rows in the same
+    positions); a permuted map gives the same ids wherever the oracle margin
+    exceeds 1e-3 (a permutation moves rows between tiles, which may change
+    the fp32 summation order of a row, not its value beyond rounding)."""
+    rng = np.random.default_rng(31)
+    V, K, T = 3000, 512, 4
+    Wq, sc = gen.weights(rng, V, K)
+    x = gen.activations(rng, T, K)
+    dx, dW, ds = dev_bits16(x), dev_words(Wq), dev_bits16(sc)
+    ids_full, vals_full = sv.lmhead_argmax(dx, dW, ds)
+    ids_id, vals_id = sv.lmhead_argmax(dx, dW, ds, vocab_map=dev_i32(np.arange(V)))
+    perm = rng.permutation(V).astype(np.int32)
+    ids_p, vals_p = sv.lmhead_argmax(dx, dW, ds, vocab_map=dev_i32(perm))
+    torch.cuda.synchronize()
+    assert torch.equal(ids_full, ids_id) and torch.equal(vals_full, vals_id)
+    lg = oracle.lmhead_logits(x, Wq, sc, K, T, V)
+    a, best, second = oracle.argmax(lg)
+    for t in range(T):
+        if best[t] - second[t] > MARGIN:
+            assert int(ids_p[t]) == int(a[t]) == int(ids_full[t])
+    assert np.allclose(vals_p.cpu().numpy(), vals_full.cpu().numpy(), rtol=0, atol=1e-4 * np.abs(lg).max())
+    one = dev_i32(np.array([1234]))
+    ids_1, _ = sv.lmhead_argmax(dx, dW, ds, vocab_map=one)
+    torch.cuda.synchronize()
+    assert ids_1.cpu().tolist() == [1234] * T
+
+
+def test_exact_tie_goes_to_lowest_id(sv, oracle):
+    """Copies of the best row placed in the same 64-row tile (where every row
+    is summed in the same order, so the tie is exact on the GPU too): the
+    lowest id of the tied set wins, over the full head and over a map that
+    lists the tied ids highest first."""
+    rng = np.random.default_rng(32)
+    V, K = 2000, 512
+    Wq, sc = gen.weights(rng, V, K)
+    x = gen.activations(rng, 1, K)
+    a0 = int(oracle.argmax(oracle.lmhead_logits(x, Wq, sc, K, 1, V))[0][0])
+    base = (a0 // 64) * 64
+    tied = sorted({base, min(V - 1, base + 63), a0})
+    for d in tied:
+        Wq[d] = Wq[a0]
+        sc[d] = sc[a0]
+    lg = oracle.lmhead_logits(x, Wq, sc, K, 1, V)
+    a, _, _ = oracle.argmax(lg)
+    assert int(a[0]) == tied[0] and len(tied) > 1
+    ids, _ = sv.lmhead_argmax(dev_bits16(x), dev_words(Wq), dev_bits16(sc))
+    rest = np.setdiff1d(rng.permutation(V), tied)
+    vm = np.concatenate([rest[:64], np.array(tied[::-1]), rest[64:]]).astype(np.int32)
+    ids_m, _ = sv.lmhead_argmax(dev_bits16(x), dev_words(Wq), dev_bits16(sc), vocab_map=dev_i32(vm))
+    torch.cuda.synchronize()
+    assert ids.cpu().tolist() == [tied[0]]
+    assert ids_m.cpu().tolist() == [tied[0]]
+
+
+def test_bad_map_id_is_skipped_and_flagged(sv, oracle):
+    rng = np.random.default_rng(33)
+    V, K, T = 1500, 256, 1
+    Wq, sc = gen.weights(rng, V, K)
+    x = gen.activations(rng, T, K)
+    vm = gen.vocab_map(rng, V, 300)
+    bad = vm.copy()
+    bad[17] = V + 5
+    bad[200] = -3
+    good = np.delete(vm, [17, 200])
+    ids_b, _ = sv.lmhead_argmax(dev_bits16(x), dev_words(Wq), dev_bits16(sc), vocab_map=dev_i32(bad))
+    torch.cuda.synchronize()
+    assert sv.last_device_error() & sv.DEVERR_BAD_MAP_ID
+    assert sv.last_device_error() == 0            # cleared by the read
+    lg = oracle.lmhead_logits(x, Wq, sc, K, T, V, rows=good)
+    a, _, _ = oracle.argmax(lg, ids=good)
+    assert ids_b.cpu().tolist() == a.tolist()
+
+
+# --------------------------------------------------------------------------
+# full-size configurations (the benchmark's launch configuration)
+
+
+@pytest.mark.slow
+def test_verify_mtp_T4_full_size(sv, oracle):
+    run_head_case(sv, oracle, 2, gen.VOCAB, gen.HIDDEN, 3, 1, 0)
+
+
+@pytest.mark.slow
+def test_verify_dflash2_T8_full_size(sv, oracle):
+    run_head_case(sv, oracle, 3, gen.VOCAB, gen.HIDDEN, 7, 1, 0)
+
+
+@pytest.mark.slow
+def test_verify_dflash2_4_streams_T32_full_size(sv, oracle):
+    run_head_case(sv, oracle, 303, gen.VOCAB, gen.HIDDEN, 7, 4, 0)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("n_draft", [0, 3])
+def test_restricted_head_full_size(sv, oracle, n_draft):
+    run_head_case(sv, oracle, 4 + n_draft, gen.VOCAB, gen.HIDDEN, n_draft, 1, gen.DRAFT_VOCAB)
