@@ -1,10 +1,13 @@
 // specverify.cu -- the C ABI declared in include/specverify.h: argument
 // checks, the per-device scratch area, launch configuration and dispatch to
 // the sm_103a stream kernel (w4a16_stream.cuh).
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <cstdint>
 #include <cstdio>
+#include <cstring>
 #include <mutex>
 
 #include "specverify.h"
@@ -29,11 +32,40 @@ struct DeviceState {
 DeviceState g_state[MAX_DEVICES];
 std::mutex g_mu;
 
-template <int NT, bool HEAD>
+template <int NT, bool HEAD, bool GATHER>
 cudaError_t raise_smem_limit(int bytes)
 {
-    return cudaFuncSetAttribute(w4a16_stream_kernel<NT, HEAD>,
+    return cudaFuncSetAttribute(w4a16_stream_kernel<NT, HEAD, GATHER>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int tensor_map_fn()
+{
+    if (g_encode) return SV_OK;
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+        return SV_ERR_CUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return SV_OK;
+}
+
+// 2-D row-major tensor [rows][cols] of `esize`-byte elements; box = bc x br.
+int encode_2d(CUtensorMap *m, CUtensorMapDataType dt, int esize, const void *base,
+              unsigned long long cols, unsigned long long rows, unsigned bc, unsigned br)
+{
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * static_cast<unsigned long long>(esize)};
+    const cuuint32_t box[2] = {bc, br};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? SV_OK : SV_ERR_CUDA;
 }
 
 // Scratch layout (one cudaMalloc): part [sms][2][PART_FLOATS] fp32, then
@@ -77,13 +109,16 @@ int device_state(DeviceState **out)
         off += sizeof(unsigned);
         st.err = reinterpret_cast<int *>(base + off);
         cudaError_t e = cudaSuccess;
-        e = e != cudaSuccess ? e : raise_smem_limit<1, false>(optin);
-        e = e != cudaSuccess ? e : raise_smem_limit<2, false>(optin);
-        e = e != cudaSuccess ? e : raise_smem_limit<4, false>(optin);
-        e = e != cudaSuccess ? e : raise_smem_limit<1, true>(optin);
-        e = e != cudaSuccess ? e : raise_smem_limit<2, true>(optin);
-        e = e != cudaSuccess ? e : raise_smem_limit<4, true>(optin);
-        if (e != cudaSuccess) {
+        e = e != cudaSuccess ? e : raise_smem_limit<1, false, false>(optin);
+        e = e != cudaSuccess ? e : raise_smem_limit<2, false, false>(optin);
+        e = e != cudaSuccess ? e : raise_smem_limit<4, false, false>(optin);
+        e = e != cudaSuccess ? e : raise_smem_limit<1, true, false>(optin);
+        e = e != cudaSuccess ? e : raise_smem_limit<2, true, false>(optin);
+        e = e != cudaSuccess ? e : raise_smem_limit<4, true, false>(optin);
+        e = e != cudaSuccess ? e : raise_smem_limit<1, true, true>(optin);
+        e = e != cudaSuccess ? e : raise_smem_limit<2, true, true>(optin);
+        e = e != cudaSuccess ? e : raise_smem_limit<4, true, true>(optin);
+        if (e != cudaSuccess || tensor_map_fn() != SV_OK) {
             cudaFree(base);
             return SV_ERR_CUDA;
         }
@@ -98,32 +133,57 @@ int device_state(DeviceState **out)
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
-template <int NT>
-struct Layout {
-    int stage_bytes;
-    int fixed_bytes;
-};
-
-template <int NT>
-Layout<NT> layout_for(int T)
+// Shared-memory layout of one launch (offsets in bytes, 128-byte aligned):
+// nst pipeline stages | scales of 2 tiles | token ids of 3 tiles | reduction
+// buffers | per-CTA argmax keys | flags | mbarriers.
+template <int NT, bool GATHER>
+int plan_layout(Params &p, int smem_optin, int *smem_total)
 {
-    using C = Cfg<NT>;
-    Layout<NT> l;
-    l.stage_bytes = (ROWS * C::WSTR + T * C::XSTR + 127) & ~127;
-    l.fixed_bytes = C::RED_FLOATS * 4 + TMAX * 8 + 16;   // + 16 bytes of barriers per stage
-    return l;
-}
-
-template <int NT, bool HEAD>
-int launch(Params p, const DeviceState &st, cudaStream_t stream)
-{
-    const Layout<NT> l = layout_for<NT>(p.T);
-    int nst = (st.smem_optin - l.fixed_bytes) / (l.stage_bytes + 16);
+    using C = Cfg<NT, GATHER>;
+    auto up = [](int v, int a) { return (v + a - 1) / a * a; };
+    p.xslot_bytes = up(p.T * XROW_BYTES, 128);
+    p.stage_bytes = up(C::W_BYTES + C::GPS * p.xslot_bytes, 128);
+    p.sbuf_bytes = up(ROWS * p.G * 2, 128);
+    const int fixed = 2 * p.sbuf_bytes + up(3 * ROWS * 4, 128) + C::RED_BUFS * C::RED_FLOATS * 4 +
+                      TMAX * 8 + 128;
+    int nst = (smem_optin - fixed - 1024) / (p.stage_bytes + 16);
     if (nst > 6) nst = 6;
     if (nst < 2) return SV_ERR_SHAPE;
     p.nst = nst;
-    p.stage_bytes = l.stage_bytes;
-    const int smem = nst * l.stage_bytes + l.fixed_bytes + nst * 16;
+    int off = nst * p.stage_bytes;
+    p.off_sbuf = off;
+    off += 2 * p.sbuf_bytes;
+    p.off_ids = off;
+    off += up(3 * ROWS * 4, 128);
+    p.off_red = off;
+    off += C::RED_BUFS * C::RED_FLOATS * 4;
+    p.off_best = off;
+    off += TMAX * 8;
+    p.off_flags = off;
+    off += 16;
+    p.off_bars = off;
+    off += 2 * nst * 8;
+    *smem_total = off;
+    return off <= smem_optin ? SV_OK : SV_ERR_SHAPE;
+}
+
+template <int NT, bool HEAD, bool GATHER>
+int launch(Params p, const DeviceState &st, cudaStream_t stream)
+{
+    int smem = 0;
+    int rc = plan_layout<NT, GATHER>(p, st.smem_optin, &smem);
+    if (rc != SV_OK) return rc;
+    CUtensorMap tmW, tmX;
+    std::memset(&tmW, 0, sizeof tmW);
+    if (!GATHER) {
+        rc = encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, p.Wq,
+                       static_cast<unsigned long long>(p.K / 8), static_cast<unsigned long long>(p.n_rows),
+                       16, ROWS);
+        if (rc != SV_OK) return rc;
+    }
+    rc = encode_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, p.x, static_cast<unsigned long long>(p.K),
+                   static_cast<unsigned long long>(p.T), XBOX, static_cast<unsigned>(p.T));
+    if (rc != SV_OK) return rc;
     long long B = st.sms;
     if (B > p.U) B = p.U;
     p.part = st.part;
@@ -131,16 +191,16 @@ int launch(Params p, const DeviceState &st, cudaStream_t stream)
     p.keys = st.keys;
     p.done = st.done;
     p.err = st.err;
-    w4a16_stream_kernel<NT, HEAD><<<static_cast<unsigned>(B), NTHREADS, smem, stream>>>(p);
+    w4a16_stream_kernel<NT, HEAD, GATHER><<<static_cast<unsigned>(B), NTHREADS, smem, stream>>>(p, tmW, tmX);
     return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
-template <bool HEAD>
+template <bool HEAD, bool GATHER>
 int dispatch(Params &p, const DeviceState &st, cudaStream_t stream)
 {
-    if (p.T <= 8) return launch<1, HEAD>(p, st, stream);
-    if (p.T <= 16) return launch<2, HEAD>(p, st, stream);
-    return launch<4, HEAD>(p, st, stream);
+    if (p.T <= 8) return launch<1, HEAD, GATHER>(p, st, stream);
+    if (p.T <= 16) return launch<2, HEAD, GATHER>(p, st, stream);
+    return launch<4, HEAD, GATHER>(p, st, stream);
 }
 
 int check_common(const void *x, const void *Wq, const void *scales, int T, int K)
@@ -195,7 +255,7 @@ int head_call(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, int K
     p.next_token = next_token;
     p.ids = ids;
     p.vals = vals;
-    return dispatch<true>(p, *st, stream);
+    return vocab_map ? dispatch<true, true>(p, *st, stream) : dispatch<true, false>(p, *st, stream);
 }
 
 }  // namespace
@@ -227,7 +287,7 @@ int w4a16_gemm(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, int 
     const long long tiles = (static_cast<long long>(N) + ROWS - 1) / ROWS;
     p.U = tiles * p.G;
     p.y = y;
-    return dispatch<false>(p, *st, reinterpret_cast<cudaStream_t>(stream));
+    return dispatch<false, false>(p, *st, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int lmhead_verify_batched(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, int K,

@@ -1,6 +1,7 @@
 // sv_ptx.cuh -- thin inline-PTX wrappers used by the sm_103a kernels:
-// mbarriers, 1-D bulk (TMA) copies global -> shared, L2 cache policies,
-// the bf16 tensor-core MMA and the int4 -> bf16x2 dequantisation.
+// mbarriers, bulk and tensor (TMA) copies global -> shared, cp.async,
+// L2 cache policies, the bf16 tensor-core MMA and the int4 -> bf16x2
+// dequantisation.
 #pragma once
 
 #include <cstdint>
@@ -83,7 +84,7 @@ __device__ __forceinline__ uint64_t policy_evict_last()
     return p;
 }
 
-// ---------------------------------------------------------------- bulk copy
+// ---------------------------------------------------------------- bulk / tensor copies
 
 // 1-D bulk copy of `bytes` (multiple of 16; both addresses 16-byte aligned)
 // from global memory into this CTA's shared memory, completing on `bar`.
@@ -93,6 +94,40 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
                  " [%0], [%1], %2, [%3], %4;"
                  ::"r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(policy) : "memory");
+}
+
+// 2-D tiled tensor copy of one box at coordinates (c0 innermost, c1) into
+// shared memory (128-byte aligned), completing on `bar`.  Out-of-range parts
+// of the box are filled with zeros and still count towards the bytes.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int c0, int c1,
+                                            uint32_t bar, uint64_t policy)
+{
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                 ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;"
+                 ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(bar),
+                   "l"(policy)
+                 : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const void *tmap)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+}
+
+// 4-byte asynchronous copy global -> shared (both 4-byte aligned).
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit()
+{
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all()
+{
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- named barriers
@@ -112,6 +147,13 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr)
     return v;
 }
 
+__device__ __forceinline__ uint32_t lds_u16(uint32_t addr)
+{
+    uint16_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+    return v;
+}
+
 // ---------------------------------------------------------------- global loads
 
 __device__ __forceinline__ uint16_t ldg_u16(const uint16_t *p)
@@ -121,9 +163,9 @@ __device__ __forceinline__ uint16_t ldg_u16(const uint16_t *p)
     return v;
 }
 
-__device__ __forceinline__ float bf16_bits_to_float(uint16_t h)
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t h)
 {
-    return __uint_as_float(static_cast<uint32_t>(h) << 16);
+    return __uint_as_float(h << 16);
 }
 
 // ---------------------------------------------------------------- dequant
@@ -149,9 +191,9 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
                                                uint32_t b1)
 {
     asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-                 "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 // ---------------------------------------------------------------- argmax keys
