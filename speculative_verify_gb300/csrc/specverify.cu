@@ -134,35 +134,32 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 // Shared-memory layout of one launch (offsets in bytes, 128-byte aligned):
-// nst pipeline stages | scales of 2 tiles | token ids of 3 tiles | reduction
-// buffers | per-CTA argmax keys | flags | mbarriers.
+// nst pipeline stages | scales of 2 tiles | token ids of 2 tiles | the
+// consumers' partial sums of one tile | mbarriers and a flag.
 template <int NT, bool GATHER>
 int plan_layout(Params &p, int smem_optin, int *smem_total)
 {
     using C = Cfg<NT, GATHER>;
     auto up = [](int v, int a) { return (v + a - 1) / a * a; };
-    p.xslot_bytes = up(p.T * XROW_BYTES, 128);
+    p.xslot_bytes = up(C::TP * XROW_BYTES, 128);
     p.stage_bytes = up(C::W_BYTES + C::GPS * p.xslot_bytes, 128);
     p.sbuf_bytes = up(ROWS * p.G * 2, 128);
-    const int fixed = 2 * p.sbuf_bytes + up(3 * ROWS * 4, 128) + C::RED_BUFS * C::RED_FLOATS * 4 +
-                      TMAX * 8 + 128;
+    const int ids_bytes = up(2 * ROWS * 4, 128);
+    const int red_bytes = up(C::RED_FLOATS * 4, 128);
+    const int fixed = 2 * p.sbuf_bytes + ids_bytes + red_bytes + 7 * 8 + 8;
     int nst = (smem_optin - fixed - 1024) / (p.stage_bytes + 16);
-    if (nst > 6) nst = 6;
+    if (nst > 8) nst = 8;
     if (nst < 2) return SV_ERR_SHAPE;
     p.nst = nst;
     int off = nst * p.stage_bytes;
     p.off_sbuf = off;
     off += 2 * p.sbuf_bytes;
     p.off_ids = off;
-    off += up(3 * ROWS * 4, 128);
+    off += ids_bytes;
     p.off_red = off;
-    off += C::RED_BUFS * C::RED_FLOATS * 4;
-    p.off_best = off;
-    off += TMAX * 8;
-    p.off_flags = off;
-    off += 16;
+    off += red_bytes;
     p.off_bars = off;
-    off += 2 * nst * 8;
+    off += (2 * nst + 6) * 8 + 8;
     *smem_total = off;
     return off <= smem_optin ? SV_OK : SV_ERR_SHAPE;
 }
@@ -181,6 +178,9 @@ int launch(Params p, const DeviceState &st, cudaStream_t stream)
                        16, ROWS);
         if (rc != SV_OK) return rc;
     }
+    // The activation box is exactly T rows high (boxes reaching past the
+    // tensor are much slower to fill); the kernel zeroes the spare token rows
+    // of every stage once, so B fragments can be loaded unconditionally.
     rc = encode_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, p.x, static_cast<unsigned long long>(p.K),
                    static_cast<unsigned long long>(p.T), XBOX, static_cast<unsigned>(p.T));
     if (rc != SV_OK) return rc;

@@ -27,6 +27,13 @@ __device__ __forceinline__ void fence_barrier_init()
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Order this thread's generic-proxy shared-memory writes before later
+// async-proxy (TMA) accesses of shared memory.
+__device__ __forceinline__ void fence_proxy_async()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive(uint32_t bar)
 {
     asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
@@ -120,6 +127,19 @@ __device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src)
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared (both 16-byte aligned), L2 only.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// Arrive on `bar` once every cp.async this thread issued so far has landed.
+// The arrival is one of the barrier's expected arrivals (.noinc).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 __device__ __forceinline__ void cp_async_commit()
 {
     asm volatile("cp.async.commit_group;" ::: "memory");
@@ -169,6 +189,13 @@ __device__ __forceinline__ float bf16_bits_to_float(uint32_t h)
 }
 
 // ---------------------------------------------------------------- dequant
+
+__device__ __forceinline__ uint32_t mulhi(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("mul.hi.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
 
 // Two nibbles -> two bf16 levels.  v holds nibble a in bits 0..3 and nibble
 // b in bits 16..19 (other bits ignored).  OR-ing a nibble into the mantissa

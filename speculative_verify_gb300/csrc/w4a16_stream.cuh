@@ -11,18 +11,25 @@
 // counter in the scratch area), which adds the fp32 partial sums of all the
 // tile's CTAs in a fixed order: results do not depend on arrival order.
 //
-// Inside a CTA: warp 16 is the producer.  Each pipeline stage holds up to
-// GPS units of one tile; the producer fills it with tensor (TMA) copies --
-// one 64-row x 64-byte box per group of packed weights and one box of the
-// activations per group -- completing on the stage's mbarrier.  (When rows
-// are gathered through a vocab_map, each weight row segment is a 1-D bulk
-// copy instead.)  Warps 0..15 consume: warp w takes group (w % GPS) of the
-// stage for R m16 tiles, dequantises its nibbles in registers and feeds them
-// to the bf16 tensor cores as the A operand (mma.sync m16n8k16, tokens as the
-// n8 B operand), and folds each group's fp32 sum into its accumulators with
-// the group scale.  Scales of a tile are staged in shared memory two tiles
-// ahead with cp.async.  Every weight byte crosses HBM once per call; T only
-// changes how many n8 token tiles each dequantised fragment multiplies.
+// Warp roles inside a CTA (all hand-offs are mbarriers; no CTA-wide barrier
+// after set-up):
+//  * warp 16, producer: fills each pipeline stage (up to GPS units of one
+//    tile) with tensor (TMA) copies -- one 64-row x 64-byte box of packed
+//    weights and one box of activations per group -- completing on the
+//    stage's mbarrier.  Gathered rows (a vocab_map) use one 1-D bulk copy per
+//    row segment instead.
+//  * warps 0..15, consumers: warp w takes group (w % GPS) of a stage for R
+//    m16 tiles, dequantises its nibbles in registers and feeds them to the
+//    bf16 tensor cores as the A operand (mma.sync m16n8k16; tokens are the
+//    n8 B operand), and folds each group's fp32 sum into its accumulators
+//    with the group scale.  At the end of a tile each warp hands its partial
+//    sums to the epilogue warp through shared memory.
+//  * warp 17, epilogue: stages the scales (and token ids) of tile k+2 while
+//    tile k+1 is being computed, adds the consumers' partials in a fixed
+//    order, finishes split tiles, and runs the GEMM store or the lm_head
+//    argmax; at the end it runs the grid-level argmax and the verify.
+// Every weight byte crosses HBM once per call; T only changes how many n8
+// token tiles each dequantised fragment multiplies.
 #pragma once
 
 #include <cstdint>
@@ -35,8 +42,9 @@ namespace sv {
 
 constexpr int ROWS = 64;                        // rows per tile
 constexpr int NCW = 16;                         // consumer warps
-constexpr int NTHREADS = (NCW + 1) * 32;        // + one producer warp
-constexpr int CONSUMERS = NCW * 32;
+constexpr int PRODUCER_WARP = NCW;
+constexpr int EPILOGUE_WARP = NCW + 1;
+constexpr int NTHREADS = (NCW + 2) * 32;
 constexpr int TMAX = 32;                        // largest T
 constexpr int PART_FLOATS = TMAX * ROWS;        // one split-tile partial
 constexpr int XBOX = 144;                       // activation box width (elements)
@@ -56,7 +64,6 @@ struct Cfg {
     static constexpr int WSTR_G = GPS * 64 + 64;
     static constexpr int W_BYTES = GATHER ? ROWS * WSTR_G : GPS * ROWS * 64;
     static constexpr int RED_FLOATS = GPS * TP * ROWS;
-    static constexpr int RED_BUFS = (NT == 4) ? 1 : 2;
 };
 
 struct Params {
@@ -70,7 +77,7 @@ struct Params {
     long long U;                // units = tiles * G
     // shared-memory layout (bytes)
     int nst, stage_bytes, xslot_bytes, sbuf_bytes;
-    int off_sbuf, off_ids, off_red, off_best, off_flags, off_bars;
+    int off_sbuf, off_ids, off_red, off_bars;
     // GEMM output
     uint16_t *y;                // [T][N]
     // HEAD outputs
@@ -102,7 +109,8 @@ __device__ __forceinline__ int cta_of(long long u, long long U, int B)
     return static_cast<int>(b);
 }
 
-// Token id of row rloc of tile `tile` (or -1 when the row does not exist).
+// Token id of row rloc of tile `tile` (or -1 when the row does not exist or
+// its vocab_map entry is out of range; the latter sets the error word).
 __device__ __forceinline__ int row_id(const Params &p, int tile, int rloc)
 {
     const long long rg = static_cast<long long>(tile) * ROWS + rloc;
@@ -114,38 +122,59 @@ __device__ __forceinline__ int row_id(const Params &p, int tile, int rloc)
     return -1;
 }
 
-// Stage the scales (and, for the head, the token ids) of one tile into
-// shared memory.  Warp w owns rows w, w+16, w+32, w+48.  Uses 4-byte
-// cp.async when a scale row has an even number of groups, plain loads
-// otherwise; the caller commits / waits.
-template <bool HEAD>
-__device__ __forceinline__ void stage_tile_meta(const Params &p, int tile, const int (&id)[4],
-                                                uint8_t *sb, int32_t *ib, int cw, int lane)
+__device__ __forceinline__ void wait_or_flag(const Params &p, volatile int *flag, uint32_t bar,
+                                             uint32_t parity)
 {
-    const int G = p.G;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int rloc = cw + 16 * i;
-        uint16_t *dst = reinterpret_cast<uint16_t *>(sb) + rloc * G;
-        if (HEAD && lane == 0) ib[rloc] = id[i];
-        if (id[i] < 0) {
-            for (int j = lane; j < G; j += 32) dst[j] = 0;
-            continue;
-        }
-        const uint16_t *src = p.scales + static_cast<size_t>(id[i]) * G;
-        if ((G & 1) == 0) {
-            for (int j = lane; j < G / 2; j += 32) cp_async_4(smem_addr(dst + 2 * j), src + 2 * j);
-        } else {
-            for (int j = lane; j < G; j += 32) dst[j] = ldg_u16(src + j);
-        }
+    const uint64_t lim = *flag ? WAIT_LIMIT_AFTER_ERR_NS : WAIT_LIMIT_NS;
+    if (!mbar_wait_bounded(bar, parity, lim)) {
+        *flag = 1;
+        atomicOr(p.err, 2);
     }
-    (void)tile;
 }
 
-__device__ __forceinline__ void tile_ids(const Params &p, int tile, int last_tile, int cw, int (&id)[4])
+// Epilogue warp: stage the scales (and, for the head, the token ids) of one
+// tile into shared memory with cp.async, then arrive on `bar` (expected
+// arrivals: 32 cp.async completions + 1 plain arrival).  Rows that do not
+// exist get scale 0 and id -1.
+template <bool HEAD, bool GATHER>
+__device__ __forceinline__ void stage_tile_meta(const Params &p, int tile, uint8_t *sb,
+                                                int32_t *ib, uint32_t bar, int lane)
 {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) id[i] = (tile <= last_tile) ? row_id(p, tile, cw + 16 * i) : -1;
+    const int G = p.G;
+    uint16_t *dst = reinterpret_cast<uint16_t *>(sb);
+    const int id0 = row_id(p, tile, lane), id1 = row_id(p, tile, lane + 32);
+    if (HEAD) {
+        ib[lane] = id0;
+        ib[lane + 32] = id1;
+    }
+    if (!GATHER) {
+        // rows are contiguous: one contiguous block of nvalid * G scales
+        const long long r0 = static_cast<long long>(tile) * ROWS;
+        const int nvalid = static_cast<int>(min(static_cast<long long>(ROWS), p.n_rows - r0));
+        const uint16_t *src = p.scales + r0 * G;
+        const int nel = nvalid * G;
+        const int n16 = nel / 8;                         // 16-byte chunks
+        for (int i = lane; i < n16; i += 32) cp_async_16(smem_addr(dst + 8 * i), src + 8 * i);
+        for (int i = 8 * n16 + lane; i < nel; i += 32) dst[i] = ldg_u16(src + i);
+        for (int i = nel + lane; i < ROWS * G; i += 32) dst[i] = 0;
+    } else {
+        for (int r = 0; r < ROWS; ++r) {
+            const int id = __shfl_sync(0xFFFFFFFFu, r < 32 ? id0 : id1, r & 31);
+            uint16_t *d = dst + r * G;
+            if (id < 0) {
+                for (int j = lane; j < G; j += 32) d[j] = 0;
+            } else if ((G & 1) == 0) {
+                const uint16_t *src = p.scales + static_cast<size_t>(id) * G;
+                for (int j = lane; j < G / 2; j += 32) cp_async_4(smem_addr(d + 2 * j), src + 2 * j);
+            } else {
+                const uint16_t *src = p.scales + static_cast<size_t>(id) * G;
+                for (int j = lane; j < G; j += 32) d[j] = ldg_u16(src + j);
+            }
+        }
+    }
+    cp_async_mbar_arrive(bar);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar);
 }
 
 template <int NT, bool HEAD, bool GATHER>
@@ -156,13 +185,17 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
     using C = Cfg<NT, GATHER>;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int nst = p.nst;
-    uint8_t *sbuf = smem + p.off_sbuf;                       // [2][sbuf_bytes]
-    int32_t *idbuf = reinterpret_cast<int32_t *>(smem + p.off_ids);   // [3][ROWS]
-    float *red = reinterpret_cast<float *>(smem + p.off_red);          // [RED_BUFS][RED_FLOATS]
-    unsigned long long *best = reinterpret_cast<unsigned long long *>(smem + p.off_best);  // [TMAX]
-    volatile int *flags = reinterpret_cast<volatile int *>(smem + p.off_flags);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.off_bars);
-    uint64_t *empty = full + nst;
+    uint8_t *sbuf = smem + p.off_sbuf;                                // [2][sbuf_bytes]
+    int32_t *idbuf = reinterpret_cast<int32_t *>(smem + p.off_ids);   // [2][ROWS]
+    float *red = reinterpret_cast<float *>(smem + p.off_red);         // [RED_FLOATS]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + p.off_bars);
+    uint64_t *full = bars;                    // [nst]  producer -> consumers
+    uint64_t *empty = bars + nst;             // [nst]  consumers -> producer
+    uint64_t *meta_full = bars + 2 * nst;     // [2]    epilogue -> consumers
+    uint64_t *meta_empty = meta_full + 2;     // [2]    consumers -> epilogue
+    uint64_t *red_full = meta_full + 4;       //        consumers -> epilogue
+    uint64_t *red_empty = meta_full + 5;      //        epilogue -> consumers
+    volatile int *flag = reinterpret_cast<volatile int *>(meta_full + 6);   // a wait timed out
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int B = gridDim.x, b = blockIdx.x;
@@ -172,21 +205,39 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
     const int tile_first = static_cast<int>(u0 / G);
     const int grp_first = static_cast<int>(u0 - static_cast<long long>(tile_first) * G);
     const int tile_last = static_cast<int>((u1 - 1) / G);
+    const int n_units = static_cast<int>(u1 - u0);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < nst; ++s) {
             mbar_init(smem_addr(&full[s]), 1);
             mbar_init(smem_addr(&empty[s]), NCW);
         }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_addr(&meta_full[i]), 33);
+            mbar_init(smem_addr(&meta_empty[i]), NCW);
+        }
+        mbar_init(smem_addr(red_full), NCW);
+        mbar_init(smem_addr(red_empty), 1);
+        *flag = 0;
         fence_barrier_init();
-        flags[0] = 0;   // a wait timed out in this CTA
-        flags[1] = 0;   // this CTA finishes the current split tile
-        flags[2] = 0;   // this CTA is the last one of the grid
     }
-    if (threadIdx.x < TMAX) best[threadIdx.x] = 0ull;
+    // Token rows T..TP-1 of every stage's activation slots stay zero for the
+    // whole kernel (the tensor copies only write rows 0..T-1).
+    if (T < C::TP) {
+        const int per_slot = (C::TP - T) * XROW_BYTES / 16;
+        const int total = nst * C::GPS * per_slot;
+        for (int i = threadIdx.x; i < total; i += NTHREADS) {
+            const int st = i / (C::GPS * per_slot), rest = i % (C::GPS * per_slot);
+            const int sl = rest / per_slot, q = rest % per_slot;
+            uint4 *d = reinterpret_cast<uint4 *>(smem + static_cast<size_t>(st) * p.stage_bytes + C::W_BYTES +
+                                                 sl * p.xslot_bytes + T * XROW_BYTES) + q;
+            *d = make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async();
+    }
     __syncthreads();
 
-    if (warp == NCW) {
+    if (warp == PRODUCER_WARP) {
         // ============================================================ producer
         const uint64_t pol_w = policy_evict_first();
         const uint64_t pol_x = policy_evict_last();
@@ -194,7 +245,7 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
             if (!GATHER) prefetch_tmap(&tmW);
             prefetch_tmap(&tmX);
         }
-        int s = 0, issued = 0, tile = tile_first, grp = grp_first;
+        int s = 0, issued = 0, tile = tile_first, grp = grp_first, rem = n_units;
         uint32_t ph = 0;
         // gathered rows: ids of this lane's two rows, for this tile and the next
         int gid[2] = {-1, -1}, gid_next[2] = {-1, -1};
@@ -206,17 +257,11 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
                 gid_next[1] = row_id(p, tile + 1, lane + 32);
             }
         }
-        for (long long u = u0; u < u1;) {
-            const int n = static_cast<int>(min(static_cast<long long>(min(C::GPS, G - grp)), u1 - u));
-            if (issued >= nst) {
-                const uint64_t lim = flags[0] ? WAIT_LIMIT_AFTER_ERR_NS : WAIT_LIMIT_NS;
-                if (!mbar_wait_bounded(smem_addr(&empty[s]), ph ^ 1u, lim)) {
-                    flags[0] = 1;
-                    atomicOr(p.err, 2);
-                }
-            }
+        while (rem > 0) {
+            const int n = min(min(C::GPS, G - grp), rem);
+            if (issued >= nst) wait_or_flag(p, flag, smem_addr(&empty[s]), ph ^ 1u);
             const uint32_t fb = smem_addr(&full[s]);
-            const uint32_t stage = smem_addr(smem + static_cast<size_t>(s) * p.stage_bytes);
+            const uint32_t stage = smem_addr(smem) + static_cast<uint32_t>(s * p.stage_bytes);
             uint32_t wbytes;
             if (GATHER) {
                 const int cnt = __popc(__ballot_sync(0xFFFFFFFFu, gid[0] >= 0)) +
@@ -240,7 +285,7 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
             if (lane >= 16 && lane - 16 < n)
                 tma_load_2d(stage + C::W_BYTES + (lane - 16) * p.xslot_bytes, &tmX,
                             (grp + lane - 16) * 128, 0, fb, pol_x);
-            u += n;
+            rem -= n;
             grp += n;
             if (grp == G) {
                 grp = 0;
@@ -263,8 +308,146 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
         while (left-- > 0) {
             if (--ds < 0) { ds = nst - 1; dph ^= 1u; }
             if (!mbar_wait_bounded(smem_addr(&full[ds]), dph, WAIT_LIMIT_AFTER_ERR_NS)) {
-                flags[0] = 1;
+                *flag = 1;
                 atomicOr(p.err, 2);
+            }
+        }
+        return;
+    }
+
+    if (warp == EPILOGUE_WARP) {
+        // ============================================================ epilogue
+        stage_tile_meta<HEAD, GATHER>(p, tile_first, sbuf, idbuf, smem_addr(&meta_full[0]), lane);
+        if (tile_first + 1 <= tile_last)
+            stage_tile_meta<HEAD, GATHER>(p, tile_first + 1, sbuf + p.sbuf_bytes, idbuf + ROWS,
+                                          smem_addr(&meta_full[1]), lane);
+        unsigned long long best = 0ull;    // lane t: best key of token t so far
+        for (int k = 0, tile = tile_first; tile <= tile_last; ++k, ++tile) {
+            const int kb = k & 1;
+            wait_or_flag(p, flag, smem_addr(red_full), static_cast<uint32_t>(k & 1));
+            const long long ts = static_cast<long long>(tile) * G, te = ts + G;
+            const bool complete = (u0 <= ts) && (u1 >= te);
+            // Sum the group slots (fixed order) for rows lane and lane+32.
+            // Split tiles are published and possibly finished first.
+            int bf = 0, bl = 0;
+            bool finish = true;
+            if (!complete) {
+                bf = cta_of(ts, U, B);
+                bl = cta_of(te - 1, U, B);
+                float *mine = p.part + (static_cast<size_t>(b) * 2 + (tile == tile_first ? 0 : 1)) * PART_FLOATS;
+                for (int t = 0; t < T; ++t)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int row = lane + 32 * h;
+                        float sum = red[t * ROWS + row];
+#pragma unroll
+                        for (int sl = 1; sl < C::GPS; ++sl) sum += red[(sl * C::TP + t) * ROWS + row];
+                        mine[t * ROWS + row] = sum;
+                    }
+                __threadfence();
+                __syncwarp();
+                unsigned last = 0;
+                if (lane == 0) {
+                    const unsigned old = atomicAdd(&p.ctr[bf], 1u);
+                    last = (old == static_cast<unsigned>(bl - bf));
+                    if (last) atomicExch(&p.ctr[bf], 0u);
+                }
+                finish = __shfl_sync(0xFFFFFFFFu, last, 0) != 0;
+                if (finish) __threadfence();
+            }
+            const int32_t *ids = idbuf + kb * ROWS;
+            const int id0 = HEAD ? ids[lane] : 0, id1 = HEAD ? ids[lane + 32] : 0;
+            for (int t = 0; t < T && finish; ++t) {
+                float v[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int row = lane + 32 * h;
+                    if (complete) {
+                        float sum = red[t * ROWS + row];
+#pragma unroll
+                        for (int sl = 1; sl < C::GPS; ++sl) sum += red[(sl * C::TP + t) * ROWS + row];
+                        v[h] = sum;
+                    } else {
+                        float sum = 0.f;
+                        for (int bb = bf; bb <= bl; ++bb) {
+                            const int wb2 = (cta_start(bb, U, B) >= ts) ? 0 : 1;
+                            const float pv = __ldcg(p.part + (static_cast<size_t>(bb) * 2 + wb2) * PART_FLOATS +
+                                                    t * ROWS + row);
+                            sum = (bb == bf) ? pv : sum + pv;
+                        }
+                        v[h] = sum;
+                    }
+                }
+                if constexpr (!HEAD) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const long long rg = static_cast<long long>(tile) * ROWS + lane + 32 * h;
+                        if (rg < p.n_rows)
+                            p.y[static_cast<size_t>(t) * p.n_rows + rg] =
+                                __bfloat16_as_ushort(__float2bfloat16_rn(v[h]));
+                    }
+                } else {
+                    unsigned long long k0 = id0 >= 0 ? make_key(v[0], static_cast<uint32_t>(id0)) : 0ull;
+                    unsigned long long k1 = id1 >= 0 ? make_key(v[1], static_cast<uint32_t>(id1)) : 0ull;
+                    unsigned long long kk = k0 > k1 ? k0 : k1;
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        const unsigned long long ko = shfl_xor_u64(kk, o);
+                        kk = ko > kk ? ko : kk;
+                    }
+                    if (lane == t && kk > best) best = kk;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(red_empty));     // red may be overwritten
+            // Metadata of tile k+2 goes into the buffers tile k used.
+            if (tile + 2 <= tile_last) {
+                wait_or_flag(p, flag, smem_addr(&meta_empty[kb]), static_cast<uint32_t>((k >> 1) & 1));
+                stage_tile_meta<HEAD, GATHER>(p, tile + 2, sbuf + kb * p.sbuf_bytes, idbuf + kb * ROWS,
+                                              smem_addr(&meta_full[kb]), lane);
+            }
+        }
+        if constexpr (HEAD) {
+            // ================================================ grid argmax + verify
+            if (lane < T && best != 0ull) atomicMax(&p.keys[lane], best);
+            __threadfence();
+            __syncwarp();
+            unsigned last = 0;
+            if (lane == 0) last = (atomicAdd(p.done, 1u) == static_cast<unsigned>(B - 1));
+            if (__shfl_sync(0xFFFFFFFFu, last, 0)) {
+                __threadfence();
+                int32_t a = -1;
+                unsigned long long kk = 0ull;
+                if (lane < T) {
+                    kk = __ldcg(&p.keys[lane]);
+                    a = (kk == 0ull) ? -1 : key_id(kk);
+                    p.keys[lane] = 0ull;
+                }
+                if (p.mode == 1) {
+                    if (lane < T) {
+                        p.ids[lane] = a;
+                        if (p.vals) p.vals[lane] = (kk == 0ull) ? __int_as_float(0x7fc00000) : key_value(kk);
+                    }
+                } else {
+                    const int rows_per = p.n_draft + 1;
+                    const int sidx = lane < p.n_streams ? lane : 0;
+                    int acc = -1, nxt = -1;
+                    for (int i = 0; i <= p.n_draft; ++i) {
+                        const int ai = __shfl_sync(0xFFFFFFFFu, a, (sidx * rows_per + i) & 31);
+                        if (acc < 0) {
+                            if (i == p.n_draft || p.drafts[static_cast<size_t>(sidx) * p.n_draft + i] != ai) {
+                                acc = i;
+                                nxt = ai;
+                            }
+                        }
+                    }
+                    if (lane < p.n_streams) {
+                        p.accept_len[lane] = acc;
+                        p.next_token[lane] = nxt;
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) *p.done = 0u;
             }
         }
         return;
@@ -275,22 +458,17 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
     const int slot = cw % C::GPS;
     const int mset = cw / C::GPS;
     const int g = lane >> 2, c = lane & 3;
-    const int tid = cw * 32 + lane;
 
-    // Tile metadata: scales of tile k live in sbuf[k & 1], ids in idbuf[k % 3].
-    int idreg[4];
-    {
-        tile_ids(p, tile_first, tile_last, cw, idreg);
-        stage_tile_meta<HEAD>(p, tile_first, idreg, sbuf, idbuf, cw, lane);
-        if (tile_first + 1 <= tile_last) {
-            tile_ids(p, tile_first + 1, tile_last, cw, idreg);
-            stage_tile_meta<HEAD>(p, tile_first + 1, idreg, sbuf + p.sbuf_bytes, idbuf + ROWS, cw, lane);
-        }
-        cp_async_commit();
-        tile_ids(p, tile_first + 2, tile_last, cw, idreg);     // for the first flush
-        cp_async_wait_all();
-        named_bar_sync(1, CONSUMERS);
-    }
+    // Lane-constant shared-memory offsets (within a stage / a scale buffer).
+    constexpr int RSTEP = GATHER ? 16 * C::WSTR_G : 16 * 64;   // next m16 tile
+    constexpr int HSTEP = GATHER ? 8 * C::WSTR_G : 8 * 64;     // row g + 8
+    const int row0 = mset * C::R * 16 + g;                     // first row of this lane
+    const uint32_t w_lane = GATHER ? static_cast<uint32_t>(row0 * C::WSTR_G + slot * 64 + c * 16)
+                                   : static_cast<uint32_t>(slot * (ROWS * 64) + row0 * 64 + c * 16);
+    const uint32_t x_lane = static_cast<uint32_t>(C::W_BYTES + slot * p.xslot_bytes + g * XROW_BYTES + c * 64);
+    const uint32_t s_lane = static_cast<uint32_t>(row0 * G * 2);
+    const uint32_t sbuf0 = smem_addr(sbuf);
+    const uint32_t smem0 = smem_addr(smem);
 
     float acc[C::R][NT][4];
 #pragma unroll
@@ -300,28 +478,21 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[r][nt][e] = 0.f;
 
-    int s = 0, tile = tile_first, grp = grp_first, k_rel = 0, nflush = 0;
+    int s = 0, grp = grp_first, rem = n_units, k = 0;
     uint32_t ph = 0;
-    const uint32_t sbuf0 = smem_addr(sbuf);
-    for (long long u = u0; u < u1;) {
-        const int n = static_cast<int>(min(static_cast<long long>(min(C::GPS, G - grp)), u1 - u));
-        {
-            const uint64_t lim = flags[0] ? WAIT_LIMIT_AFTER_ERR_NS : WAIT_LIMIT_NS;
-            if (!mbar_wait_bounded(smem_addr(&full[s]), ph, lim)) {
-                flags[0] = 1;
-                atomicOr(p.err, 2);
-            }
+    bool tile_start = true;
+    while (rem > 0) {
+        const int n = min(min(C::GPS, G - grp), rem);
+        const int kb = k & 1;
+        if (tile_start) {
+            wait_or_flag(p, flag, smem_addr(&meta_full[kb]), static_cast<uint32_t>((k >> 1) & 1));
+            tile_start = false;
         }
+        wait_or_flag(p, flag, smem_addr(&full[s]), ph);
         if (slot < n) {
             const int gs = grp + slot;     // group within the row
-            const uint32_t stage = smem_addr(smem + static_cast<size_t>(s) * p.stage_bytes);
-            uint32_t wbase;
-            constexpr int RSTEP = GATHER ? 16 * C::WSTR_G : 16 * 64;   // next m16 tile
-            constexpr int HSTEP = GATHER ? 8 * C::WSTR_G : 8 * 64;     // row g + 8
-            if (GATHER)
-                wbase = stage + (mset * C::R * 16 + g) * C::WSTR_G + slot * 64 + c * 16;
-            else
-                wbase = stage + slot * (ROWS * 64) + (mset * C::R * 16 + g) * 64 + c * 16;
+            const uint32_t stage = smem0 + static_cast<uint32_t>(s * p.stage_bytes);
+            const uint32_t wbase = stage + w_lane;
             uint4 wa[C::R], wb[C::R];
 #pragma unroll
             for (int r = 0; r < C::R; ++r) {
@@ -336,24 +507,20 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
 #pragma unroll
                     for (int e = 0; e < 4; ++e) gacc[r][nt][e] = 0.f;
 
-            const uint32_t xbase = stage + C::W_BYTES + slot * p.xslot_bytes + c * 64;
+            const uint32_t xbase = stage + x_lane;
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
                 // B fragments: token (nt*8 + g), the 8 activations of word
                 // (4c + m) of the group, paired (j, j+4) like the nibbles.
+                // Token rows >= T are zeros (filled by the tensor copy).
                 uint32_t bx[NT][4];
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    const int tok = nt * 8 + g;
-                    if (tok < T) {
-                        const uint4 v = lds128(xbase + tok * XROW_BYTES + m * 16);
-                        bx[nt][0] = __byte_perm(v.x, v.z, 0x5410);   // (x0, x4)
-                        bx[nt][1] = __byte_perm(v.x, v.z, 0x7632);   // (x1, x5)
-                        bx[nt][2] = __byte_perm(v.y, v.w, 0x5410);   // (x2, x6)
-                        bx[nt][3] = __byte_perm(v.y, v.w, 0x7632);   // (x3, x7)
-                    } else {
-                        bx[nt][0] = bx[nt][1] = bx[nt][2] = bx[nt][3] = 0u;
-                    }
+                    const uint4 v = lds128(xbase + nt * 8 * XROW_BYTES + m * 16);
+                    bx[nt][0] = __byte_perm(v.x, v.z, 0x5410);   // (x0, x4)
+                    bx[nt][1] = __byte_perm(v.x, v.z, 0x7632);   // (x1, x5)
+                    bx[nt][2] = __byte_perm(v.y, v.w, 0x5410);   // (x2, x6)
+                    bx[nt][3] = __byte_perm(v.y, v.w, 0x7632);   // (x3, x7)
                 }
 #pragma unroll
                 for (int r = 0; r < C::R; ++r) {
@@ -376,12 +543,11 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
                 }
             }
             // group scales of this lane's rows (staged in shared memory)
-            const uint32_t sb = sbuf0 + (k_rel & 1) * p.sbuf_bytes;
+            const uint32_t sb = sbuf0 + kb * p.sbuf_bytes + s_lane + gs * 2;
 #pragma unroll
             for (int r = 0; r < C::R; ++r) {
-                const int row = (mset * C::R + r) * 16 + g;
-                const float s0 = bf16_bits_to_float(lds_u16(sb + (row * G + gs) * 2));
-                const float s1 = bf16_bits_to_float(lds_u16(sb + ((row + 8) * G + gs) * 2));
+                const float s0 = bf16_bits_to_float(lds_u16(sb + r * 16 * G * 2));
+                const float s1 = bf16_bits_to_float(lds_u16(sb + (r * 16 + 8) * G * 2));
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     acc[r][nt][0] += s0 * gacc[r][nt][0];
@@ -394,13 +560,13 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
         if (++s == nst) { s = 0; ph ^= 1u; }
-        u += n;
+        rem -= n;
         grp += n;
 
-        if (grp == G || u == u1) {
-            // ================================================ tile flush
-            float *rbuf = red + ((C::RED_BUFS == 2) ? (nflush & 1) : 0) * C::RED_FLOATS;
-            // 1. warp partials -> rbuf[slot][tok][row]
+        if (grp == G || rem == 0) {
+            // End of this CTA's share of a tile: hand the partial sums over.
+            if (lane == 0) mbar_arrive(smem_addr(&meta_empty[kb]));   // scales no longer read
+            wait_or_flag(p, flag, smem_addr(red_empty), static_cast<uint32_t>((k & 1) ^ 1));
 #pragma unroll
             for (int r = 0; r < C::R; ++r)
 #pragma unroll
@@ -409,154 +575,14 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
                     for (int e = 0; e < 4; ++e) {
                         const int row = (mset * C::R + r) * 16 + g + 8 * (e >> 1);
                         const int tok = nt * 8 + 2 * c + (e & 1);
-                        rbuf[(slot * C::TP + tok) * ROWS + row] = acc[r][nt][e];
+                        red[(slot * C::TP + tok) * ROWS + row] = acc[r][nt][e];
                         acc[r][nt][e] = 0.f;
                     }
-            cp_async_wait_all();                 // metadata of the next tile(s)
-            named_bar_sync(1, CONSUMERS);
-
-            // 2. sum the group slots in a fixed order
-            constexpr int PER = (C::TP * ROWS + CONSUMERS - 1) / CONSUMERS;
-            float v[PER];
-#pragma unroll
-            for (int q = 0; q < PER; ++q) {
-                const int pidx = tid + q * CONSUMERS;
-                const int tok = pidx / ROWS, row = pidx % ROWS;
-                float sum = 0.f;
-                if (tok < T) {
-                    sum = rbuf[tok * ROWS + row];
-#pragma unroll
-                    for (int sl = 1; sl < C::GPS; ++sl) sum += rbuf[(sl * C::TP + tok) * ROWS + row];
-                }
-                v[q] = sum;
-            }
-
-            // 3. split tile: publish the partial; the last CTA adds them all
-            const long long ts = static_cast<long long>(tile) * G, te = ts + G;
-            const bool complete = (u0 <= ts) && (u1 >= te);
-            bool finish = true;
-            if (!complete) {
-                const int bf = cta_of(ts, U, B), bl = cta_of(te - 1, U, B);
-                const int which = (tile == tile_first) ? 0 : 1;
-                float *mine = p.part + (static_cast<size_t>(b) * 2 + which) * PART_FLOATS;
-#pragma unroll
-                for (int q = 0; q < PER; ++q) {
-                    const int pidx = tid + q * CONSUMERS;
-                    if (pidx / ROWS < T) mine[pidx] = v[q];
-                }
-                __threadfence();
-                named_bar_sync(1, CONSUMERS);
-                if (tid == 0) {
-                    const unsigned old = atomicAdd(&p.ctr[bf], 1u);
-                    const int last = (old == static_cast<unsigned>(bl - bf));
-                    if (last) atomicExch(&p.ctr[bf], 0u);
-                    flags[1] = last;
-                }
-                named_bar_sync(1, CONSUMERS);
-                finish = flags[1] != 0;
-                if (finish) {
-                    __threadfence();
-#pragma unroll
-                    for (int q = 0; q < PER; ++q) {
-                        const int pidx = tid + q * CONSUMERS;
-                        if (pidx / ROWS >= T) continue;
-                        float sum = 0.f;
-                        for (int bb = bf; bb <= bl; ++bb) {
-                            float pv;
-                            if (bb == b) {
-                                pv = v[q];
-                            } else {
-                                const int wb2 = (cta_start(bb, U, B) >= ts) ? 0 : 1;
-                                pv = __ldcg(p.part + (static_cast<size_t>(bb) * 2 + wb2) * PART_FLOATS + pidx);
-                            }
-                            sum = (bb == bf) ? pv : sum + pv;
-                        }
-                        v[q] = sum;
-                    }
-                }
-            }
-
-            // 4. epilogue
-            if (finish) {
-                if constexpr (!HEAD) {
-#pragma unroll
-                    for (int q = 0; q < PER; ++q) {
-                        const int pidx = tid + q * CONSUMERS;
-                        const int tok = pidx / ROWS, row = pidx % ROWS;
-                        const long long rg = static_cast<long long>(tile) * ROWS + row;
-                        if (tok < T && rg < p.n_rows)
-                            p.y[static_cast<size_t>(tok) * p.n_rows + rg] =
-                                __bfloat16_as_ushort(__float2bfloat16_rn(v[q]));
-                    }
-                } else {
-                    const int32_t *ids = idbuf + (k_rel % 3) * ROWS;
-#pragma unroll
-                    for (int q = 0; q < PER; ++q) {
-                        const int pidx = tid + q * CONSUMERS;
-                        const int tok = pidx / ROWS, row = pidx % ROWS;   // tok is warp-uniform
-                        if (tok < T) {
-                            const int id = ids[row];
-                            unsigned long long k = id >= 0 ? make_key(v[q], static_cast<uint32_t>(id)) : 0ull;
-#pragma unroll
-                            for (int o = 16; o > 0; o >>= 1) {
-                                const unsigned long long ko = shfl_xor_u64(k, o);
-                                k = ko > k ? ko : k;
-                            }
-                            if (lane == 0 && k != 0ull) atomicMax(&best[tok], k);
-                        }
-                    }
-                }
-            }
-            if (C::RED_BUFS == 1) named_bar_sync(1, CONSUMERS);   // rbuf free again
-
-            // 5. metadata of tile k+2 into the buffers tile k used (free now)
-            if (tile + 2 <= tile_last) {
-                stage_tile_meta<HEAD>(p, tile + 2, idreg, sbuf + (k_rel & 1) * p.sbuf_bytes,
-                                      idbuf + ((k_rel + 2) % 3) * ROWS, cw, lane);
-                cp_async_commit();
-            }
-            tile_ids(p, tile + 3, tile_last, cw, idreg);
-            ++nflush;
-            ++k_rel;
-            ++tile;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(red_full));
+            ++k;
             grp = 0;
-        }
-    }
-
-    if constexpr (HEAD) {
-        // ==================================================== grid argmax + verify
-        named_bar_sync(1, CONSUMERS);
-        if (tid < T && best[tid] != 0ull) atomicMax(&p.keys[tid], best[tid]);
-        __threadfence();
-        named_bar_sync(1, CONSUMERS);
-        if (tid == 0) {
-            const unsigned old = atomicAdd(p.done, 1u);
-            flags[2] = (old == static_cast<unsigned>(B - 1));
-        }
-        named_bar_sync(1, CONSUMERS);
-        if (flags[2]) {
-            __threadfence();
-            int32_t *a = reinterpret_cast<int32_t *>(red);    // [TMAX] argmax ids
-            if (tid < T) {
-                const unsigned long long k = __ldcg(&p.keys[tid]);
-                a[tid] = (k == 0ull) ? -1 : key_id(k);
-                if (p.mode == 1) {
-                    p.ids[tid] = a[tid];
-                    if (p.vals) p.vals[tid] = (k == 0ull) ? __int_as_float(0x7fc00000) : key_value(k);
-                }
-                p.keys[tid] = 0ull;
-            }
-            named_bar_sync(1, CONSUMERS);
-            if (p.mode == 0 && tid < p.n_streams) {
-                const int rows_per = p.n_draft + 1;
-                const int32_t *as = a + tid * rows_per;
-                const int32_t *ds = p.drafts + static_cast<size_t>(tid) * p.n_draft;
-                int i = 0;
-                while (i < p.n_draft && ds[i] == as[i]) ++i;
-                p.accept_len[tid] = i;
-                p.next_token[tid] = as[i];
-            }
-            if (tid == 0) *p.done = 0u;
+            tile_start = true;
         }
     }
 }
