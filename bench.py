@@ -186,16 +186,34 @@ class Workload:
         self.bytes_per_step = sum(g["bytes"] for g in self.gemms) + self.head["bytes"]
         self.launches_per_step = len(self.gemms) + 1
 
-    def step(self, sv, stream, head_events=None):
+    def gemm_part(self, sv, stream):
         for g in self.gemms:
             sv.w4a16_gemm(g["x"], g["Wq"], g["sc"], y=g["y"], stream=stream)
+
+    def head_part(self, sv, stream):
         h = self.head
-        if head_events is not None:
-            head_events[0].record(stream)
         sv.lmhead_verify(h["x"], h["Wq"], h["sc"], h["drafts"], accept_len=h["acc"],
                          next_token=h["nxt"], stream=stream)
-        if head_events is not None:
-            head_events[1].record(stream)
+
+    def step(self, sv, stream):
+        self.gemm_part(sv, stream)
+        self.head_part(sv, stream)
+
+    def capture(self, torch, sv):
+        """Two CUDA graphs per step (the three GEMMs, then the head pass), as a
+        decode engine issues a verify cycle; the split lets the head's own
+        duration be timed between them."""
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        g1, g2 = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g1, stream=side):
+                self.gemm_part(sv, side)
+            with torch.cuda.graph(g2, stream=side):
+                self.head_part(sv, side)
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        return g1, g2
 
 
 # ----------------------------------------------------------------------------
@@ -320,23 +338,29 @@ def run_ours(args, rank, world, local_rank):
         wl.step(sv, stream)
         torch.cuda.synchronize()
 
+    g_gemm, g_head = wl.capture(torch, sv)
+    for _ in range(3):
+        g_gemm.replay()
+        g_head.replay()
+    torch.cuda.synchronize()
+    ev_mid = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev_end = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    head_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
     barrier()
     torch.cuda.synchronize()
     t_host0 = time.perf_counter()
     ev0.record(stream)
     for i in range(args.steps):
-        wl.step(sv, stream, head_events=head_ev[i])
-    ev1.record(stream)
+        g_gemm.replay()
+        ev_mid[i].record(stream)
+        g_head.replay()
+        ev_end[i].record(stream)
     torch.cuda.synchronize()
     t_host1 = time.perf_counter()
     barrier()
     sampler.stop()
-    ms = ev0.elapsed_time(ev1)
-    head_ms = float(np.mean([a.elapsed_time(b) for a, b in head_ev]))
+    ms = ev0.elapsed_time(ev_end[-1])
+    head_ms = float(np.mean([a.elapsed_time(b) for a, b in zip(ev_mid, ev_end)]))
     if dist is not None:
         t = torch.tensor([ms], device=device)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -411,6 +435,7 @@ def run_ours(args, rank, world, local_rank):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms, "steps": e2e_steps},
         "gpu_launches": wl.launches_per_step * args.steps,
+        "timing": "each step replays two CUDA graphs (3 GEMM launches, then the head launch)",
         "cpu_baseline": cpu,
     }
     if breakdown is not None:
@@ -440,7 +465,7 @@ def per_kernel_breakdown(torch, sv, device, stream, reps=50):
             Ws = [(dev(Wq, np.int32), dev(sc, np.int16)) for _ in range(copies)]
             x = dev(gen.activations(rng, T, K), np.int16)
             y = torch.empty((T, N), dtype=torch.bfloat16, device=device)
-            fn = lambda i: sv.w4a16_gemm(x, Ws[i % copies][0], Ws[i % copies][1], y=y, stream=stream)
+            fn = lambda i: sv.w4a16_gemm(x, Ws[i % copies][0], Ws[i % copies][1], y=y)
             nbytes = gen.gemm_bytes(T, K, N)
         else:
             Tt, S = T
@@ -452,25 +477,35 @@ def per_kernel_breakdown(torch, sv, device, stream, reps=50):
             drafts = torch.zeros((S, n_draft), dtype=torch.int32, device=device)
             vm = dev(gen.vocab_map(rng, N, gen.DRAFT_VOCAB), np.int32) if kind == "head_map" else None
             fn = lambda i: sv.lmhead_verify_batched(x, Ws[i % copies][0], Ws[i % copies][1], drafts,
-                                                    vocab_map=vm, stream=stream)
+                                                    vocab_map=vm)
             n_map = gen.DRAFT_VOCAB if vm is not None else 0
             nbytes = gen.lmhead_bytes(N, K, Tt, n_map=n_map, n_streams=S, n_draft=n_draft)
             T = Tt
         for i in range(5):
             fn(i)
         torch.cuda.synchronize()
+        # one graph of `reps` back-to-back launches (rotating weight copies)
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(graph, stream=side):
+                for i in range(reps):
+                    fn(i)
+        stream.wait_stream(side)
+        graph.replay()
+        torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for i in range(reps):
-            fn(i)
+        graph.replay()
         e1.record(stream)
         torch.cuda.synchronize()
         us = e0.elapsed_time(e1) * 1e3 / reps
         gbs = nbytes / (us * 1e-6) / 1e9
         out.append({"kernel": kind, "shape": label, "K": K, "N": N, "T": T, "us": round(us, 2),
                     "GB/s": round(gbs, 1), "frac_8TBps": round(gbs / NOMINAL_HBM_GBS, 3)})
-        del Ws
+        del Ws, graph
         torch.cuda.empty_cache()
     return out
 

@@ -32,10 +32,10 @@ struct DeviceState {
 DeviceState g_state[MAX_DEVICES];
 std::mutex g_mu;
 
-template <int NT, bool HEAD, bool GATHER>
+template <int NT, bool HEAD, bool GATHER, bool XRES>
 cudaError_t raise_smem_limit(int bytes)
 {
-    return cudaFuncSetAttribute(w4a16_stream_kernel<NT, HEAD, GATHER>,
+    return cudaFuncSetAttribute(w4a16_stream_kernel<NT, HEAD, GATHER, XRES>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
@@ -109,15 +109,18 @@ int device_state(DeviceState **out)
         off += sizeof(unsigned);
         st.err = reinterpret_cast<int *>(base + off);
         cudaError_t e = cudaSuccess;
-        e = e != cudaSuccess ? e : raise_smem_limit<1, false, false>(optin);
-        e = e != cudaSuccess ? e : raise_smem_limit<2, false, false>(optin);
-        e = e != cudaSuccess ? e : raise_smem_limit<4, false, false>(optin);
-        e = e != cudaSuccess ? e : raise_smem_limit<1, true, false>(optin);
-        e = e != cudaSuccess ? e : raise_smem_limit<2, true, false>(optin);
-        e = e != cudaSuccess ? e : raise_smem_limit<4, true, false>(optin);
-        e = e != cudaSuccess ? e : raise_smem_limit<1, true, true>(optin);
-        e = e != cudaSuccess ? e : raise_smem_limit<2, true, true>(optin);
-        e = e != cudaSuccess ? e : raise_smem_limit<4, true, true>(optin);
+        e = e != cudaSuccess ? e : raise_smem_limit<1, false, false, false>(optin);
+        e = e != cudaSuccess ? e : raise_smem_limit<1, false, false, true>(optin);
+        e = e != cudaSuccess ? e : raise_smem_limit<2, false, false, false>(optin);
+        e = e != cudaSuccess ? e : raise_smem_limit<4, false, false, false>(optin);
+        e = e != cudaSuccess ? e : raise_smem_limit<1, true, false, false>(optin);
+        e = e != cudaSuccess ? e : raise_smem_limit<1, true, false, true>(optin);
+        e = e != cudaSuccess ? e : raise_smem_limit<2, true, false, false>(optin);
+        e = e != cudaSuccess ? e : raise_smem_limit<4, true, false, false>(optin);
+        e = e != cudaSuccess ? e : raise_smem_limit<1, true, true, false>(optin);
+        e = e != cudaSuccess ? e : raise_smem_limit<1, true, true, true>(optin);
+        e = e != cudaSuccess ? e : raise_smem_limit<2, true, true, false>(optin);
+        e = e != cudaSuccess ? e : raise_smem_limit<4, true, true, false>(optin);
         if (e != cudaSuccess || tensor_map_fn() != SV_OK) {
             cudaFree(base);
             return SV_ERR_CUDA;
@@ -134,24 +137,29 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 // Shared-memory layout of one launch (offsets in bytes, 128-byte aligned):
-// nst pipeline stages | scales of 2 tiles | token ids of 2 tiles | the
-// consumers' partial sums of one tile | mbarriers and a flag.
-template <int NT, bool GATHER>
+// nst pipeline stages | resident activations (XRES) | scales of 2 tiles |
+// token ids of 2 tiles | the consumers' partial sums of one tile | mbarriers
+// and a flag.
+template <int NT, bool GATHER, bool XRES>
 int plan_layout(Params &p, int smem_optin, int *smem_total)
 {
     using C = Cfg<NT, GATHER>;
     auto up = [](int v, int a) { return (v + a - 1) / a * a; };
     p.xslot_bytes = up(C::TP * XROW_BYTES, 128);
-    p.stage_bytes = up(C::W_BYTES + C::GPS * p.xslot_bytes, 128);
+    p.stage_bytes = XRES ? C::W_BYTES : up(C::W_BYTES + C::GPS * p.xslot_bytes, 128);
     p.sbuf_bytes = up(ROWS * p.G * 2, 128);
+    p.xres_stride = 2 * p.K + 16;                     // = 16 (mod 128)
+    const int xres_bytes = XRES ? up((p.T + 1) * p.xres_stride, 128) : 0;
     const int ids_bytes = up(2 * ROWS * 4, 128);
     const int red_bytes = up(C::RED_FLOATS * 4, 128);
-    const int fixed = 2 * p.sbuf_bytes + ids_bytes + red_bytes + 7 * 8 + 8;
+    const int fixed = xres_bytes + 2 * p.sbuf_bytes + ids_bytes + red_bytes + 7 * 8 + 8;
     int nst = (smem_optin - fixed - 1024) / (p.stage_bytes + 16);
     if (nst > 8) nst = 8;
     if (nst < 2) return SV_ERR_SHAPE;
     p.nst = nst;
     int off = nst * p.stage_bytes;
+    p.off_xres = off;
+    off += xres_bytes;
     p.off_sbuf = off;
     off += 2 * p.sbuf_bytes;
     p.off_ids = off;
@@ -164,26 +172,32 @@ int plan_layout(Params &p, int smem_optin, int *smem_total)
     return off <= smem_optin ? SV_OK : SV_ERR_SHAPE;
 }
 
-template <int NT, bool HEAD, bool GATHER>
+// Resident activations pay off when they fit with at least 3 weight stages.
+constexpr int XRES_MAX_BYTES = 100 * 1024;
+
+template <int NT, bool HEAD, bool GATHER, bool XRES>
 int launch(Params p, const DeviceState &st, cudaStream_t stream)
 {
     int smem = 0;
-    int rc = plan_layout<NT, GATHER>(p, st.smem_optin, &smem);
+    int rc = plan_layout<NT, GATHER, XRES>(p, st.smem_optin, &smem);
     if (rc != SV_OK) return rc;
     CUtensorMap tmW, tmX;
     std::memset(&tmW, 0, sizeof tmW);
+    std::memset(&tmX, 0, sizeof tmX);
     if (!GATHER) {
         rc = encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, p.Wq,
                        static_cast<unsigned long long>(p.K / 8), static_cast<unsigned long long>(p.n_rows),
                        16, ROWS);
         if (rc != SV_OK) return rc;
     }
-    // The activation box is exactly T rows high (boxes reaching past the
-    // tensor are much slower to fill); the kernel zeroes the spare token rows
-    // of every stage once, so B fragments can be loaded unconditionally.
-    rc = encode_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, p.x, static_cast<unsigned long long>(p.K),
-                   static_cast<unsigned long long>(p.T), XBOX, static_cast<unsigned>(p.T));
-    if (rc != SV_OK) return rc;
+    if (!XRES) {
+        // The activation box is exactly T rows high (boxes reaching past the
+        // tensor are much slower to fill); the kernel zeroes the spare token
+        // rows of every stage once, so B fragments load unconditionally.
+        rc = encode_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, p.x, static_cast<unsigned long long>(p.K),
+                       static_cast<unsigned long long>(p.T), XBOX, static_cast<unsigned>(p.T));
+        if (rc != SV_OK) return rc;
+    }
     long long B = st.sms;
     if (B > p.U) B = p.U;
     p.part = st.part;
@@ -191,16 +205,20 @@ int launch(Params p, const DeviceState &st, cudaStream_t stream)
     p.keys = st.keys;
     p.done = st.done;
     p.err = st.err;
-    w4a16_stream_kernel<NT, HEAD, GATHER><<<static_cast<unsigned>(B), NTHREADS, smem, stream>>>(p, tmW, tmX);
+    w4a16_stream_kernel<NT, HEAD, GATHER, XRES><<<static_cast<unsigned>(B), NTHREADS, smem, stream>>>(p, tmW, tmX);
     return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
 template <bool HEAD, bool GATHER>
 int dispatch(Params &p, const DeviceState &st, cudaStream_t stream)
 {
-    if (p.T <= 8) return launch<1, HEAD, GATHER>(p, st, stream);
-    if (p.T <= 16) return launch<2, HEAD, GATHER>(p, st, stream);
-    return launch<4, HEAD, GATHER>(p, st, stream);
+    if (p.T <= 8) {
+        if (static_cast<long long>(p.T + 1) * (2LL * p.K + 16) <= XRES_MAX_BYTES)
+            return launch<1, HEAD, GATHER, true>(p, st, stream);
+        return launch<1, HEAD, GATHER, false>(p, st, stream);
+    }
+    if (p.T <= 16) return launch<2, HEAD, GATHER, false>(p, st, stream);
+    return launch<4, HEAD, GATHER, false>(p, st, stream);
 }
 
 int check_common(const void *x, const void *Wq, const void *scales, int T, int K)

@@ -78,6 +78,7 @@ struct Params {
     // shared-memory layout (bytes)
     int nst, stage_bytes, xslot_bytes, sbuf_bytes;
     int off_sbuf, off_ids, off_red, off_bars;
+    int off_xres, xres_stride;  // resident activations (XRES kernels only)
     // GEMM output
     uint16_t *y;                // [T][N]
     // HEAD outputs
@@ -177,12 +178,13 @@ __device__ __forceinline__ void stage_tile_meta(const Params &p, int tile, uint8
     if (lane == 0) mbar_arrive(bar);
 }
 
-template <int NT, bool HEAD, bool GATHER>
+template <int NT, bool HEAD, bool GATHER, bool XRES>
 __global__ void __launch_bounds__(NTHREADS, 1)
 w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tmW,
                     const __grid_constant__ CUtensorMap tmX)
 {
     using C = Cfg<NT, GATHER>;
+    static_assert(!XRES || NT == 1, "resident activations are laid out for one n8 token tile");
     extern __shared__ __align__(1024) uint8_t smem[];
     const int nst = p.nst;
     uint8_t *sbuf = smem + p.off_sbuf;                                // [2][sbuf_bytes]
@@ -223,7 +225,7 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
     }
     // Token rows T..TP-1 of every stage's activation slots stay zero for the
     // whole kernel (the tensor copies only write rows 0..T-1).
-    if (T < C::TP) {
+    if (!XRES && T < C::TP) {
         const int per_slot = (C::TP - T) * XROW_BYTES / 16;
         const int total = nst * C::GPS * per_slot;
         for (int i = threadIdx.x; i < total; i += NTHREADS) {
@@ -243,7 +245,7 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
         const uint64_t pol_x = policy_evict_last();
         if (lane == 0) {
             if (!GATHER) prefetch_tmap(&tmW);
-            prefetch_tmap(&tmX);
+            if (!XRES) prefetch_tmap(&tmX);
         }
         int s = 0, issued = 0, tile = tile_first, grp = grp_first, rem = n_units;
         uint32_t ph = 0;
@@ -270,7 +272,8 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
             } else {
                 wbytes = static_cast<uint32_t>(n * ROWS * 64);
             }
-            if (lane == 0) mbar_arrive_expect_tx(fb, wbytes + static_cast<uint32_t>(n * T * XROW_BYTES));
+            const uint32_t xbytes = XRES ? 0u : static_cast<uint32_t>(n * T * XROW_BYTES);
+            if (lane == 0) mbar_arrive_expect_tx(fb, wbytes + xbytes);
             __syncwarp();
             if (GATHER) {
 #pragma unroll
@@ -282,7 +285,7 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
             } else if (lane < n) {
                 tma_load_2d(stage + lane * (ROWS * 64), &tmW, (grp + lane) * 16, tile * ROWS, fb, pol_w);
             }
-            if (lane >= 16 && lane - 16 < n)
+            if (!XRES && lane >= 16 && lane - 16 < n)
                 tma_load_2d(stage + C::W_BYTES + (lane - 16) * p.xslot_bytes, &tmX,
                             (grp + lane - 16) * 128, 0, fb, pol_x);
             rem -= n;
@@ -470,6 +473,36 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
     const uint32_t sbuf0 = smem_addr(sbuf);
     const uint32_t smem0 = smem_addr(smem);
 
+    // Resident activations: x[t] is stored once per CTA as rows of 16-byte
+    // chunks, each chunk holding its 8 values in B-fragment order
+    // (x0,x4, x1,x5, x2,x6, x3,x7), chunk index XOR-swizzled (bit 1 ^= bit 3)
+    // and rows padded to 16 (mod 128) bytes, so that the B loads below are
+    // conflict-free and need no byte permutes.  Row T is zeros, read by the
+    // lanes of absent tokens.
+    uint32_t xr_lane = 0, xr_off[4] = {0, 0, 0, 0};
+    if constexpr (XRES) {
+        uint8_t *xr = smem + p.off_xres;
+        const int chunks_per_row = p.K / 8;
+        const int nchunks = (T + 1) * chunks_per_row;
+        for (int i = cw * 32 + lane; i < nchunks; i += NCW * 32) {
+            const int t = i / chunks_per_row, w = i - t * chunks_per_row;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (t < T) {
+                const uint4 r = *reinterpret_cast<const uint4 *>(p.x + static_cast<size_t>(t) * p.K + 8 * w);
+                v.x = __byte_perm(r.x, r.z, 0x5410);
+                v.y = __byte_perm(r.x, r.z, 0x7632);
+                v.z = __byte_perm(r.y, r.w, 0x5410);
+                v.w = __byte_perm(r.y, r.w, 0x7632);
+            }
+            const int sw = w ^ ((w >> 2) & 2);
+            *reinterpret_cast<uint4 *>(xr + static_cast<size_t>(t) * p.xres_stride + sw * 16) = v;
+        }
+        named_bar_sync(1, NCW * 32);
+        xr_lane = smem_addr(xr) + static_cast<uint32_t>((g < T ? g : T) * p.xres_stride);
+#pragma unroll
+        for (int m = 0; m < 4; ++m) xr_off[m] = static_cast<uint32_t>((4 * c + (m ^ (c & 2))) * 16);
+    }
+
     float acc[C::R][NT][4];
 #pragma unroll
     for (int r = 0; r < C::R; ++r)
@@ -507,20 +540,28 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
 #pragma unroll
                     for (int e = 0; e < 4; ++e) gacc[r][nt][e] = 0.f;
 
-            const uint32_t xbase = stage + x_lane;
+            const uint32_t xbase = XRES ? xr_lane + gs * 256 : stage + x_lane;
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
                 // B fragments: token (nt*8 + g), the 8 activations of word
                 // (4c + m) of the group, paired (j, j+4) like the nibbles.
-                // Token rows >= T are zeros (filled by the tensor copy).
+                // Token rows >= T are zeros.
                 uint32_t bx[NT][4];
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    const uint4 v = lds128(xbase + nt * 8 * XROW_BYTES + m * 16);
-                    bx[nt][0] = __byte_perm(v.x, v.z, 0x5410);   // (x0, x4)
-                    bx[nt][1] = __byte_perm(v.x, v.z, 0x7632);   // (x1, x5)
-                    bx[nt][2] = __byte_perm(v.y, v.w, 0x5410);   // (x2, x6)
-                    bx[nt][3] = __byte_perm(v.y, v.w, 0x7632);   // (x3, x7)
+                    if constexpr (XRES) {
+                        const uint4 v = lds128(xbase + xr_off[m]);
+                        bx[nt][0] = v.x;
+                        bx[nt][1] = v.y;
+                        bx[nt][2] = v.z;
+                        bx[nt][3] = v.w;
+                    } else {
+                        const uint4 v = lds128(xbase + nt * 8 * XROW_BYTES + m * 16);
+                        bx[nt][0] = __byte_perm(v.x, v.z, 0x5410);   // (x0, x4)
+                        bx[nt][1] = __byte_perm(v.x, v.z, 0x7632);   // (x1, x5)
+                        bx[nt][2] = __byte_perm(v.y, v.w, 0x5410);   // (x2, x6)
+                        bx[nt][3] = __byte_perm(v.y, v.w, 0x7632);   // (x3, x7)
+                    }
                 }
 #pragma unroll
                 for (int r = 0; r < C::R; ++r) {
