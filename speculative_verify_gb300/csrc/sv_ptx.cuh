@@ -150,6 +150,22 @@ __device__ __forceinline__ void cp_async_wait_all()
     asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- gpu-scope atomics
+
+// atomicAdd with acquire-release semantics at GPU scope: orders this
+// thread's earlier writes before the add and later reads after it.
+__device__ __forceinline__ unsigned atomic_add_acq_rel_gpu(unsigned *p, unsigned v)
+{
+    unsigned old;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ float4 ldcg_f4(const float *p)
+{
+    return __ldcg(reinterpret_cast<const float4 *>(p));
+}
+
 // ---------------------------------------------------------------- named barriers
 
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads)

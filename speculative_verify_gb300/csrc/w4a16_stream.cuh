@@ -330,75 +330,132 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
             wait_or_flag(p, flag, smem_addr(red_full), static_cast<uint32_t>(k & 1));
             const long long ts = static_cast<long long>(tile) * G, te = ts + G;
             const bool complete = (u0 <= ts) && (u1 >= te);
-            // Sum the group slots (fixed order) for rows lane and lane+32.
-            // Split tiles are published and possibly finished first.
-            int bf = 0, bl = 0;
+            // This CTA's sums of the group slots (fixed slot order) for rows
+            // lane and lane+32 of every token, kept as v[t][h] in registers
+            // for the tokens being processed (chunks of 4).
+            // Split tiles: the partial goes to the scratch area as
+            // [row][TMAX] floats; the CTA that arrives last adds all the
+            // tile's partials in CTA order (fixed, so results are
+            // deterministic) with vectorised loads issued together.
+            int bf = 0, nc = 1;
             bool finish = true;
+            const float *others[4] = {nullptr, nullptr, nullptr, nullptr};
             if (!complete) {
                 bf = cta_of(ts, U, B);
-                bl = cta_of(te - 1, U, B);
+                const int bl = cta_of(te - 1, U, B);
+                nc = bl - bf + 1;
                 float *mine = p.part + (static_cast<size_t>(b) * 2 + (tile == tile_first ? 0 : 1)) * PART_FLOATS;
-                for (int t = 0; t < T; ++t)
+                for (int t0 = 0; t0 < T; t0 += 4) {
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const int row = lane + 32 * h;
-                        float sum = red[t * ROWS + row];
+                        float q[4];
 #pragma unroll
-                        for (int sl = 1; sl < C::GPS; ++sl) sum += red[(sl * C::TP + t) * ROWS + row];
-                        mine[t * ROWS + row] = sum;
+                        for (int j = 0; j < 4; ++j) {
+                            const int t = t0 + j;
+                            float sum = 0.f;
+                            if (t < T) {
+                                sum = red[t * ROWS + row];
+#pragma unroll
+                                for (int sl = 1; sl < C::GPS; ++sl) sum += red[(sl * C::TP + t) * ROWS + row];
+                            }
+                            q[j] = sum;
+                        }
+                        *reinterpret_cast<float4 *>(mine + row * TMAX + t0) = make_float4(q[0], q[1], q[2], q[3]);
                     }
+                }
                 __threadfence();
                 __syncwarp();
                 unsigned last = 0;
                 if (lane == 0) {
-                    const unsigned old = atomicAdd(&p.ctr[bf], 1u);
-                    last = (old == static_cast<unsigned>(bl - bf));
-                    if (last) atomicExch(&p.ctr[bf], 0u);
+                    const unsigned old = atomic_add_acq_rel_gpu(&p.ctr[bf], 1u);
+                    last = (old == static_cast<unsigned>(nc - 1));
+                    if (last) p.ctr[bf] = 0u;          // ready for the next launch
                 }
                 finish = __shfl_sync(0xFFFFFFFFu, last, 0) != 0;
-                if (finish) __threadfence();
+                if (finish) {
+                    __threadfence();
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int bb = bf + j;
+                        const int wb2 = (j < nc && cta_start(bb, U, B) >= ts) ? 0 : 1;
+                        others[j] = p.part + (static_cast<size_t>(bb) * 2 + wb2) * PART_FLOATS;
+                    }
+                }
             }
             const int32_t *ids = idbuf + kb * ROWS;
             const int id0 = HEAD ? ids[lane] : 0, id1 = HEAD ? ids[lane + 32] : 0;
-            for (int t = 0; t < T && finish; ++t) {
-                float v[2];
+            for (int t0 = 0; t0 < T && finish; t0 += 4) {
+                float v[4][2];
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const int row = lane + 32 * h;
                     if (complete) {
-                        float sum = red[t * ROWS + row];
 #pragma unroll
-                        for (int sl = 1; sl < C::GPS; ++sl) sum += red[(sl * C::TP + t) * ROWS + row];
-                        v[h] = sum;
-                    } else {
-                        float sum = 0.f;
-                        for (int bb = bf; bb <= bl; ++bb) {
-                            const int wb2 = (cta_start(bb, U, B) >= ts) ? 0 : 1;
-                            const float pv = __ldcg(p.part + (static_cast<size_t>(bb) * 2 + wb2) * PART_FLOATS +
-                                                    t * ROWS + row);
-                            sum = (bb == bf) ? pv : sum + pv;
+                        for (int j = 0; j < 4; ++j) {
+                            const int t = t0 + j;
+                            float sum = 0.f;
+                            if (t < T) {
+                                sum = red[t * ROWS + row];
+#pragma unroll
+                                for (int sl = 1; sl < C::GPS; ++sl) sum += red[(sl * C::TP + t) * ROWS + row];
+                            }
+                            v[j][h] = sum;
                         }
-                        v[h] = sum;
+                    } else {
+                        // all contributors' float4s first, then the ordered sum
+                        float4 pv[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            if (j < nc) pv[j] = ldcg_f4(others[j] + row * TMAX + t0);
+                        float4 acc4 = pv[0];
+#pragma unroll
+                        for (int j = 1; j < 4; ++j)
+                            if (j < nc) {
+                                acc4.x += pv[j].x;
+                                acc4.y += pv[j].y;
+                                acc4.z += pv[j].z;
+                                acc4.w += pv[j].w;
+                            }
+                        for (int j = 4; j < nc; ++j) {      // more than 4 CTAs on one tile (small K)
+                            const int bb = bf + j;
+                            const int wb2 = (cta_start(bb, U, B) >= ts) ? 0 : 1;
+                            const float4 e = ldcg_f4(p.part + (static_cast<size_t>(bb) * 2 + wb2) * PART_FLOATS +
+                                                     row * TMAX + t0);
+                            acc4.x += e.x;
+                            acc4.y += e.y;
+                            acc4.z += e.z;
+                            acc4.w += e.w;
+                        }
+                        v[0][h] = acc4.x;
+                        v[1][h] = acc4.y;
+                        v[2][h] = acc4.z;
+                        v[3][h] = acc4.w;
                     }
                 }
-                if constexpr (!HEAD) {
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const long long rg = static_cast<long long>(tile) * ROWS + lane + 32 * h;
-                        if (rg < p.n_rows)
-                            p.y[static_cast<size_t>(t) * p.n_rows + rg] =
-                                __bfloat16_as_ushort(__float2bfloat16_rn(v[h]));
-                    }
-                } else {
-                    unsigned long long k0 = id0 >= 0 ? make_key(v[0], static_cast<uint32_t>(id0)) : 0ull;
-                    unsigned long long k1 = id1 >= 0 ? make_key(v[1], static_cast<uint32_t>(id1)) : 0ull;
-                    unsigned long long kk = k0 > k1 ? k0 : k1;
+                for (int j = 0; j < 4; ++j) {
+                    const int t = t0 + j;
+                    if (t >= T) break;
+                    if constexpr (!HEAD) {
 #pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) {
-                        const unsigned long long ko = shfl_xor_u64(kk, o);
-                        kk = ko > kk ? ko : kk;
+                        for (int h = 0; h < 2; ++h) {
+                            const long long rg = static_cast<long long>(tile) * ROWS + lane + 32 * h;
+                            if (rg < p.n_rows)
+                                p.y[static_cast<size_t>(t) * p.n_rows + rg] =
+                                    __bfloat16_as_ushort(__float2bfloat16_rn(v[j][h]));
+                        }
+                    } else {
+                        unsigned long long k0 = id0 >= 0 ? make_key(v[j][0], static_cast<uint32_t>(id0)) : 0ull;
+                        unsigned long long k1 = id1 >= 0 ? make_key(v[j][1], static_cast<uint32_t>(id1)) : 0ull;
+                        unsigned long long kk = k0 > k1 ? k0 : k1;
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) {
+                            const unsigned long long ko = shfl_xor_u64(kk, o);
+                            kk = ko > kk ? ko : kk;
+                        }
+                        if (lane == t && kk > best) best = kk;
                     }
-                    if (lane == t && kk > best) best = kk;
                 }
             }
             __syncwarp();
