@@ -205,8 +205,26 @@ int launch(Params p, const DeviceState &st, cudaStream_t stream)
     p.keys = st.keys;
     p.done = st.done;
     p.err = st.err;
-    w4a16_stream_kernel<NT, HEAD, GATHER, XRES><<<static_cast<unsigned>(B), NTHREADS, smem, stream>>>(p, tmW, tmX);
-    return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+    // Programmatic dependent launch: the kernel may begin while the previous
+    // kernel of the stream drains; it waits (griddepcontrol.wait) before it
+    // touches anything that kernel could have written.
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3(static_cast<unsigned>(B));
+    cfg.blockDim = dim3(NTHREADS);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, w4a16_stream_kernel<NT, HEAD, GATHER, XRES>, p, tmW, tmX);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return SV_ERR_CUDA;
+    }
+    return SV_OK;
 }
 
 template <bool HEAD, bool GATHER>

@@ -166,6 +166,21 @@ __device__ __forceinline__ float4 ldcg_f4(const float *p)
     return __ldcg(reinterpret_cast<const float4 *>(p));
 }
 
+// ---------------------------------------------------------------- dependent launch
+
+// Let the next kernel in the stream start launching its CTAs now.
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Wait until the previous kernel in the stream has completed and its writes
+// are visible (a no-op when this kernel was not launched as a dependent).
+__device__ __forceinline__ void pdl_wait_prior()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- named barriers
 
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads)

@@ -30,6 +30,13 @@
 //    argmax; at the end it runs the grid-level argmax and the verify.
 // Every weight byte crosses HBM once per call; T only changes how many n8
 // token tiles each dequantised fragment multiplies.
+//
+// Back-to-back launches overlap (programmatic dependent launch): a CTA may
+// start while the previous kernel of the stream is still finishing, and it
+// streams packed weights and scales -- read-only model data -- right away.
+// Everything that a preceding kernel may produce or use (activations, drafts,
+// the vocab_map, the scratch area, the outputs) is touched only after
+// griddepcontrol.wait.
 #pragma once
 
 #include <cstdint>
@@ -238,6 +245,7 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
         fence_proxy_async();
     }
     __syncthreads();
+    pdl_launch_dependents();
 
     if (warp == PRODUCER_WARP) {
         // ============================================================ producer
@@ -249,6 +257,11 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
         }
         int s = 0, issued = 0, tile = tile_first, grp = grp_first, rem = n_units;
         uint32_t ph = 0;
+        bool waited = false;
+        if (GATHER) {
+            pdl_wait_prior();       // the id list may come from the previous kernel
+            waited = true;
+        }
         // gathered rows: ids of this lane's two rows, for this tile and the next
         int gid[2] = {-1, -1}, gid_next[2] = {-1, -1};
         if (GATHER) {
@@ -285,6 +298,10 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
             } else if (lane < n) {
                 tma_load_2d(stage + lane * (ROWS * 64), &tmW, (grp + lane) * 16, tile * ROWS, fb, pol_w);
             }
+            if (!XRES && !waited) {
+                pdl_wait_prior();   // activations may come from the previous kernel
+                waited = true;
+            }
             if (!XRES && lane >= 16 && lane - 16 < n)
                 tma_load_2d(stage + C::W_BYTES + (lane - 16) * p.xslot_bytes, &tmX,
                             (grp + lane - 16) * 128, 0, fb, pol_x);
@@ -320,11 +337,13 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
 
     if (warp == EPILOGUE_WARP) {
         // ============================================================ epilogue
+        if (GATHER) pdl_wait_prior();   // the id list may come from the previous kernel
         stage_tile_meta<HEAD, GATHER>(p, tile_first, sbuf, idbuf, smem_addr(&meta_full[0]), lane);
         if (tile_first + 1 <= tile_last)
             stage_tile_meta<HEAD, GATHER>(p, tile_first + 1, sbuf + p.sbuf_bytes, idbuf + ROWS,
                                           smem_addr(&meta_full[1]), lane);
         unsigned long long best = 0ull;    // lane t: best key of token t so far
+        pdl_wait_prior();                  // scratch area, outputs and drafts from here on
         for (int k = 0, tile = tile_first; tile <= tile_last; ++k, ++tile) {
             const int kb = k & 1;
             wait_or_flag(p, flag, smem_addr(red_full), static_cast<uint32_t>(k & 1));
@@ -538,6 +557,7 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
     // lanes of absent tokens.
     uint32_t xr_lane = 0, xr_off[4] = {0, 0, 0, 0};
     if constexpr (XRES) {
+        pdl_wait_prior();                  // activations may come from the previous kernel
         uint8_t *xr = smem + p.off_xres;
         const int chunks_per_row = p.K / 8;
         const int nchunks = (T + 1) * chunks_per_row;
