@@ -135,6 +135,34 @@ int lmhead_argmax(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, i
                   int T, const int32_t *vocab_map, int n_map, int V,
                   int32_t *ids, float *vals, sv_stream stream);
 
+/*
+ * lmhead_verify_noalloc -- the same greedy verify as lmhead_verify, for
+ * callers that must not allocate GPU memory: code running under CUDA-graph
+ * stream capture (where a first-call cudaMalloc is not allowed), serving
+ * runtimes that own every byte of device memory through their own arena
+ * and forbid stray allocations, and latency-critical paths that cannot
+ * afford cudaMalloc's implicit device synchronisation.  No source page has
+ * a counterpart to this entry point; it exists for this library's users.
+ *   Arguments, layouts and results are those of lmhead_verify.
+ *   Scratch: a fixed device array inside the library (about 2.6 MB per
+ *   device, held until the process exits), sized for at most 160 thread
+ *   blocks and 32 verify rows; the call launches at most 160 blocks and
+ *   rejects more than 31 drafts with SV_ERR_SHAPE.  It calls no cudaMalloc,
+ *   cudaFree or other allocating routine.
+ *   The first call on a device resolves the array's device address and
+ *   sets kernel attributes (no allocation, but make that first call outside
+ *   stream capture).  Each call clears the array's counters with an
+ *   asynchronous memset on `stream` before its kernel.
+ *   All calls share the one array: calls that overlap on the GPU (two
+ *   streams, or two host threads) race on it and must be ordered by the
+ *   caller.  Device-side problems (a bad vocab_map id is skipped) are not
+ *   reported through sv_last_device_error by this variant.
+ */
+int lmhead_verify_noalloc(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, int K,
+                          const int32_t *drafts, int n_draft,
+                          const int32_t *vocab_map, int n_map, int V,
+                          int32_t *accept_len, int32_t *next_token, sv_stream stream);
+
 /* A static, human-readable name for a status code. */
 const char *sv_status_string(int status);
 

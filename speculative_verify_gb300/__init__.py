@@ -55,6 +55,8 @@ def load(path: str | None = None):
     lib.lmhead_verify.restype = ci
     lib.lmhead_verify_batched.argtypes = [vp, vp, vp, ci, vp, ci, ci, vp, ci, ci, vp, vp, vp]
     lib.lmhead_verify_batched.restype = ci
+    lib.lmhead_verify_noalloc.argtypes = [vp, vp, vp, ci, vp, ci, vp, ci, ci, vp, vp, vp]
+    lib.lmhead_verify_noalloc.restype = ci
     lib.lmhead_argmax.argtypes = [vp, vp, vp, ci, ci, vp, ci, ci, vp, vp, vp]
     lib.lmhead_argmax.restype = ci
     lib.sv_status_string.argtypes = [ci]
@@ -198,6 +200,36 @@ def lmhead_verify(x, Wq, scales, drafts, vocab_map=None, accept_len=None, next_t
         next_token = torch.empty(1, dtype=torch.int32, device=x.device)
     n_map = 0 if vocab_map is None else vocab_map.numel()
     _check("lmhead_verify", load().lmhead_verify(
+        _ptr(x), _ptr(Wq), _ptr(scales), K, _ptr(drafts) if n_draft else None, n_draft,
+        _ptr(vocab_map), n_map, V, _ptr(accept_len), _ptr(next_token), _stream(stream)))
+    return accept_len, next_token
+
+
+def lmhead_verify_noalloc(x, Wq, scales, drafts, vocab_map=None, accept_len=None,
+                          next_token=None, stream=None):
+    """lmhead_verify for callers that cannot allocate device memory: the
+    kernel's scratch is a fixed array inside the library.  Pass accept_len and
+    next_token (one-element int32 CUDA tensors) to keep the call itself free of
+    allocations."""
+    torch = _torch()
+    _bits16(x, "x"), _words(Wq, "Wq"), _bits16(scales, "scales")
+    T, K = x.shape
+    V = Wq.shape[0]
+    n_draft = drafts.numel()
+    if T != n_draft + 1:
+        raise ValueError("x must have 1 + n_draft rows")
+    if Wq.shape[1] * 8 != K or tuple(scales.shape) != (V, K // 128):
+        raise ValueError("shape mismatch between x, Wq and scales")
+    if n_draft:
+        _i32(drafts, "drafts")
+    if vocab_map is not None:
+        _i32(vocab_map, "vocab_map")
+    if accept_len is None:
+        accept_len = torch.empty(1, dtype=torch.int32, device=x.device)
+    if next_token is None:
+        next_token = torch.empty(1, dtype=torch.int32, device=x.device)
+    n_map = 0 if vocab_map is None else vocab_map.numel()
+    _check("lmhead_verify_noalloc", load().lmhead_verify_noalloc(
         _ptr(x), _ptr(Wq), _ptr(scales), K, _ptr(drafts) if n_draft else None, n_draft,
         _ptr(vocab_map), n_map, V, _ptr(accept_len), _ptr(next_token), _stream(stream)))
     return accept_len, next_token

@@ -294,10 +294,131 @@ int head_call(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, int K
     return vocab_map ? dispatch<true, true>(p, *st, stream) : dispatch<true, false>(p, *st, stream);
 }
 
+// ----------------------------------------------------------------------------
+// Allocation-free variant of the verify (lmhead_verify_noalloc).
+//
+// Its scratch -- split-tile partial sums, arrival counters, argmax keys --
+// lives in the file-scope device array below instead of a cudaMalloc'd
+// area, so the call never allocates.  The array is sized for at most
+// NOALLOC_MAX_CTAS thread blocks (each keeps two 32-token partial tiles);
+// the call never launches more blocks than that.  Every device that loads
+// this library holds the array (about 2.6 MB) until the process exits.
+
+constexpr int NOALLOC_MAX_CTAS = 160;
+constexpr size_t NOALLOC_PART_BYTES = static_cast<size_t>(NOALLOC_MAX_CTAS) * 2 * PART_FLOATS * sizeof(float);
+constexpr size_t NOALLOC_CTR_OFF = NOALLOC_PART_BYTES;
+constexpr size_t NOALLOC_KEYS_OFF = NOALLOC_CTR_OFF + 1024;                 // 160 counters, padded
+constexpr size_t NOALLOC_DONE_OFF = NOALLOC_KEYS_OFF + TMAX * sizeof(unsigned long long);
+constexpr size_t NOALLOC_ERR_OFF = NOALLOC_DONE_OFF + 256;
+constexpr size_t NOALLOC_BYTES = NOALLOC_ERR_OFF + 256;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_BYTES];
+
+DeviceState g_noalloc_state[MAX_DEVICES];
+
+// Once per device, with that device current: resolve the array's device
+// address (the array's name is only a host-side stand-in), and raise the
+// shared-memory limit of the head kernels.  Nothing here allocates.
+int noalloc_state(DeviceState **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_CUDA;
+    if (dev < 0 || dev >= MAX_DEVICES) return SV_ERR_DEVICE;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState &st = g_noalloc_state[dev];
+    if (!st.ready) {
+        int major = 0, sms = 0, optin = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            return SV_ERR_CUDA;
+        if (major != 10) return SV_ERR_DEVICE;
+        unsigned char *base = nullptr;
+        if (cudaGetSymbolAddress(reinterpret_cast<void **>(&base), g_noalloc_scratch) != cudaSuccess) {
+            cudaGetLastError();
+            return SV_ERR_CUDA;
+        }
+        cudaError_t e = cudaSuccess;
+        e = e != cudaSuccess ? e : raise_smem_limit<1, true, false, false>(optin);
+        e = e != cudaSuccess ? e : raise_smem_limit<1, true, false, true>(optin);
+        e = e != cudaSuccess ? e : raise_smem_limit<2, true, false, false>(optin);
+        e = e != cudaSuccess ? e : raise_smem_limit<4, true, false, false>(optin);
+        e = e != cudaSuccess ? e : raise_smem_limit<1, true, true, false>(optin);
+        e = e != cudaSuccess ? e : raise_smem_limit<1, true, true, true>(optin);
+        e = e != cudaSuccess ? e : raise_smem_limit<2, true, true, false>(optin);
+        e = e != cudaSuccess ? e : raise_smem_limit<4, true, true, false>(optin);
+        if (e != cudaSuccess || tensor_map_fn() != SV_OK) {
+            cudaGetLastError();
+            return SV_ERR_CUDA;
+        }
+        st.part = reinterpret_cast<float *>(base);
+        st.ctr = reinterpret_cast<unsigned *>(base + NOALLOC_CTR_OFF);
+        st.keys = reinterpret_cast<unsigned long long *>(base + NOALLOC_KEYS_OFF);
+        st.done = reinterpret_cast<unsigned *>(base + NOALLOC_DONE_OFF);
+        st.err = reinterpret_cast<int *>(base + NOALLOC_ERR_OFF);
+        st.sms = sms < NOALLOC_MAX_CTAS ? sms : NOALLOC_MAX_CTAS;
+        st.smem_optin = optin;
+        st.ready = true;
+    }
+    *out = &st;
+    return SV_OK;
+}
+
 }  // namespace
 }  // namespace sv
 
 extern "C" {
+
+int lmhead_verify_noalloc(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, int K,
+                          const int32_t *drafts, int n_draft, const int32_t *vocab_map, int n_map, int V,
+                          int32_t *accept_len, int32_t *next_token, sv_stream stream)
+{
+    using namespace sv;
+    if (n_draft < 0 || n_draft > TMAX - 1) return SV_ERR_SHAPE;
+    const int T = n_draft + 1;
+    int rc = check_common(x, Wq, scales, T, K);
+    if (rc != SV_OK) return rc;
+    if (V < 1) return SV_ERR_SHAPE;
+    if (vocab_map) {
+        if (n_map < 1 || n_map > V) return SV_ERR_SHAPE;
+        if (!aligned4(vocab_map)) return SV_ERR_ALIGN;
+    }
+    if (!accept_len || !next_token) return SV_ERR_NULL;
+    if (n_draft > 0 && !drafts) return SV_ERR_NULL;
+    if ((drafts && !aligned4(drafts)) || !aligned4(accept_len) || !aligned4(next_token))
+        return SV_ERR_ALIGN;
+    DeviceState *st = nullptr;
+    rc = noalloc_state(&st);
+    if (rc != SV_OK) return rc;
+    const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    // The array keeps whatever the last call left: the counters, keys and
+    // completion count must start at zero, so clear them (and the error word)
+    // on the stream first.
+    if (cudaMemsetAsync(st->ctr, 0, NOALLOC_BYTES - NOALLOC_CTR_OFF, cs) != cudaSuccess) {
+        cudaGetLastError();
+        return SV_ERR_CUDA;
+    }
+    Params p{};
+    p.x = x;
+    p.Wq = Wq;
+    p.scales = scales;
+    p.map = vocab_map;
+    p.T = T;
+    p.K = K;
+    p.G = K / 128;
+    p.n_rows = vocab_map ? n_map : V;
+    p.V = V;
+    const long long tiles = (static_cast<long long>(p.n_rows) + ROWS - 1) / ROWS;
+    p.U = tiles * p.G;
+    p.mode = 0;
+    p.drafts = drafts;
+    p.n_draft = n_draft;
+    p.n_streams = 1;
+    p.accept_len = accept_len;
+    p.next_token = next_token;
+    return vocab_map ? dispatch<true, true>(p, *st, cs) : dispatch<true, false>(p, *st, cs);
+}
+
 
 int w4a16_gemm(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, int T, int K, int N,
                sv_bf16 *y, sv_stream stream)

@@ -1,0 +1,89 @@
+"""lmhead_verify_noalloc: the verify for callers that cannot allocate GPU
+memory at call time -- code under CUDA-graph stream capture, serving runtimes
+that hand out every device byte from their own arena, latency-critical paths
+that cannot take cudaMalloc's implicit synchronisation.  Its scratch is a fixed
+array inside the library, so the call itself never allocates.
+
+The test drives it through the C ABI, twice in a row on the same inputs and
+once more on other drafts, and requires exactly the results of the regular
+lmhead_verify (same kernel, same launch shape) and of the CPU oracle where the
+deciding rows' top-1 margin exceeds 1e-3.  The file is named so that pytest
+collects it last; it needs no state left by other tests.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+import gen
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+MARGIN = 1e-3
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import speculative_verify_gb300 as sv
+    from speculative_verify_gb300 import build
+    build.build()
+    return sv.load()
+
+
+def _dev(a, dt):
+    return torch.from_numpy(np.ascontiguousarray(a).view(dt)).cuda()
+
+
+def _p(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+@pytest.mark.parametrize("V,K,n_draft,n_map", [(30011, 1024, 3, 0), (20000, 512, 7, 5000)])
+def test_noalloc_matches_regular_entry_point(lib, oracle, V, K, n_draft, n_map):
+    rng = np.random.default_rng(4242 + V + n_map)
+    Wq, sc = gen.weights(rng, V, K)
+    T = n_draft + 1
+    x = gen.activations(rng, T, K)
+    vm = gen.vocab_map(rng, V, n_map) if n_map else None
+    a, _, _ = oracle.argmax(oracle.lmhead_logits(x, Wq, sc, K, T, V, rows=vm), ids=vm)
+    dx, dW, ds = _dev(x, np.int16), _dev(Wq, np.int32), _dev(sc, np.int16)
+    dvm = None if vm is None else _dev(vm, np.int32)
+    n_map_arg = 0 if vm is None else vm.size
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+    draft_sets = [gen.drafts_with_mismatch(rng, a, 1, V, pool=vm),
+                  gen.drafts_with_mismatch(rng, a, n_draft, V, pool=vm)]
+    acc_r = torch.empty(1, dtype=torch.int32, device="cuda")
+    nxt_r = torch.empty(1, dtype=torch.int32, device="cuda")
+    acc_n = torch.empty(1, dtype=torch.int32, device="cuda")
+    nxt_n = torch.empty(1, dtype=torch.int32, device="cuda")
+    for call, d in enumerate([draft_sets[0], draft_sets[0], draft_sets[1]]):
+        dd = _dev(d.astype(np.int32), np.int32)
+        acc_r.fill_(-7)
+        acc_n.fill_(-7)
+        rc = lib.lmhead_verify(_p(dx), _p(dW), _p(ds), K, _p(dd), n_draft,
+                               None if dvm is None else _p(dvm), n_map_arg, V, _p(acc_r), _p(nxt_r),
+                               stream)
+        assert rc == 0
+        rc = lib.lmhead_verify_noalloc(_p(dx), _p(dW), _p(ds), K, _p(dd), n_draft,
+                                       None if dvm is None else _p(dvm), n_map_arg, V, _p(acc_n),
+                                       _p(nxt_n), stream)
+        assert rc == 0, "lmhead_verify_noalloc returned %d on call %d" % (rc, call)
+        torch.cuda.synchronize()
+        assert int(acc_n.item()) == int(acc_r.item()), call
+        assert int(nxt_n.item()) == int(nxt_r.item()), call
+        ref = oracle.lmhead_verify(x, Wq, sc, K, V, d, vocab_map=vm)
+        acc = int(ref.accept_len[0])
+        if all(ref.margin[t] > MARGIN for t in range(acc + 1)):
+            assert int(acc_n.item()) == acc
+            assert int(nxt_n.item()) == int(ref.next_token[0])
+
+
+def test_noalloc_rejects_too_many_drafts(lib):
+    buf = torch.zeros(64, dtype=torch.int32, device="cuda")
+    rc = lib.lmhead_verify_noalloc(_p(buf), _p(buf), _p(buf), 128, _p(buf), 32, None, 0, 16,
+                                   _p(buf), _p(buf), None)
+    assert rc == -2
