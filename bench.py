@@ -55,14 +55,18 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
+KERNEL_SOURCES = ("w4a16_stream.cuh", "sv_ptx.cuh")
+
+
 def kernel_source_digest():
+    """Digest of the device-code sources; ncu counters recorded for another
+    digest describe a different kernel and are not reported."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_verify_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode())
-                h.update(f.read())
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
