@@ -609,13 +609,7 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
                 wa[r] = lds128(wbase + r * RSTEP);
                 wb[r] = lds128(wbase + r * RSTEP + HSTEP);
             }
-            float gacc[C::R][NT][4];
-#pragma unroll
-            for (int r = 0; r < C::R; ++r)
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) gacc[r][nt][e] = 0.f;
+            float gacc[C::R][NT][4];     // first k-step writes, later ones accumulate
 
             const uint32_t xbase = XRES ? xr_lane + gs * 256 : stage + x_lane;
 #pragma unroll
@@ -648,8 +642,12 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
                     uint32_t a0 = dequant2(wA), a1 = dequant2(wB);
                     uint32_t a2 = dequant2(wA >> 4), a3 = dequant2(wB >> 4);
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
-                        mma_bf16_16816(gacc[r][nt], a0, a1, a2, a3, bx[nt][0], bx[nt][1]);
+                    for (int nt = 0; nt < NT; ++nt) {
+                        if (m == 0)
+                            mma_bf16_16816_zc(gacc[r][nt], a0, a1, a2, a3, bx[nt][0], bx[nt][1]);
+                        else
+                            mma_bf16_16816(gacc[r][nt], a0, a1, a2, a3, bx[nt][0], bx[nt][1]);
+                    }
                     // k-step 2m+1: nibble pairs (2,6) and (3,7)
                     a0 = dequant2(wA >> 8);
                     a1 = dequant2(wB >> 8);
