@@ -161,6 +161,15 @@ __device__ __forceinline__ unsigned atomic_add_acq_rel_gpu(unsigned *p, unsigned
     return old;
 }
 
+// Load with acquire semantics at GPU scope: later reads of this thread see
+// every write released before the value it returns.
+__device__ __forceinline__ unsigned ld_acquire_gpu_u32(const unsigned *p)
+{
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ float4 ldcg_f4(const float *p)
 {
     return __ldcg(reinterpret_cast<const float4 *>(p));
@@ -241,7 +250,76 @@ __device__ __forceinline__ uint32_t dequant2(uint32_t v)
     return r;
 }
 
+// fp16 levels.  fp16 1024.0 (0x6400) has spacing 1 and a 10-bit mantissa,
+// so a nibble fits either at bits 0..3 (value 1024 + n) or at bits 4..7
+// (value 1024 + 16 n) without touching the exponent; a word then needs one
+// shift (by 8) for its four nibble pairs instead of three.
+// Low position: v holds nibble a in bits 0..3 and b in bits 16..19;
+// (1024 + n) * 1 - 1032 = n - 8.
+__device__ __forceinline__ uint32_t dequant2_f16_lo(uint32_t v)
+{
+    uint32_t q, r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(q) : "r"(v), "r"(0x000F000Fu), "r"(0x64006400u));
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(q), "r"(0x3C003C00u), "r"(0xE408E408u));
+    return r;
+}
+
+// High position: nibble a in bits 4..7 and b in bits 20..23;
+// (1024 + 16 n) / 16 - 72 = n - 8.
+__device__ __forceinline__ uint32_t dequant2_f16_hi(uint32_t v)
+{
+    uint32_t q, r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(q) : "r"(v), "r"(0x00F000F0u), "r"(0x64006400u));
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(q), "r"(0x2C002C00u), "r"(0xD480D480u));
+    return r;
+}
+
 // ---------------------------------------------------------------- tensor core
+
+// D (16x8 fp32) += A (16x16 fp16, row) * B (16x8 fp16, col).
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1)
+{
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// D (16x8 fp32) = A (16x16 fp16, row) * B (16x8 fp16, col), no accumulator input.
+__device__ __forceinline__ void mma_f16_16816_zc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                                 uint32_t a3, uint32_t b0, uint32_t b1)
+{
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%10, %10, %10, %10};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
+}
+
+// Exponent s for the fp16 copy of an activation row whose largest magnitude
+// has bf16 bits mx (sign cleared): 2^s * max lies in [2^14, 2^15), below the
+// fp16 maximum 65504.  Clamped to [-120, 120] so that 2^s and 2^-s are normal
+// fp32 numbers; 0 for an all-zero row.
+__device__ __forceinline__ int xres_shift(unsigned mx)
+{
+    if (mx == 0u) return 0;
+    const int s = 141 - static_cast<int>(mx >> 7);
+    return s < -120 ? -120 : (s > 120 ? 120 : s);
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v)
+{
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// Two floats -> fp16x2 (round to nearest even); lo in the low half.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
 
 // D (16x8 fp32) += A (16x16 bf16, row) * B (16x8 bf16, col).
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,

@@ -86,6 +86,7 @@ struct Params {
     int nst, stage_bytes, xslot_bytes, sbuf_bytes;
     int off_sbuf, off_ids, off_red, off_bars;
     int off_xres, xres_stride;  // resident activations (XRES kernels only)
+    int off_xsc;                // XRES: per-token largest |x| (bf16 bits), [8] u32
     // GEMM output
     uint16_t *y;                // [T][N]
     // HEAD outputs
@@ -228,6 +229,8 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
         mbar_init(smem_addr(red_full), NCW);
         mbar_init(smem_addr(red_empty), 1);
         *flag = 0;
+        if (XRES)
+            for (int t = 0; t < 8; ++t) reinterpret_cast<unsigned *>(smem + p.off_xsc)[t] = 0u;
         fence_barrier_init();
     }
     // Token rows T..TP-1 of every stage's activation slots stay zero for the
@@ -352,48 +355,58 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
             // This CTA's sums of the group slots (fixed slot order) for rows
             // lane and lane+32 of every token, kept as v[t][h] in registers
             // for the tokens being processed (chunks of 4).
-            // Split tiles: the partial goes to the scratch area as
-            // [row][TMAX] floats; the CTA that arrives last adds all the
-            // tile's partials in CTA order (fixed, so results are
-            // deterministic) with vectorised loads issued together.
-            int bf = 0, nc = 1;
+            // Split tiles: the tile's contributors are CTAs bf..bf+nc-1.  A
+            // CTA that finds (acquire load of the tile's counter) that all
+            // the others have already published their partials finishes the
+            // tile at once.  Otherwise it publishes its own partial in the
+            // scratch area as [row][TMAX] floats and counts itself in; the
+            // CTA whose count completes the tile finishes it.  The finisher
+            // adds the contributions in CTA order -- its own from shared
+            // memory, the others' with vectorised loads issued together --
+            // so results do not depend on who finishes.
+            int bf = 0, nc = 1, me = 0;
             bool finish = true;
             const float *others[4] = {nullptr, nullptr, nullptr, nullptr};
             if (!complete) {
                 bf = cta_of(ts, U, B);
                 const int bl = cta_of(te - 1, U, B);
                 nc = bl - bf + 1;
-                float *mine = p.part + (static_cast<size_t>(b) * 2 + (tile == tile_first ? 0 : 1)) * PART_FLOATS;
-                for (int t0 = 0; t0 < T; t0 += 4) {
+                me = b - bf;
+                const unsigned seen = ld_acquire_gpu_u32(&p.ctr[bf]);
+                finish = __all_sync(0xFFFFFFFFu, seen == static_cast<unsigned>(nc - 1));
+                if (!finish) {
+                    float *mine = p.part + (static_cast<size_t>(b) * 2 + (tile == tile_first ? 0 : 1)) * PART_FLOATS;
+                    for (int t0 = 0; t0 < T; t0 += 4) {
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int row = lane + 32 * h;
-                        float q[4];
+                        for (int h = 0; h < 2; ++h) {
+                            const int row = lane + 32 * h;
+                            float q[4];
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const int t = t0 + j;
-                            float sum = 0.f;
-                            if (t < T) {
-                                sum = red[t * ROWS + row];
+                            for (int j = 0; j < 4; ++j) {
+                                const int t = t0 + j;
+                                float sum = 0.f;
+                                if (t < T) {
+                                    sum = red[t * ROWS + row];
 #pragma unroll
-                                for (int sl = 1; sl < C::GPS; ++sl) sum += red[(sl * C::TP + t) * ROWS + row];
+                                    for (int sl = 1; sl < C::GPS; ++sl) sum += red[(sl * C::TP + t) * ROWS + row];
+                                }
+                                q[j] = sum;
                             }
-                            q[j] = sum;
+                            *reinterpret_cast<float4 *>(mine + row * TMAX + t0) = make_float4(q[0], q[1], q[2], q[3]);
                         }
-                        *reinterpret_cast<float4 *>(mine + row * TMAX + t0) = make_float4(q[0], q[1], q[2], q[3]);
                     }
-                }
-                __threadfence();
-                __syncwarp();
-                unsigned last = 0;
-                if (lane == 0) {
-                    const unsigned old = atomic_add_acq_rel_gpu(&p.ctr[bf], 1u);
-                    last = (old == static_cast<unsigned>(nc - 1));
-                    if (last) p.ctr[bf] = 0u;          // ready for the next launch
-                }
-                finish = __shfl_sync(0xFFFFFFFFu, last, 0) != 0;
-                if (finish) {
                     __threadfence();
+                    __syncwarp();
+                    unsigned last = 0;
+                    if (lane == 0) {
+                        const unsigned old = atomic_add_acq_rel_gpu(&p.ctr[bf], 1u);
+                        last = (old == static_cast<unsigned>(nc - 1));
+                    }
+                    finish = __shfl_sync(0xFFFFFFFFu, last, 0) != 0;
+                    if (finish) __threadfence();
+                }
+                if (finish) {
+                    if (lane == 0) p.ctr[bf] = 0u;        // ready for the next launch
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         const int bb = bf + j;
@@ -409,38 +422,46 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const int row = lane + 32 * h;
+                    float own[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int t = t0 + j;
+                        float sum = 0.f;
+                        if (t < T) {
+                            sum = red[t * ROWS + row];
+#pragma unroll
+                            for (int sl = 1; sl < C::GPS; ++sl) sum += red[(sl * C::TP + t) * ROWS + row];
+                        }
+                        own[j] = sum;
+                    }
                     if (complete) {
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const int t = t0 + j;
-                            float sum = 0.f;
-                            if (t < T) {
-                                sum = red[t * ROWS + row];
-#pragma unroll
-                                for (int sl = 1; sl < C::GPS; ++sl) sum += red[(sl * C::TP + t) * ROWS + row];
-                            }
-                            v[j][h] = sum;
-                        }
+                        for (int j = 0; j < 4; ++j) v[j][h] = own[j];
                     } else {
-                        // all contributors' float4s first, then the ordered sum
-                        float4 pv[4];
+                        // contributions in CTA order (the loads are independent of
+                        // the sum, so they are all in flight together)
+                        const float4 mine4 = make_float4(own[0], own[1], own[2], own[3]);
+                        float4 acc4 = mine4;
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
-                            if (j < nc) pv[j] = ldcg_f4(others[j] + row * TMAX + t0);
-                        float4 acc4 = pv[0];
-#pragma unroll
-                        for (int j = 1; j < 4; ++j)
                             if (j < nc) {
-                                acc4.x += pv[j].x;
-                                acc4.y += pv[j].y;
-                                acc4.z += pv[j].z;
-                                acc4.w += pv[j].w;
+                                const float4 e = j == me ? mine4 : ldcg_f4(others[j] + row * TMAX + t0);
+                                if (j == 0) {
+                                    acc4 = e;
+                                } else {
+                                    acc4.x += e.x;
+                                    acc4.y += e.y;
+                                    acc4.z += e.z;
+                                    acc4.w += e.w;
+                                }
                             }
                         for (int j = 4; j < nc; ++j) {      // more than 4 CTAs on one tile (small K)
-                            const int bb = bf + j;
-                            const int wb2 = (cta_start(bb, U, B) >= ts) ? 0 : 1;
-                            const float4 e = ldcg_f4(p.part + (static_cast<size_t>(bb) * 2 + wb2) * PART_FLOATS +
-                                                     row * TMAX + t0);
+                            float4 e = mine4;
+                            if (j != me) {
+                                const int bb = bf + j;
+                                const int wb2 = (cta_start(bb, U, B) >= ts) ? 0 : 1;
+                                e = ldcg_f4(p.part + (static_cast<size_t>(bb) * 2 + wb2) * PART_FLOATS + row * TMAX + t0);
+                            }
                             acc4.x += e.x;
                             acc4.y += e.y;
                             acc4.z += e.z;
@@ -555,26 +576,100 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
     // and rows padded to 16 (mod 128) bytes, so that the B loads below are
     // conflict-free and need no byte permutes.  Row T is zeros, read by the
     // lanes of absent tokens.
+    //
+    // The resident rows are fp16, not bf16: row t holds x[t] * 2^s_t, with
+    // s_t chosen so that the row's largest magnitude lands in [2^14, 2^15).
+    // A bf16 value has 8 significant bits and fp16 11, so every element of
+    // magnitude >= 2^-32 of the row maximum converts exactly (smaller ones
+    // round to fp16 subnormals, an error below 2^-40 of the row maximum);
+    // fp16 weights then dequantise with one shift per word instead of three
+    // (dequant2_f16_lo/hi).  Products are exact in the fp32 accumulators and
+    // a power-of-two scale commutes with fp32 rounding, so multiplying each
+    // token's sums by 2^-s_t at the end of a tile gives exactly the sums of
+    // the unscaled bf16 products.
     uint32_t xr_lane = 0, xr_off[4] = {0, 0, 0, 0};
+    float xinv[2] = {1.f, 1.f};        // 2^-s of tokens 2c and 2c+1
     if constexpr (XRES) {
         pdl_wait_prior();                  // activations may come from the previous kernel
+        // Token-major: the warps of token tt (wpt of them) load its row,
+        // XB 16-byte chunks per thread in flight at once, and reduce the
+        // row's largest |x| (bf16 bits) into xmax[tt]; after a barrier every
+        // thread converts the chunks it holds to fp16 and stores them in
+        // B-fragment order.  Rows longer than XB chunks per thread take two
+        // passes over global memory (maximum, then conversion).
         uint8_t *xr = smem + p.off_xres;
-        const int chunks_per_row = p.K / 8;
-        const int nchunks = (T + 1) * chunks_per_row;
-        for (int i = cw * 32 + lane; i < nchunks; i += NCW * 32) {
-            const int t = i / chunks_per_row, w = i - t * chunks_per_row;
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (t < T) {
-                const uint4 r = *reinterpret_cast<const uint4 *>(p.x + static_cast<size_t>(t) * p.K + 8 * w);
-                v.x = __byte_perm(r.x, r.z, 0x5410);
-                v.y = __byte_perm(r.x, r.z, 0x7632);
-                v.z = __byte_perm(r.y, r.w, 0x5410);
-                v.w = __byte_perm(r.y, r.w, 0x7632);
+        unsigned *xmax = reinterpret_cast<unsigned *>(smem + p.off_xsc);
+        const int cpr = p.K / 8;                       // chunks per row
+        const int wpt = NCW / T;                       // warps per token (T <= 8)
+        const int tt = cw / wpt;                       // this warp's token
+        const int nthr = wpt * 32;
+        const int j0 = (cw - tt * wpt) * 32 + lane;
+        const bool loader = tt < T;
+        const uint4 *xrow = reinterpret_cast<const uint4 *>(p.x) + static_cast<size_t>(loader ? tt : 0) * cpr;
+        uint8_t *xdst = xr + static_cast<size_t>(tt) * p.xres_stride;
+        constexpr int XB = 10;
+        const bool one_batch = cpr <= XB * nthr;
+        uint4 r[XB];
+        unsigned mx = 0u;
+        for (int jb = j0; jb < cpr; jb += XB * nthr) {
+#pragma unroll
+            for (int u = 0; u < XB; ++u) {
+                const int j = jb + u * nthr;
+                r[u] = (loader && j < cpr) ? xrow[j] : make_uint4(0u, 0u, 0u, 0u);
             }
-            const int sw = w ^ ((w >> 2) & 2);
-            *reinterpret_cast<uint4 *>(xr + static_cast<size_t>(t) * p.xres_stride + sw * 16) = v;
+#pragma unroll
+            for (int u = 0; u < XB; ++u) {
+                const unsigned hi = max(max(r[u].x & 0x7FFF0000u, r[u].y & 0x7FFF0000u),
+                                        max(r[u].z & 0x7FFF0000u, r[u].w & 0x7FFF0000u)) >> 16;
+                const unsigned lo = max(max(r[u].x & 0x7FFFu, r[u].y & 0x7FFFu),
+                                        max(r[u].z & 0x7FFFu, r[u].w & 0x7FFFu));
+                mx = max(mx, max(hi, lo));
+            }
+            if (one_batch) break;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+        if (loader && lane == 0 && mx != 0u) atomicMax(&xmax[tt], mx);
+        // row T: zeros, read by the lanes of absent tokens
+        for (int i = cw * 32 + lane; i < cpr; i += NCW * 32)
+            sts128(smem_addr(xr + static_cast<size_t>(T) * p.xres_stride + i * 16), make_uint4(0u, 0u, 0u, 0u));
+        named_bar_sync(1, NCW * 32);
+        if (loader) {
+            const float sc = __uint_as_float(static_cast<uint32_t>(127 + xres_shift(xmax[tt])) << 23);
+            for (int jb = j0; jb < cpr; jb += XB * nthr) {
+                if (!one_batch) {
+#pragma unroll
+                    for (int u = 0; u < XB; ++u) {
+                        const int j = jb + u * nthr;
+                        r[u] = j < cpr ? xrow[j] : make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < XB; ++u) {
+                    const int j = jb + u * nthr;
+                    if (j < cpr) {
+                        // (x0,x4) (x1,x5) (x2,x6) (x3,x7) as fp16 pairs
+                        const uint32_t lo0 = r[u].x << 16, hi0 = r[u].x & 0xFFFF0000u;
+                        const uint32_t lo1 = r[u].y << 16, hi1 = r[u].y & 0xFFFF0000u;
+                        const uint32_t lo2 = r[u].z << 16, hi2 = r[u].z & 0xFFFF0000u;
+                        const uint32_t lo3 = r[u].w << 16, hi3 = r[u].w & 0xFFFF0000u;
+                        uint4 v;
+                        v.x = pack_f16x2(__uint_as_float(lo0) * sc, __uint_as_float(lo2) * sc);
+                        v.y = pack_f16x2(__uint_as_float(hi0) * sc, __uint_as_float(hi2) * sc);
+                        v.z = pack_f16x2(__uint_as_float(lo1) * sc, __uint_as_float(lo3) * sc);
+                        v.w = pack_f16x2(__uint_as_float(hi1) * sc, __uint_as_float(hi3) * sc);
+                        const int sw = j ^ ((j >> 2) & 2);
+                        sts128(smem_addr(xdst + sw * 16), v);
+                    }
+                }
+            }
         }
         named_bar_sync(1, NCW * 32);
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int tok = 2 * c + e;
+            if (tok < T) xinv[e] = __uint_as_float(static_cast<uint32_t>(127 - xres_shift(xmax[tok])) << 23);
+        }
         xr_lane = smem_addr(xr) + static_cast<uint32_t>((g < T ? g : T) * p.xres_stride);
 #pragma unroll
         for (int m = 0; m < 4; ++m) xr_off[m] = static_cast<uint32_t>((4 * c + (m ^ (c & 2))) * 16);
@@ -638,6 +733,23 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
                 for (int r = 0; r < C::R; ++r) {
                     const uint32_t wA = (m == 0) ? wa[r].x : (m == 1) ? wa[r].y : (m == 2) ? wa[r].z : wa[r].w;
                     const uint32_t wB = (m == 0) ? wb[r].x : (m == 1) ? wb[r].y : (m == 2) ? wb[r].z : wb[r].w;
+                    if constexpr (XRES) {
+                        // fp16: k-step 2m takes nibble pairs (0,4) and (1,5),
+                        // k-step 2m+1 pairs (2,6) and (3,7) of the word >> 8
+                        uint32_t a0 = dequant2_f16_lo(wA), a1 = dequant2_f16_lo(wB);
+                        uint32_t a2 = dequant2_f16_hi(wA), a3 = dequant2_f16_hi(wB);
+                        if (m == 0)
+                            mma_f16_16816_zc(gacc[r][0], a0, a1, a2, a3, bx[0][0], bx[0][1]);
+                        else
+                            mma_f16_16816(gacc[r][0], a0, a1, a2, a3, bx[0][0], bx[0][1]);
+                        const uint32_t wA8 = wA >> 8, wB8 = wB >> 8;
+                        a0 = dequant2_f16_lo(wA8);
+                        a1 = dequant2_f16_lo(wB8);
+                        a2 = dequant2_f16_hi(wA8);
+                        a3 = dequant2_f16_hi(wB8);
+                        mma_f16_16816(gacc[r][0], a0, a1, a2, a3, bx[0][2], bx[0][3]);
+                        continue;
+                    }
                     // k-step 2m: nibble pairs (0,4) and (1,5)
                     uint32_t a0 = dequant2(wA), a1 = dequant2(wB);
                     uint32_t a2 = dequant2(wA >> 4), a3 = dequant2(wB >> 4);
@@ -691,7 +803,7 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
                     for (int e = 0; e < 4; ++e) {
                         const int row = (mset * C::R + r) * 16 + g + 8 * (e >> 1);
                         const int tok = nt * 8 + 2 * c + (e & 1);
-                        red[(slot * C::TP + tok) * ROWS + row] = acc[r][nt][e];
+                        red[(slot * C::TP + tok) * ROWS + row] = XRES ? acc[r][nt][e] * xinv[e & 1] : acc[r][nt][e];
                         acc[r][nt][e] = 0.f;
                     }
             __syncwarp();

@@ -122,6 +122,58 @@ def test_gemm_matches_oracle(sv, oracle, T, K, N):
     assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
 
 
+def wide_range_activations(rng, K):
+    """Four bf16 rows far from N(0,1): scaled by 2^100, by 2^-100, with
+    per-element magnitudes spread over 2^-40 .. 2^40, and N(0,1) with a few
+    outliers of 2^20.  The kernels keep activations as fp16 scaled by a
+    power of two per row; these rows check that the scaling reaches both ends
+    of the bf16 range and that a row spanning far more than fp16's range
+    stays within tolerance."""
+    z = rng.standard_normal((4, K))
+    z[0] *= 2.0 ** 100
+    z[1] *= 2.0 ** -100
+    z[2] *= 2.0 ** rng.uniform(-40, 40, K)
+    z[3, rng.choice(K, 5, replace=False)] = 2.0 ** 20 * rng.choice([-1.0, 1.0], 5)
+    return gen.f32_to_bf16_bits(z.astype(np.float32))
+
+
+@pytest.mark.parametrize("K,N", [(1152, 300), (5120, 64)])
+def test_gemm_activation_dynamic_range(sv, oracle, K, N):
+    rng = np.random.default_rng(4100 + K)
+    Wq, sc = gen.weights(rng, N, K)
+    x = wide_range_activations(rng, K)
+    y32, _ = oracle.w4a16_gemm(x, Wq, sc, 4, K, N)
+    assert np.all(np.isfinite(y32))
+    y = sv.w4a16_gemm(dev_bits16(x), dev_words(Wq), dev_bits16(sc))
+    torch.cuda.synchronize()
+    assert_gemm_close(y.view(torch.int16).cpu().numpy().view(np.uint16), y32)
+
+
+def test_head_argmax_activation_dynamic_range(sv, oracle):
+    """Rows scaled by 2^30, unscaled, by 2^-30 and the spread row: argmax
+    ids bit-exact where the margin allows, chosen logits within reordering."""
+    rng = np.random.default_rng(4242)
+    V, K = 3000, 768
+    Wq, sc = gen.weights(rng, V, K)
+    z = rng.standard_normal((4, K))
+    z[0] *= 2.0 ** 30
+    z[2] *= 2.0 ** -30
+    z[3] *= 2.0 ** rng.uniform(-40, 40, K)
+    x = gen.f32_to_bf16_bits(z.astype(np.float32))
+    lg = oracle.lmhead_logits(x, Wq, sc, K, 4, V)
+    a, best, second = oracle.argmax(lg)
+    ids, vals = sv.lmhead_argmax(dev_bits16(x), dev_words(Wq), dev_bits16(sc))
+    torch.cuda.synchronize()
+    ids, vals = ids.cpu().numpy(), vals.cpu().numpy()
+    for t in range(4):
+        rowmax = np.abs(lg[t]).max()
+        if best[t] - second[t] > 1e-3 and best[t] - second[t] > 1e-5 * rowmax:
+            assert ids[t] == a[t], t
+        assert 0 <= ids[t] < V
+        assert abs(float(vals[t]) - float(lg[t, ids[t]])) <= 1e-4 * rowmax
+        assert float(lg[t, ids[t]]) >= best[t] - 1e-4 * rowmax
+
+
 @pytest.mark.slow
 @pytest.mark.parametrize("T", [1, 4, 8, 32])
 @pytest.mark.parametrize("label,K,N", gen.GEMM_SHAPES)
