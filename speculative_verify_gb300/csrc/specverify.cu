@@ -152,7 +152,7 @@ int plan_layout(Params &p, int smem_optin, int *smem_total)
     const int xres_bytes = XRES ? up((p.T + 1) * p.xres_stride, 128) : 0;
     const int ids_bytes = up(2 * ROWS * 4, 128);
     const int red_bytes = up(C::RED_FLOATS * 4, 128);
-    const int fixed = xres_bytes + 2 * p.sbuf_bytes + ids_bytes + red_bytes + 128 + 7 * 8 + 8;
+    const int fixed = xres_bytes + 2 * p.sbuf_bytes + ids_bytes + red_bytes + 128 + ROWS * 8 * 4 + 7 * 8 + 8;
     int nst = (smem_optin - fixed - 1024) / (p.stage_bytes + 16);
     if (nst > 8) nst = 8;
     if (nst < 2) return SV_ERR_SHAPE;
@@ -168,6 +168,8 @@ int plan_layout(Params &p, int smem_optin, int *smem_total)
     off += red_bytes;
     p.off_xsc = off;
     off += 128;
+    p.off_pre = off;
+    off += ROWS * 8 * 4;
     p.off_bars = off;
     off += (2 * nst + 6) * 8 + 8;
     *smem_total = off;

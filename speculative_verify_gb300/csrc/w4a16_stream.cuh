@@ -87,6 +87,7 @@ struct Params {
     int off_sbuf, off_ids, off_red, off_bars;
     int off_xres, xres_stride;  // resident activations (XRES kernels only)
     int off_xsc;                // XRES: per-token largest |x| (bf16 bits), [8] u32
+    int off_pre;                // prefetched partial of a split last tile, [ROWS][8] floats
     // GEMM output
     uint16_t *y;                // [T][N]
     // HEAD outputs
@@ -346,9 +347,60 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
             stage_tile_meta<HEAD, GATHER>(p, tile_first + 1, sbuf + p.sbuf_bytes, idbuf + ROWS,
                                           smem_addr(&meta_full[1]), lane);
         unsigned long long best = 0ull;    // lane t: best key of token t so far
+        // Contributors of the only tiles that can be split, the first and
+        // the last: CTAs bf .. bf+nc-1, and whether the tile is bf's first
+        // tile (its partial then sits in slot 0).  Worked out once here
+        // (64-bit divisions) instead of at the end of the run.
+        int bfA = b, ncA = 1, bfZ = b, ncZ = 1;
+        bool bf_firstA = true;
+        {
+            const long long ts = static_cast<long long>(tile_first) * G, te = ts + G;
+            if (u0 > ts || u1 < te) {
+                bfA = cta_of(ts, U, B);
+                ncA = cta_of(te - 1, U, B) - bfA + 1;
+                bf_firstA = cta_start(bfA, U, B) == ts;
+            }
+            const long long tz = static_cast<long long>(tile_last) * G;
+            if (tile_last != tile_first && u1 < tz + G) ncZ = cta_of(tz + G - 1, U, B) - b + 1;
+        }
         pdl_wait_prior();                  // scratch area, outputs and drafts from here on
         for (int k = 0, tile = tile_first; tile <= tile_last; ++k, ++tile) {
             const int kb = k & 1;
+            // The CTA's last tile, when it is shared with exactly one later
+            // CTA: that CTA works on it first and has normally published its
+            // partial long before.  Confirm that (acquire load of the tile's
+            // counter) and copy the partial to shared memory while the
+            // consumers are still on this tile, so that the end of the kernel
+            // only adds and stores.  Polling stops when this CTA's own sums
+            // arrive; the regular path below then takes over.
+            const bool first = tile == tile_first;
+            const int tbf = first ? bfA : bfZ, tnc = first ? ncA : ncZ;
+            bool pre_ok = false;
+            if (NT == 1 && tile == tile_last) {
+                if (tbf == b && tnc == 2) {
+                    const uint64_t t0 = global_timer_ns();
+                    while (true) {
+                        const unsigned seen = ld_acquire_gpu_u32(&p.ctr[b]);
+                        if (__all_sync(0xFFFFFFFFu, seen == 1u)) {
+                            pre_ok = true;
+                            break;
+                        }
+                        if (mbar_try_wait(smem_addr(red_full), static_cast<uint32_t>(k & 1))) break;
+                        if (global_timer_ns() - t0 > WAIT_LIMIT_NS) break;
+                    }
+                    if (pre_ok) {
+                        const float *src = p.part + static_cast<size_t>(b + 1) * 2 * PART_FLOATS;
+                        float *dst = reinterpret_cast<float *>(smem + p.off_pre);
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+#pragma unroll
+                            for (int q = 0; q < 2; ++q)
+                                if (4 * q < T)
+                                    *reinterpret_cast<float4 *>(dst + (lane + 32 * h) * 8 + 4 * q) =
+                                        ldcg_f4(src + (lane + 32 * h) * TMAX + 4 * q);
+                    }
+                }
+            }
             wait_or_flag(p, flag, smem_addr(red_full), static_cast<uint32_t>(k & 1));
             const long long ts = static_cast<long long>(tile) * G, te = ts + G;
             const bool complete = (u0 <= ts) && (u1 >= te);
@@ -368,12 +420,15 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
             bool finish = true;
             const float *others[4] = {nullptr, nullptr, nullptr, nullptr};
             if (!complete) {
-                bf = cta_of(ts, U, B);
-                const int bl = cta_of(te - 1, U, B);
-                nc = bl - bf + 1;
+                bf = tbf;
+                nc = tnc;
                 me = b - bf;
-                const unsigned seen = ld_acquire_gpu_u32(&p.ctr[bf]);
-                finish = __all_sync(0xFFFFFFFFu, seen == static_cast<unsigned>(nc - 1));
+                if (pre_ok) {
+                    finish = true;          // the other contributor is counted in
+                } else {
+                    const unsigned seen = ld_acquire_gpu_u32(&p.ctr[bf]);
+                    finish = __all_sync(0xFFFFFFFFu, seen == static_cast<unsigned>(nc - 1));
+                }
                 if (!finish) {
                     float *mine = p.part + (static_cast<size_t>(b) * 2 + (tile == tile_first ? 0 : 1)) * PART_FLOATS;
                     for (int t0 = 0; t0 < T; t0 += 4) {
@@ -409,9 +464,11 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
                     if (lane == 0) p.ctr[bf] = 0u;        // ready for the next launch
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        const int bb = bf + j;
-                        const int wb2 = (j < nc && cta_start(bb, U, B) >= ts) ? 0 : 1;
-                        others[j] = p.part + (static_cast<size_t>(bb) * 2 + wb2) * PART_FLOATS;
+                        // partial slot 0 holds a CTA's first tile: every later
+                        // contributor starts inside this tile; bf does when its
+                        // range starts exactly at the tile
+                        const int wb2 = (j > 0 || (first ? bf_firstA : u0 == ts)) ? 0 : 1;
+                        others[j] = p.part + (static_cast<size_t>(bf + j) * 2 + wb2) * PART_FLOATS;
                     }
                 }
             }
@@ -445,7 +502,11 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
                             if (j < nc) {
-                                const float4 e = j == me ? mine4 : ldcg_f4(others[j] + row * TMAX + t0);
+                                const float4 e =
+                                    j == me ? mine4
+                                    : (NT == 1 && pre_ok) ? *reinterpret_cast<const float4 *>(
+                                                   reinterpret_cast<const float *>(smem + p.off_pre) + row * 8 + t0)
+                                             : ldcg_f4(others[j] + row * TMAX + t0);
                                 if (j == 0) {
                                     acc4 = e;
                                 } else {
