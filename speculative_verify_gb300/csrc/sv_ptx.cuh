@@ -133,6 +133,13 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src)
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 
+// As cp_async_16, with an L2 eviction-policy hint.
+__device__ __forceinline__ void cp_async_16_hint(uint32_t dst, const void *src, uint64_t policy)
+{
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "l"(policy)
+                 : "memory");
+}
+
 // Arrive on `bar` once every cp.async this thread issued so far has landed.
 // The arrival is one of the barrier's expected arrivals (.noinc).
 __device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar)

@@ -153,7 +153,7 @@ __device__ __forceinline__ void stage_tile_meta(const Params &p, int tile, uint8
     const int G = p.G;
     uint16_t *dst = reinterpret_cast<uint16_t *>(sb);
     const int id0 = row_id(p, tile, lane), id1 = row_id(p, tile, lane + 32);
-    if (HEAD) {
+    if (HEAD || GATHER) {
         ib[lane] = id0;
         ib[lane + 32] = id1;
     }
@@ -167,6 +167,21 @@ __device__ __forceinline__ void stage_tile_meta(const Params &p, int tile, uint8
         for (int i = lane; i < n16; i += 32) cp_async_16(smem_addr(dst + 8 * i), src + 8 * i);
         for (int i = 8 * n16 + lane; i < nel; i += 32) dst[i] = ldg_u16(src + i);
         for (int i = nel + lane; i < ROWS * G; i += 32) dst[i] = 0;
+    } else if ((G & 7) == 0) {
+        // gathered rows, 16-byte aligned (G*2 bytes a multiple of 16): the
+        // ROWS x G/8 chunks are spread over the lanes, so one warp keeps
+        // many independent small copies in flight
+        __syncwarp();
+        const int cpr = G / 8;
+        for (int i = lane; i < ROWS * cpr; i += 32) {
+            const int r = i / cpr, j = i - r * cpr;
+            const int id = ib[r];
+            uint16_t *d = dst + r * G + 8 * j;
+            if (id < 0)
+                *reinterpret_cast<uint4 *>(d) = make_uint4(0u, 0u, 0u, 0u);
+            else
+                cp_async_16(smem_addr(d), p.scales + static_cast<size_t>(id) * G + 8 * j);
+        }
     } else {
         for (int r = 0; r < ROWS; ++r) {
             const int id = __shfl_sync(0xFFFFFFFFu, r < 32 ? id0 : id1, r & 31);
@@ -220,7 +235,7 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < nst; ++s) {
-            mbar_init(smem_addr(&full[s]), 1);
+            mbar_init(smem_addr(&full[s]), GATHER ? 33 : 1);
             mbar_init(smem_addr(&empty[s]), NCW);
         }
         for (int i = 0; i < 2; ++i) {
@@ -268,6 +283,8 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
         }
         // gathered rows: ids of this lane's two rows, for this tile and the next
         int gid[2] = {-1, -1}, gid_next[2] = {-1, -1};
+        long long goff[8];              // word offsets of the rows this lane copies
+        int goff_tile = -1;
         if (GATHER) {
             gid[0] = row_id(p, tile, lane);
             gid[1] = row_id(p, tile, lane + 32);
@@ -281,24 +298,39 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
             if (issued >= nst) wait_or_flag(p, flag, smem_addr(&empty[s]), ph ^ 1u);
             const uint32_t fb = smem_addr(&full[s]);
             const uint32_t stage = smem_addr(smem) + static_cast<uint32_t>(s * p.stage_bytes);
-            uint32_t wbytes;
-            if (GATHER) {
-                const int cnt = __popc(__ballot_sync(0xFFFFFFFFu, gid[0] >= 0)) +
-                                __popc(__ballot_sync(0xFFFFFFFFu, gid[1] >= 0));
-                wbytes = static_cast<uint32_t>(cnt * n * 64);
-            } else {
-                wbytes = static_cast<uint32_t>(n * ROWS * 64);
-            }
+            // gathered rows arrive through cp.async (counted as arrivals),
+            // contiguous rows through the tensor copy (counted in bytes)
+            const uint32_t wbytes = GATHER ? 0u : static_cast<uint32_t>(n * ROWS * 64);
             const uint32_t xbytes = XRES ? 0u : static_cast<uint32_t>(n * T * XROW_BYTES);
             if (lane == 0) mbar_arrive_expect_tx(fb, wbytes + xbytes);
             __syncwarp();
             if (GATHER) {
+                // Rows at scattered addresses: 16-byte copies.  Lane 4k+q
+                // owns rows k, k+8, .., k+56 (word offsets in goff, set per
+                // tile) and copies chunk q of every group of them, so one
+                // instruction moves 64 contiguous bytes of each of 8 rows.
+                // One small tensor or bulk copy per row would be limited by
+                // the copy engine's cost per request.  Absent rows are
+                // skipped: their scale is 0.
+                if (goff_tile != tile) {
 #pragma unroll
-                for (int h = 0; h < 2; ++h)
-                    if (gid[h] >= 0)
-                        bulk_g2s(stage + (lane + 32 * h) * C::WSTR_G,
-                                 p.Wq + static_cast<size_t>(gid[h]) * (p.K / 8) + grp * 16,
-                                 static_cast<uint32_t>(n * 64), fb, pol_w);
+                    for (int i = 0; i < 8; ++i) {
+                        const int id = __shfl_sync(0xFFFFFFFFu, i < 4 ? gid[0] : gid[1], (lane >> 2) + 8 * (i & 3));
+                        goff[i] = id >= 0 ? static_cast<long long>(id) * (p.K / 8) : -1;
+                    }
+                    goff_tile = tile;
+                }
+                const uint32_t *wsrc = p.Wq + grp * 16 + (lane & 3) * 4;
+                const uint32_t wdst = stage + (lane >> 2) * C::WSTR_G + (lane & 3) * 16;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    if (goff[i] < 0) continue;
+#pragma unroll
+                    for (int j = 0; j < C::GPS; ++j)
+                        if (j < n)
+                            cp_async_16_hint(wdst + 8 * i * C::WSTR_G + j * 64, wsrc + goff[i] + j * 16, pol_w);
+                }
+                cp_async_mbar_arrive(fb);
             } else if (lane < n) {
                 tma_load_2d(stage + lane * (ROWS * 64), &tmW, (grp + lane) * 16, tile * ROWS, fb, pol_w);
             }
