@@ -192,8 +192,13 @@ int launch(Params p, const DeviceState &st, cudaStream_t stream)
         rc = encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, p.Wq,
                        static_cast<unsigned long long>(p.K / 8), static_cast<unsigned long long>(p.n_rows),
                        16, ROWS);
-        if (rc != SV_OK) return rc;
+    } else {
+        // gathered rows: boxes one row high, GPS groups wide (tile::gather4)
+        rc = encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, p.Wq,
+                       static_cast<unsigned long long>(p.K / 8), static_cast<unsigned long long>(p.V),
+                       static_cast<unsigned>(Cfg<NT, GATHER>::GPS * 16), 1);
     }
+    if (rc != SV_OK) return rc;
     if (!XRES) {
         // The activation box is exactly T rows high (boxes reaching past the
         // tensor are much slower to fill); the kernel zeroes the spare token

@@ -116,6 +116,19 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int 
                  : "memory");
 }
 
+// Four rows (r0..r3, any order, out-of-range rows read as zeros) of a 2-D
+// tensor map whose box is one row high, columns c0 .. c0 + box width - 1,
+// into shared memory as 4 consecutive box rows; completes on `bar`.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const void *tmap, int c0, int r0, int r1, int r2, int r3,
+                                            uint32_t bar, uint64_t policy)
+{
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+                 ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;"
+                 ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
+                   "r"(bar), "l"(policy)
+                 : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void *tmap)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");

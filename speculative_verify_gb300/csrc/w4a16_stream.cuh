@@ -67,9 +67,12 @@ struct Cfg {
     static constexpr int TP = 8 * NT;               // tokens, padded to n8 tiles
     // Weights in a stage.  Contiguous rows: one dense [64 rows][64 B] block
     // per group (a quarter warp reads 2 rows x 64 B = 128 consecutive bytes).
-    // Gathered rows: [64 rows][GPS*64 B + 64 B pad] (row stride = 64 mod 128).
-    static constexpr int WSTR_G = GPS * 64 + 64;
-    static constexpr int W_BYTES = GATHER ? ROWS * WSTR_G : GPS * ROWS * 64;
+    // Gathered rows: [64 rows][GPS*64 B], filled by 16 four-row boxes
+    // (tile::gather4; box b holds rows 4b..4b+3).  Box destinations stay
+    // 128-byte aligned, so the two rows a quarter warp reads share banks (a
+    // 2-way conflict on the weight loads, a few per 2 KB of weights).
+    static constexpr int GROW = GPS * 64;           // one gathered row of a stage
+    static constexpr int W_BYTES = GATHER ? ROWS * GROW : GPS * ROWS * 64;
     static constexpr int RED_FLOATS = GPS * TP * ROWS;
 };
 
@@ -235,7 +238,7 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < nst; ++s) {
-            mbar_init(smem_addr(&full[s]), GATHER ? 33 : 1);
+            mbar_init(smem_addr(&full[s]), 1);
             mbar_init(smem_addr(&empty[s]), NCW);
         }
         for (int i = 0; i < 2; ++i) {
@@ -271,7 +274,7 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
         const uint64_t pol_w = policy_evict_first();
         const uint64_t pol_x = policy_evict_last();
         if (lane == 0) {
-            if (!GATHER) prefetch_tmap(&tmW);
+            prefetch_tmap(&tmW);
             if (!XRES) prefetch_tmap(&tmX);
         }
         int s = 0, issued = 0, tile = tile_first, grp = grp_first, rem = n_units;
@@ -283,8 +286,8 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
         }
         // gathered rows: ids of this lane's two rows, for this tile and the next
         int gid[2] = {-1, -1}, gid_next[2] = {-1, -1};
-        long long goff[8];              // word offsets of the rows this lane copies
-        int goff_tile = -1;
+        int grows[4] = {0, 0, 0, 0};    // lanes 0..15: rows 4*lane .. 4*lane+3 (gather box `lane`)
+        int grows_tile = -1;
         if (GATHER) {
             gid[0] = row_id(p, tile, lane);
             gid[1] = row_id(p, tile, lane + 32);
@@ -298,39 +301,31 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
             if (issued >= nst) wait_or_flag(p, flag, smem_addr(&empty[s]), ph ^ 1u);
             const uint32_t fb = smem_addr(&full[s]);
             const uint32_t stage = smem_addr(smem) + static_cast<uint32_t>(s * p.stage_bytes);
-            // gathered rows arrive through cp.async (counted as arrivals),
-            // contiguous rows through the tensor copy (counted in bytes)
-            const uint32_t wbytes = GATHER ? 0u : static_cast<uint32_t>(n * ROWS * 64);
+            // gathered rows: 16 boxes of 4 full rows (GPS groups, zeros for
+            // absent rows and past the end of K)
+            const uint32_t wbytes = GATHER ? static_cast<uint32_t>(ROWS * C::GROW) : static_cast<uint32_t>(n * ROWS * 64);
             const uint32_t xbytes = XRES ? 0u : static_cast<uint32_t>(n * T * XROW_BYTES);
             if (lane == 0) mbar_arrive_expect_tx(fb, wbytes + xbytes);
             __syncwarp();
             if (GATHER) {
-                // Rows at scattered addresses: 16-byte copies.  Lane 4k+q
-                // owns rows k, k+8, .., k+56 (word offsets in goff, set per
-                // tile) and copies chunk q of every group of them, so one
-                // instruction moves 64 contiguous bytes of each of 8 rows.
-                // One small tensor or bulk copy per row would be limited by
-                // the copy engine's cost per request.  Absent rows are
-                // skipped: their scale is 0.
-                if (goff_tile != tile) {
+                // Rows at scattered addresses: lane b (< 16) loads rows
+                // 4b .. 4b+3 with one four-row gather.  Absent rows get an
+                // out-of-range row index and read zeros (their scale is 0
+                // as well).
+                if (grows_tile != tile) {
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int id = __shfl_sync(0xFFFFFFFFu, i < 4 ? gid[0] : gid[1], (lane >> 2) + 8 * (i & 3));
-                        goff[i] = id >= 0 ? static_cast<long long>(id) * (p.K / 8) : -1;
+                    for (int t = 0; t < 4; ++t) {
+                        const int src = (4 * lane + t) & 31;
+                        const int v0 = __shfl_sync(0xFFFFFFFFu, gid[0], src);
+                        const int v1 = __shfl_sync(0xFFFFFFFFu, gid[1], src);
+                        const int id = (lane & 8) ? v1 : v0;       // rows >= 32 for lanes 8..15
+                        grows[t] = id >= 0 ? id : p.V;
                     }
-                    goff_tile = tile;
+                    grows_tile = tile;
                 }
-                const uint32_t *wsrc = p.Wq + grp * 16 + (lane & 3) * 4;
-                const uint32_t wdst = stage + (lane >> 2) * C::WSTR_G + (lane & 3) * 16;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    if (goff[i] < 0) continue;
-#pragma unroll
-                    for (int j = 0; j < C::GPS; ++j)
-                        if (j < n)
-                            cp_async_16_hint(wdst + 8 * i * C::WSTR_G + j * 64, wsrc + goff[i] + j * 16, pol_w);
-                }
-                cp_async_mbar_arrive(fb);
+                if (lane < 16)
+                    tma_gather4(stage + lane * 4 * C::GROW, &tmW, grp * 16, grows[0], grows[1], grows[2], grows[3], fb,
+                                pol_w);
             } else if (lane < n) {
                 tma_load_2d(stage + lane * (ROWS * 64), &tmW, (grp + lane) * 16, tile * ROWS, fb, pol_w);
             }
@@ -653,10 +648,10 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
     const int g = lane >> 2, c = lane & 3;
 
     // Lane-constant shared-memory offsets (within a stage / a scale buffer).
-    constexpr int RSTEP = GATHER ? 16 * C::WSTR_G : 16 * 64;   // next m16 tile
-    constexpr int HSTEP = GATHER ? 8 * C::WSTR_G : 8 * 64;     // row g + 8
+    constexpr int RSTEP = GATHER ? 16 * C::GROW : 16 * 64;   // next m16 tile
+    constexpr int HSTEP = GATHER ? 8 * C::GROW : 8 * 64;     // row g + 8
     const int row0 = mset * C::R * 16 + g;                     // first row of this lane
-    const uint32_t w_lane = GATHER ? static_cast<uint32_t>(row0 * C::WSTR_G + slot * 64 + c * 16)
+    const uint32_t w_lane = GATHER ? static_cast<uint32_t>(row0 * C::GROW + slot * 64 + c * 16)
                                    : static_cast<uint32_t>(slot * (ROWS * 64) + row0 * 64 + c * 16);
     const uint32_t x_lane = static_cast<uint32_t>(C::W_BYTES + slot * p.xslot_bytes + g * XROW_BYTES + c * 64);
     const uint32_t s_lane = static_cast<uint32_t>(row0 * G * 2);
