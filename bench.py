@@ -261,15 +261,25 @@ def host_only_workload(seed=2):
 
 
 def cpu_baseline(host, budget_s=12.0):
+    """The oracle timed on the host cores on a bounded sample of the step:
+    calibrated on 1% of the rows, then a row fraction (and, once that reaches
+    every row, a number of whole passes) that fills about budget_s."""
     import oracle
     oracle.build()
-    # size the sample: calibrate on 1% of the rows, then fill the budget
     nb, dt = oracle_sample_step(oracle, host, 0.01)
-    frac = min(1.0, max(0.01, 0.01 * budget_s / max(dt, 1e-3) / 2))
-    nb, dt = oracle_sample_step(oracle, host, frac)
-    return {"value": nb / dt / 1e9, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+    frac = min(1.0, max(0.01, 0.01 * budget_s / max(dt, 1e-3)))
+    passes = 1
+    if frac >= 1.0:
+        passes = max(1, int(round(budget_s / max(dt * 100, 1e-3))))
+    tot_b, tot_t = 0, 0.0
+    for _ in range(passes):
+        b, t = oracle_sample_step(oracle, host, frac)
+        tot_b += b
+        tot_t += t
+    return {"value": tot_b / tot_t / 1e9, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
             "sample": "%.1f%% of the output rows of each of the 3 GEMMs and of the 248,320 "
-                      "lm_head rows (T=4), one pass, %.1f s" % (100 * frac, dt)}
+                      "lm_head rows (T=4), %d pass%s, %.1f s" % (100 * frac, passes, "" if passes == 1 else "es",
+                                                             tot_t)}
 
 
 # ----------------------------------------------------------------------------
