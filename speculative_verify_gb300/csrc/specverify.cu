@@ -140,7 +140,7 @@ bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0
 // nst pipeline stages | resident activations (XRES) | scales of 2 tiles |
 // token ids of 2 tiles | the consumers' partial sums of one tile | mbarriers
 // and a flag.
-template <int NT, bool GATHER, bool XRES>
+template <int NT, bool HEAD, bool GATHER, bool XRES>
 int plan_layout(Params &p, int smem_optin, int *smem_total)
 {
     using C = Cfg<NT, GATHER>;
@@ -152,7 +152,8 @@ int plan_layout(Params &p, int smem_optin, int *smem_total)
     const int xres_bytes = XRES ? up((p.T + 1) * p.xres_stride, 128) : 0;
     const int ids_bytes = up(2 * ROWS * 4, 128);
     const int red_bytes = up(C::RED_FLOATS * 4, 128);
-    const int fixed = xres_bytes + 2 * p.sbuf_bytes + ids_bytes + red_bytes + 128 + ROWS * 8 * 4 + 7 * 8 + 8;
+    const int bk_bytes = HEAD ? up(32 * BK_STRIDE * 8, 128) : 0;
+    const int fixed = xres_bytes + 2 * p.sbuf_bytes + ids_bytes + red_bytes + 128 + ROWS * 8 * 4 + bk_bytes + 7 * 8 + 8;
     int nst = (smem_optin - fixed - 1024) / (p.stage_bytes + 16);
     if (nst > 8) nst = 8;
     if (nst < 2) return SV_ERR_SHAPE;
@@ -170,6 +171,8 @@ int plan_layout(Params &p, int smem_optin, int *smem_total)
     off += 128;
     p.off_pre = off;
     off += ROWS * 8 * 4;
+    p.off_bk = off;
+    off += bk_bytes;
     p.off_bars = off;
     off += (2 * nst + 6) * 8 + 8;
     *smem_total = off;
@@ -183,7 +186,7 @@ template <int NT, bool HEAD, bool GATHER, bool XRES>
 int launch(Params p, const DeviceState &st, cudaStream_t stream)
 {
     int smem = 0;
-    int rc = plan_layout<NT, GATHER, XRES>(p, st.smem_optin, &smem);
+    int rc = plan_layout<NT, HEAD, GATHER, XRES>(p, st.smem_optin, &smem);
     if (rc != SV_OK) return rc;
     CUtensorMap tmW, tmX;
     std::memset(&tmW, 0, sizeof tmW);

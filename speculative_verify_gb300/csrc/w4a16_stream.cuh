@@ -56,6 +56,7 @@ constexpr int TMAX = 32;                        // largest T
 constexpr int PART_FLOATS = TMAX * ROWS;        // one split-tile partial
 constexpr int XBOX = 144;                       // activation box width (elements)
 constexpr int XROW_BYTES = XBOX * 2;            // = 32 (mod 128): conflict-free B loads
+constexpr int BK_STRIDE = TMAX + 1;             // u64 per lane in the best-key table (odd: no bank conflicts)
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;        // 2 s: only a broken run gets here
 constexpr uint64_t WAIT_LIMIT_AFTER_ERR_NS = 1000000ull;  // 1 ms once something failed
 
@@ -91,6 +92,7 @@ struct Params {
     int off_xres, xres_stride;  // resident activations (XRES kernels only)
     int off_xsc;                // XRES: per-token largest |x| (bf16 bits), [8] u32
     int off_pre;                // prefetched partial of a split last tile, [ROWS][8] floats
+    int off_bk;                 // HEAD: running best key per lane and token, [32][BK_STRIDE] u64
     // GEMM output
     uint16_t *y;                // [T][N]
     // HEAD outputs
@@ -373,7 +375,11 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
         if (tile_first + 1 <= tile_last)
             stage_tile_meta<HEAD, GATHER>(p, tile_first + 1, sbuf + p.sbuf_bytes, idbuf + ROWS,
                                           smem_addr(&meta_full[1]), lane);
-        unsigned long long best = 0ull;    // lane t: best key of token t so far
+        // HEAD: bk[lane][t] = best key of token t over the rows this lane has
+        // seen; reduced across lanes once, at the end.
+        unsigned long long *bk = reinterpret_cast<unsigned long long *>(smem + p.off_bk) + lane * BK_STRIDE;
+        if (HEAD)
+            for (int t = 0; t < T; ++t) bk[t] = 0ull;
         // Contributors of the only tiles that can be split, the first and
         // the last: CTAs bf .. bf+nc-1, and whether the tile is bf's first
         // tile (its partial then sits in slot 0).  Worked out once here
@@ -574,15 +580,10 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
                                     __bfloat16_as_ushort(__float2bfloat16_rn(v[j][h]));
                         }
                     } else {
-                        unsigned long long k0 = id0 >= 0 ? make_key(v[j][0], static_cast<uint32_t>(id0)) : 0ull;
-                        unsigned long long k1 = id1 >= 0 ? make_key(v[j][1], static_cast<uint32_t>(id1)) : 0ull;
-                        unsigned long long kk = k0 > k1 ? k0 : k1;
-#pragma unroll
-                        for (int o = 16; o > 0; o >>= 1) {
-                            const unsigned long long ko = shfl_xor_u64(kk, o);
-                            kk = ko > kk ? ko : kk;
-                        }
-                        if (lane == t && kk > best) best = kk;
+                        const unsigned long long k0 = id0 >= 0 ? make_key(v[j][0], static_cast<uint32_t>(id0)) : 0ull;
+                        const unsigned long long k1 = id1 >= 0 ? make_key(v[j][1], static_cast<uint32_t>(id1)) : 0ull;
+                        const unsigned long long kk = k0 > k1 ? k0 : k1;
+                        if (kk > bk[t]) bk[t] = kk;
                     }
                 }
             }
@@ -597,6 +598,15 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
         }
         if constexpr (HEAD) {
             // ================================================ grid argmax + verify
+            __syncwarp();
+            unsigned long long best = 0ull;    // lane t: best key of token t in this CTA
+            if (lane < T) {
+                const unsigned long long *col = reinterpret_cast<const unsigned long long *>(smem + p.off_bk) + lane;
+                for (int l = 0; l < 32; ++l) {
+                    const unsigned long long v = col[l * BK_STRIDE];
+                    best = v > best ? v : best;
+                }
+            }
             if (lane < T && best != 0ull) atomicMax(&p.keys[lane], best);
             __threadfence();
             __syncwarp();
