@@ -188,7 +188,8 @@ class Workload:
                          nxt=torch.zeros(1, dtype=torch.int32, device=device),
                          bytes=gen.lmhead_bytes(V, K, self.T, n_streams=1, n_draft=N_DRAFT))
         self.bytes_per_step = sum(g["bytes"] for g in self.gemms) + self.head["bytes"]
-        self.launches_per_step = len(self.gemms) + 1
+        self.launches_per_step = sum(kernels_per_call(self.T, g["K"]) for g in self.gemms) + \
+            kernels_per_call(self.T, K)
 
     def gemm_part(self, sv, stream):
         for g in self.gemms:
@@ -222,6 +223,13 @@ class Workload:
 
 # ----------------------------------------------------------------------------
 # CPU oracle timing (the cpu_baseline leg and the reference arm)
+
+
+def kernels_per_call(T, K):
+    """Kernel launches of one library call: the stream kernel, plus the
+    activation conversion kernel when the call has more than one token tile
+    (T > 8)."""
+    return 2 if T > 8 else 1
 
 
 def oracle_sample_step(oracle, host, rows_frac):

@@ -12,7 +12,8 @@
  *                             (bits 4i..4i+3) of word w; level = nibble - 8
  *      scales  [rows][K/128]  bf16 bits, one per row and 128-column group
  *      y       [T][N]         bf16 bits
- *    Format source: page "qwen-warp, llamAmpere ..." (ai.satyajit.si),
+ *    Format source: page "qwen-warp and llamAmpere: two RTX 3090 engines
+ *    for Qwen3.8, and what each one calls the same answer" (ai.satyajit.si),
  *    section "qwen-warp: keep the activations in bf16": eight nibbles per
  *    uint32 word along K, one bf16 scale per 128 columns, level = nibble - 8,
  *    the group scale applied in fp32 after each group's accumulate.
@@ -64,14 +65,18 @@ enum sv_status {
  *                          sum_{k in group g} (q(n,k) - 8) * float(x[t][k]) )
  * with fp32 products and sums; every packed weight byte and scale is read
  * from HBM once per call whatever T is ("read once per cycle regardless of
- * T": page "OpenJet engine", section "How it gets its speed").  Summation
+ * T": page "OpenJet Engine: CUDA LLM inference for Qwen3.8-27B", section "How it gets its speed").  Summation
  * order differs from a sequential loop (groups may be split across thread
  * blocks and added in a fixed order), so results agree with a sequential
  * fp32 sum to within fp32 rounding before the final bf16 rounding; they
  * are deterministic from run to run.
  *   x [T][K], Wq [N][K/8], scales [N][K/128], y [T][N] (written).
  *   Errors: SV_ERR_NULL, SV_ERR_SHAPE (T outside 1..32, K < 128 or
- *   K % 128 != 0, N < 1), SV_ERR_ALIGN, SV_ERR_CUDA, SV_ERR_NOMEM.
+ *   K % 128 != 0, N < 1; with T > 8 also K > 131072), SV_ERR_ALIGN,
+ *   SV_ERR_CUDA, SV_ERR_NOMEM.
+ *   Launches: one kernel for T <= 8; for T > 8 a small conversion kernel
+ *   (the activations into a per-device buffer) and then the main kernel,
+ *   both on `stream`.
  */
 int w4a16_gemm(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales,
                int T, int K, int N, sv_bf16 *y, sv_stream stream);
@@ -85,11 +90,12 @@ int w4a16_gemm(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales,
  *   accept_len = first i in [0, n_draft) with drafts[i] != a[i], else n_draft;
  *   next_token = a[accept_len]  (the model's own token at the first
  *   disagreement, or the bonus token when every draft was accepted).
- * Sources: page "qwen-warp, llamAmpere ..." section "What each one calls the
+ * Sources: page "qwen-warp and llamAmpere: two RTX 3090 engines for
+ * Qwen3.8, and what each one calls the same answer" section "What each one calls the
  * same answer" (greedy acceptance is an argmax equality over the verify
  * rows); page "swift-qwen3.8-rtx3090" section "Body, heads and drafter"
  * (drafts are kept up to the first one the model disagrees with); page
- * "OpenJet engine" section "How it works" (lm_head and verification run on
+ * "OpenJet Engine: CUDA LLM inference for Qwen3.8-27B" section "How it works" (lm_head and verification run on
  * the device and only the accepted tokens go back to the host).
  *   Candidates: all rows 0..V-1 when vocab_map == NULL (n_map ignored);
  *   otherwise rows vocab_map[0..n_map-1] of the V-row head, and every id
@@ -102,7 +108,7 @@ int w4a16_gemm(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales,
  *   accept_len, next_token: one int32 each (written).
  *   Errors: SV_ERR_NULL, SV_ERR_SHAPE (n_draft outside 0..31, K as above,
  *   V < 1, n_map outside 1..V with a map), SV_ERR_ALIGN, SV_ERR_CUDA,
- *   SV_ERR_NOMEM.
+ *   SV_ERR_NOMEM.  Launches as w4a16_gemm (T = 1 + n_draft).
  */
 int lmhead_verify(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, int K,
                   const int32_t *drafts, int n_draft,
@@ -111,7 +117,8 @@ int lmhead_verify(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, i
 
 /*
  * lmhead_verify_batched -- n_streams independent verify blocks in ONE pass
- * over the head (page "qwen-warp, llamAmpere ...", section "What makes each
+ * over the head (page "qwen-warp and llamAmpere: two RTX 3090 engines for
+ * Qwen3.8, and what each one calls the same answer", section "What makes each
  * one a 3090 engine": four sequences with three drafts each share one weight
  * read).  Block s owns rows s*(1+n_draft) .. s*(1+n_draft)+n_draft of x and
  * drafts[s][0..n_draft-1]; accept_len[s], next_token[s] as in lmhead_verify.
@@ -126,7 +133,7 @@ int lmhead_verify_batched(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *s
  * lmhead_argmax -- the same pass without the draft comparison: for each of
  * the T rows of x, ids[t] = the argmax token id (lowest id on ties) and
  * vals[t] = its fp32 logit.  This is the greedy step of a restricted draft
- * head (page "OpenJet engine", section "How it gets its speed": the draft
+ * head (page "OpenJet Engine: CUDA LLM inference for Qwen3.8-27B", section "How it gets its speed": the draft
  * head scores a fixed id list; page "swift-qwen3.8-rtx3090": the draft head
  * is the lm_head restricted to the draft vocabulary).
  *   ids [T] int32, vals [T] float (written).  vals may be NULL.
@@ -144,11 +151,12 @@ int lmhead_argmax(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, i
  * afford cudaMalloc's implicit device synchronisation.  No source page has
  * a counterpart to this entry point; it exists for this library's users.
  *   Arguments, layouts and results are those of lmhead_verify.
- *   Scratch: a fixed device array inside the library (about 2.6 MB per
+ *   Scratch: a fixed device array inside the library (about 3.8 MB per
  *   device, held until the process exits), sized for at most 160 thread
- *   blocks and 32 verify rows; the call launches at most 160 blocks and
- *   rejects more than 31 drafts with SV_ERR_SHAPE.  It calls no cudaMalloc,
- *   cudaFree or other allocating routine.
+ *   blocks, 32 verify rows and, with more than 7 drafts, K <= 16384; the
+ *   call launches at most 160 blocks and rejects more than 31 drafts, or
+ *   more than 7 drafts with K > 16384, with SV_ERR_SHAPE.  It calls no
+ *   cudaMalloc, cudaFree or other allocating routine.
  *   The first call on a device resolves the array's device address and
  *   sets kernel attributes (no allocation, but make that first call outside
  *   stream capture).  Each call clears the array's counters with an

@@ -11,13 +11,13 @@ arrays through ctypes and composes the three steps of the verify:
 logits -> argmax -> first-mismatch comparison.
 
 Sources, by page and section:
-  * "qwen-warp, llamAmpere ..." -- "qwen-warp: keep the activations in bf16"
+  * "qwen-warp and llamAmpere: two RTX 3090 engines for Qwen3.8, and what each one calls the same answer" -- "qwen-warp: keep the activations in bf16"
     (nibble format, level = nibble - 8, fp32 group scale after each
     128-column group) and "What each one calls the same answer" (greedy
     acceptance is argmax equality over the verify rows).
   * "swift-qwen3.8-rtx3090" -- "Body, heads and drafter" (keep drafts up to the
     first disagreement; a restricted draft head is a slice of lm_head rows).
-  * "OpenJet engine" -- "How it works" (verify over T = 1 + n_draft rows),
+  * "OpenJet Engine: CUDA LLM inference for Qwen3.8-27B" -- "How it works" (verify over T = 1 + n_draft rows),
     "How it gets its speed" (restricted draft vocabulary).
 """
 from __future__ import annotations

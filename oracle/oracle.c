@@ -8,7 +8,7 @@
  * library.
  *
  * What it follows (page titles and sections of the source pages):
- *  - "qwen-warp, llamAmpere ...", section "qwen-warp: keep the activations in
+ *  - "qwen-warp and llamAmpere: two RTX 3090 engines for Qwen3.8, and what each one calls the same answer", section "qwen-warp: keep the activations in
  *    bf16": weights are uint32 words of eight 4-bit nibbles along K with one
  *    bf16 scale per 128 columns of a row; a nibble n stands for the signed
  *    level n - 8; the group scale multiplies the fp32 sum of the group, after
@@ -19,7 +19,7 @@
  *    acceptance is an argmax equality over the verify rows.
  *  - "swift-qwen3.8-rtx3090", section "Body, heads and drafter": the model
  *    keeps drafted tokens up to the first one it disagrees with.
- *  - "OpenJet engine", sections "How it works" and "How it gets its speed":
+ *  - "OpenJet Engine: CUDA LLM inference for Qwen3.8-27B", sections "How it works" and "How it gets its speed":
  *    lm_head and verification run over T = 1 + n_draft rows; a restricted
  *    draft head scores a fixed id list.
  *

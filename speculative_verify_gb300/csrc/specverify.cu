@@ -27,7 +27,14 @@ struct DeviceState {
     unsigned long long *keys = nullptr;
     unsigned *done = nullptr;
     int *err = nullptr;
+    uint8_t *x16 = nullptr;     // streamed activations, X16_MAX_GROUPS x TMAX x XSTR bytes
+    float *xinv = nullptr;      // [TMAX]
+    int x16_max_groups = 0;
 };
+
+// Activations of calls with more than one token tile (T > 8) are converted
+// into a per-device buffer sized for K <= 128 * X16_MAX_GROUPS.
+constexpr int X16_MAX_GROUPS = 1024;
 
 DeviceState g_state[MAX_DEVICES];
 std::mutex g_mu;
@@ -87,7 +94,9 @@ int device_state(DeviceState **out)
         const size_t part_bytes = static_cast<size_t>(prop.multiProcessorCount) * 2 * PART_FLOATS * sizeof(float);
         const size_t ctr_bytes = static_cast<size_t>(prop.multiProcessorCount) * sizeof(unsigned);
         const size_t keys_bytes = TMAX * sizeof(unsigned long long);
-        const size_t total = part_bytes + ctr_bytes + keys_bytes + 2 * sizeof(unsigned) + 256;
+        const size_t x16_bytes = static_cast<size_t>(X16_MAX_GROUPS) * TMAX * XSTR;
+        const size_t total = part_bytes + ctr_bytes + keys_bytes + 2 * sizeof(unsigned) + 256 + x16_bytes +
+                             TMAX * sizeof(float) + 256;
         uint8_t *base = nullptr;
         if (cudaMalloc(&base, total) != cudaSuccess) {
             cudaGetLastError();
@@ -108,6 +117,12 @@ int device_state(DeviceState **out)
         st.done = reinterpret_cast<unsigned *>(base + off);
         off += sizeof(unsigned);
         st.err = reinterpret_cast<int *>(base + off);
+        off += sizeof(int);
+        off = (off + 255) & ~static_cast<size_t>(255);
+        st.x16 = base + off;
+        off += x16_bytes;
+        st.xinv = reinterpret_cast<float *>(base + off);
+        st.x16_max_groups = X16_MAX_GROUPS;
         cudaError_t e = cudaSuccess;
         e = e != cudaSuccess ? e : raise_smem_limit<1, false, false, false>(optin);
         e = e != cudaSuccess ? e : raise_smem_limit<1, false, false, true>(optin);
@@ -145,7 +160,8 @@ int plan_layout(Params &p, int smem_optin, int *smem_total)
 {
     using C = Cfg<NT, GATHER>;
     auto up = [](int v, int a) { return (v + a - 1) / a * a; };
-    p.xslot_bytes = up(C::TP * XROW_BYTES, 128);
+    p.xslot_bytes = NT > 1 ? C::TP * XSTR                 // one group block of xprep_kernel
+                           : up(C::TP * XROW_BYTES, 128);    // a bf16 activation box
     p.stage_bytes = XRES ? C::W_BYTES : up(C::W_BYTES + C::GPS * p.xslot_bytes, 128);
     p.sbuf_bytes = up(ROWS * p.G * 2, 128);
     p.xres_stride = 2 * p.K + 16;                     // = 16 (mod 128)
@@ -185,6 +201,8 @@ constexpr int XRES_MAX_BYTES = 100 * 1024;
 template <int NT, bool HEAD, bool GATHER, bool XRES>
 int launch(Params p, const DeviceState &st, cudaStream_t stream)
 {
+    // several token tiles: the activations go through the conversion buffer
+    if (!XRES && NT > 1 && p.G > st.x16_max_groups) return SV_ERR_SHAPE;
     int smem = 0;
     int rc = plan_layout<NT, HEAD, GATHER, XRES>(p, st.smem_optin, &smem);
     if (rc != SV_OK) return rc;
@@ -202,10 +220,10 @@ int launch(Params p, const DeviceState &st, cudaStream_t stream)
                        static_cast<unsigned>(Cfg<NT, GATHER>::GPS * 16), 1);
     }
     if (rc != SV_OK) return rc;
-    if (!XRES) {
-        // The activation box is exactly T rows high (boxes reaching past the
-        // tensor are much slower to fill); the kernel zeroes the spare token
-        // rows of every stage once, so B fragments load unconditionally.
+    if (!XRES && NT == 1) {
+        // bf16 activations copied into every stage: the box is exactly T rows
+        // high (boxes reaching past the tensor are much slower to fill); the
+        // kernel zeroes the spare token rows of every stage once.
         rc = encode_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, p.x, static_cast<unsigned long long>(p.K),
                        static_cast<unsigned long long>(p.T), XBOX, static_cast<unsigned>(p.T));
         if (rc != SV_OK) return rc;
@@ -217,22 +235,34 @@ int launch(Params p, const DeviceState &st, cudaStream_t stream)
     p.keys = st.keys;
     p.done = st.done;
     p.err = st.err;
-    // Programmatic dependent launch: the kernel may begin while the previous
+    // Programmatic dependent launch: each kernel may begin while the previous
     // kernel of the stream drains; it waits (griddepcontrol.wait) before it
     // touches anything that kernel could have written.
-    cudaLaunchConfig_t cfg;
-    std::memset(&cfg, 0, sizeof cfg);
-    cfg.gridDim = dim3(static_cast<unsigned>(B));
-    cfg.blockDim = dim3(NTHREADS);
-    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
-    cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, w4a16_stream_kernel<NT, HEAD, GATHER, XRES>, p, tmW, tmX);
-    if (e != cudaSuccess) {
+    if (!XRES && NT > 1) {
+        // several token tiles: convert x into ready-made group blocks first
+        p.x16 = st.x16;
+        p.xinv = st.xinv;
+        cfg.gridDim = dim3(static_cast<unsigned>(Cfg<NT, GATHER>::TP));
+        cfg.blockDim = dim3(XP_THREADS);
+        cfg.dynamicSmemBytes = 0;
+        if (cudaLaunchKernelEx(&cfg, xprep_kernel, p.x, p.T, p.K, Cfg<NT, GATHER>::TP, st.x16, st.xinv) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return SV_ERR_CUDA;
+        }
+    }
+    cfg.gridDim = dim3(static_cast<unsigned>(B));
+    cfg.blockDim = dim3(NTHREADS);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    if (cudaLaunchKernelEx(&cfg, w4a16_stream_kernel<NT, HEAD, GATHER, XRES>, p, tmW, tmX) != cudaSuccess) {
         cudaGetLastError();
         return SV_ERR_CUDA;
     }
@@ -322,7 +352,10 @@ constexpr size_t NOALLOC_CTR_OFF = NOALLOC_PART_BYTES;
 constexpr size_t NOALLOC_KEYS_OFF = NOALLOC_CTR_OFF + 1024;                 // 160 counters, padded
 constexpr size_t NOALLOC_DONE_OFF = NOALLOC_KEYS_OFF + TMAX * sizeof(unsigned long long);
 constexpr size_t NOALLOC_ERR_OFF = NOALLOC_DONE_OFF + 256;
-constexpr size_t NOALLOC_BYTES = NOALLOC_ERR_OFF + 256;
+constexpr int NOALLOC_X16_GROUPS = 128;                                     // K <= 16384
+constexpr size_t NOALLOC_XINV_OFF = NOALLOC_ERR_OFF + 256;
+constexpr size_t NOALLOC_X16_OFF = NOALLOC_XINV_OFF + 256;
+constexpr size_t NOALLOC_BYTES = NOALLOC_X16_OFF + static_cast<size_t>(NOALLOC_X16_GROUPS) * TMAX * XSTR;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_BYTES];
 
@@ -368,6 +401,9 @@ int noalloc_state(DeviceState **out)
         st.keys = reinterpret_cast<unsigned long long *>(base + NOALLOC_KEYS_OFF);
         st.done = reinterpret_cast<unsigned *>(base + NOALLOC_DONE_OFF);
         st.err = reinterpret_cast<int *>(base + NOALLOC_ERR_OFF);
+        st.xinv = reinterpret_cast<float *>(base + NOALLOC_XINV_OFF);
+        st.x16 = base + NOALLOC_X16_OFF;
+        st.x16_max_groups = NOALLOC_X16_GROUPS;
         st.sms = sms < NOALLOC_MAX_CTAS ? sms : NOALLOC_MAX_CTAS;
         st.smem_optin = optin;
         st.ready = true;
@@ -406,7 +442,7 @@ int lmhead_verify_noalloc(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *s
     // The array keeps whatever the last call left: the counters, keys and
     // completion count must start at zero, so clear them (and the error word)
     // on the stream first.
-    if (cudaMemsetAsync(st->ctr, 0, NOALLOC_BYTES - NOALLOC_CTR_OFF, cs) != cudaSuccess) {
+    if (cudaMemsetAsync(st->ctr, 0, NOALLOC_XINV_OFF - NOALLOC_CTR_OFF, cs) != cudaSuccess) {
         cudaGetLastError();
         return SV_ERR_CUDA;
     }

@@ -1,7 +1,7 @@
 // sv_ptx.cuh -- thin inline-PTX wrappers used by the sm_103a kernels:
 // mbarriers, bulk and tensor (TMA) copies global -> shared, cp.async,
-// L2 cache policies, the bf16 tensor-core MMA and the int4 -> bf16x2
-// dequantisation.
+// L2 cache policies, the fp16 and bf16 tensor-core MMAs and the int4 ->
+// fp16x2 / bf16x2 dequantisations.
 #pragma once
 
 #include <cstdint>

@@ -54,8 +54,11 @@ constexpr int EPILOGUE_WARP = NCW + 1;
 constexpr int NTHREADS = (NCW + 2) * 32;
 constexpr int TMAX = 32;                        // largest T
 constexpr int PART_FLOATS = TMAX * ROWS;        // one split-tile partial
-constexpr int XBOX = 144;                       // activation box width (elements)
+constexpr int XBOX = 144;                       // bf16 activation box width (elements), one token tile
 constexpr int XROW_BYTES = XBOX * 2;            // = 32 (mod 128): conflict-free B loads
+constexpr int XSTR = 272;                       // bytes per token row of a converted group block
+                                                // (256 + 16: = 16 mod 128, conflict-free B loads)
+constexpr int XP_THREADS = 256;                 // threads of the activation-conversion kernel
 constexpr int BK_STRIDE = TMAX + 1;             // u64 per lane in the best-key table (odd: no bank conflicts)
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;        // 2 s: only a broken run gets here
 constexpr uint64_t WAIT_LIMIT_AFTER_ERR_NS = 1000000ull;  // 1 ms once something failed
@@ -79,6 +82,8 @@ struct Cfg {
 
 struct Params {
     const uint16_t *x;          // [T][K] bf16 bits
+    const uint8_t *x16;         // converted activations (NT > 1): [G][TP][XSTR] bytes, see xprep_kernel
+    const float *xinv;          // converted activations: 2^-s_t of every token row (1 for rows >= T)
     const uint32_t *Wq;         // [rows][K/8]
     const uint16_t *scales;     // [rows][K/128]
     const int32_t *map;         // HEAD: candidate row -> token id, or null
@@ -145,6 +150,101 @@ __device__ __forceinline__ void wait_or_flag(const Params &p, volatile int *flag
         *flag = 1;
         atomicOr(p.err, 2);
     }
+}
+
+// Largest magnitude among the 8 bf16 values of a 16-byte chunk, as bf16 bits.
+__device__ __forceinline__ unsigned chunk_absmax(const uint4 r)
+{
+    const unsigned hi = max(max(r.x & 0x7FFF0000u, r.y & 0x7FFF0000u), max(r.z & 0x7FFF0000u, r.w & 0x7FFF0000u)) >> 16;
+    const unsigned lo = max(max(r.x & 0x7FFFu, r.y & 0x7FFFu), max(r.z & 0x7FFFu, r.w & 0x7FFFu));
+    return max(hi, lo);
+}
+
+// A chunk of 8 bf16 activations (x0..x7) -> fp16 x * sc in B-fragment order:
+// (x0,x4) (x1,x5) (x2,x6) (x3,x7), the pairing of the dequantised nibbles.
+__device__ __forceinline__ uint4 chunk_to_f16(const uint4 r, float sc)
+{
+    uint4 v;
+    v.x = pack_f16x2(__uint_as_float(r.x << 16) * sc, __uint_as_float(r.z << 16) * sc);
+    v.y = pack_f16x2(__uint_as_float(r.x & 0xFFFF0000u) * sc, __uint_as_float(r.z & 0xFFFF0000u) * sc);
+    v.z = pack_f16x2(__uint_as_float(r.y << 16) * sc, __uint_as_float(r.w << 16) * sc);
+    v.w = pack_f16x2(__uint_as_float(r.y & 0xFFFF0000u) * sc, __uint_as_float(r.w & 0xFFFF0000u) * sc);
+    return v;
+}
+
+// Position of chunk i (0..15) of a group inside its 256-byte row: chunk
+// index XOR-swizzled (bit 1 ^= bit 3), so that the B loads of a quarter warp
+// (chunks 4c + m, c = 0..3) hit distinct banks.
+__device__ __forceinline__ int chunk_slot(int i)
+{
+    return i ^ ((i >> 2) & 2);
+}
+
+// Activations for the kernels that stream them per stage (T > 8, or rows too
+// long to keep resident): x (bf16 [T][K]) is converted once per call into
+// x16, laid out per 128-column group g as a block of TP token rows of XSTR
+// bytes; row t holds the group's 16 chunks as fp16 x[t] * 2^s_t in
+// B-fragment order at chunk_slot positions (the same encoding as the
+// resident rows of the main kernel); rows T..TP-1 are zeros.  xinv[t] =
+// 2^-s_t.  One CTA per token row.  The main kernel then copies ready-made
+// group blocks into its stages (one bulk copy per group) and its B loads
+// need neither byte permutes nor conversion.
+__global__ void __launch_bounds__(XP_THREADS) xprep_kernel(const uint16_t *x, int T, int K, int TP, uint8_t *x16,
+                                                           float *xinv)
+{
+    pdl_launch_dependents();
+    pdl_wait_prior();                   // x may come from the previous kernel
+    const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int cpr = K / 8;              // 16-byte chunks per row
+    if (t >= T) {
+        for (int i = tid; i < cpr; i += XP_THREADS)
+            *reinterpret_cast<uint4 *>(x16 + (static_cast<size_t>(i >> 4) * TP + t) * XSTR + (i & 15) * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+        if (tid == 0) xinv[t] = 1.f;
+        return;
+    }
+    const uint4 *row = reinterpret_cast<const uint4 *>(x) + static_cast<size_t>(t) * cpr;
+    constexpr int XB = 12;
+    const bool one_batch = cpr <= XB * XP_THREADS;
+    uint4 r[XB];
+    unsigned mx = 0u;
+    for (int i0 = tid; i0 < cpr; i0 += XB * XP_THREADS) {
+#pragma unroll
+        for (int u = 0; u < XB; ++u) {
+            const int i = i0 + u * XP_THREADS;
+            r[u] = i < cpr ? row[i] : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < XB; ++u) mx = max(mx, chunk_absmax(r[u]));
+        if (one_batch) break;
+    }
+    __shared__ unsigned wmax[XP_THREADS / 32];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+    if (lane == 0) wmax[warp] = mx;
+    __syncthreads();
+    mx = 0u;
+#pragma unroll
+    for (int w = 0; w < XP_THREADS / 32; ++w) mx = max(mx, wmax[w]);
+    const int sh = xres_shift(mx);
+    const float sc = __uint_as_float(static_cast<uint32_t>(127 + sh) << 23);
+    for (int i0 = tid; i0 < cpr; i0 += XB * XP_THREADS) {
+        if (!one_batch) {
+#pragma unroll
+            for (int u = 0; u < XB; ++u) {
+                const int i = i0 + u * XP_THREADS;
+                r[u] = i < cpr ? row[i] : make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < XB; ++u) {
+            const int i = i0 + u * XP_THREADS;
+            if (i < cpr)
+                *reinterpret_cast<uint4 *>(x16 + (static_cast<size_t>(i >> 4) * TP + t) * XSTR +
+                                           chunk_slot(i & 15) * 16) = chunk_to_f16(r[u], sc);
+        }
+    }
+    if (tid == 0) xinv[t] = __uint_as_float(static_cast<uint32_t>(127 - sh) << 23);
 }
 
 // Epilogue warp: stage the scales (and, for the head, the token ids) of one
@@ -214,6 +314,13 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
 {
     using C = Cfg<NT, GATHER>;
     static_assert(!XRES || NT == 1, "resident activations are laid out for one n8 token tile");
+    // How activations reach the B loads: resident fp16 rows (XRES); raw bf16
+    // rows copied into every stage by tensor copies (XBF: one token tile
+    // whose rows are too long to keep resident; permuted in registers, bf16
+    // dequant); or fp16 group blocks prepared by xprep_kernel and copied into
+    // every stage (XPREP: more than one token tile).
+    constexpr bool XBF = !XRES && NT == 1;
+    constexpr bool XPREP = !XRES && NT > 1;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int nst = p.nst;
     uint8_t *sbuf = smem + p.off_sbuf;                                // [2][sbuf_bytes]
@@ -254,9 +361,9 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
             for (int t = 0; t < 8; ++t) reinterpret_cast<unsigned *>(smem + p.off_xsc)[t] = 0u;
         fence_barrier_init();
     }
-    // Token rows T..TP-1 of every stage's activation slots stay zero for the
-    // whole kernel (the tensor copies only write rows 0..T-1).
-    if (!XRES && T < C::TP) {
+    // XBF: token rows T..TP-1 of every stage's activation slots stay zero for
+    // the whole kernel (the tensor copies only write rows 0..T-1).
+    if (XBF && T < C::TP) {
         const int per_slot = (C::TP - T) * XROW_BYTES / 16;
         const int total = nst * C::GPS * per_slot;
         for (int i = threadIdx.x; i < total; i += NTHREADS) {
@@ -277,7 +384,7 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
         const uint64_t pol_x = policy_evict_last();
         if (lane == 0) {
             prefetch_tmap(&tmW);
-            if (!XRES) prefetch_tmap(&tmX);
+            if (XBF) prefetch_tmap(&tmX);
         }
         int s = 0, issued = 0, tile = tile_first, grp = grp_first, rem = n_units;
         uint32_t ph = 0;
@@ -306,7 +413,9 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
             // gathered rows: 16 boxes of 4 full rows (GPS groups, zeros for
             // absent rows and past the end of K)
             const uint32_t wbytes = GATHER ? static_cast<uint32_t>(ROWS * C::GROW) : static_cast<uint32_t>(n * ROWS * 64);
-            const uint32_t xbytes = XRES ? 0u : static_cast<uint32_t>(n * T * XROW_BYTES);
+            const uint32_t xbytes = XRES  ? 0u
+                                    : XBF ? static_cast<uint32_t>(n * T * XROW_BYTES)
+                                          : static_cast<uint32_t>(n * p.xslot_bytes);
             if (lane == 0) mbar_arrive_expect_tx(fb, wbytes + xbytes);
             __syncwarp();
             if (GATHER) {
@@ -335,9 +444,13 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
                 pdl_wait_prior();   // activations may come from the previous kernel
                 waited = true;
             }
-            if (!XRES && lane >= 16 && lane - 16 < n)
-                tma_load_2d(stage + C::W_BYTES + (lane - 16) * p.xslot_bytes, &tmX,
-                            (grp + lane - 16) * 128, 0, fb, pol_x);
+            if (XBF && lane >= 16 && lane - 16 < n)
+                tma_load_2d(stage + C::W_BYTES + (lane - 16) * p.xslot_bytes, &tmX, (grp + lane - 16) * 128, 0, fb,
+                            pol_x);
+            if (XPREP && lane >= 16 && lane - 16 < n)
+                bulk_g2s(stage + C::W_BYTES + (lane - 16) * p.xslot_bytes,
+                         p.x16 + static_cast<size_t>(grp + lane - 16) * p.xslot_bytes,
+                         static_cast<uint32_t>(p.xslot_bytes), fb, pol_x);
             rem -= n;
             grp += n;
             if (grp == G) {
@@ -663,19 +776,21 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
     const int row0 = mset * C::R * 16 + g;                     // first row of this lane
     const uint32_t w_lane = GATHER ? static_cast<uint32_t>(row0 * C::GROW + slot * 64 + c * 16)
                                    : static_cast<uint32_t>(slot * (ROWS * 64) + row0 * 64 + c * 16);
-    const uint32_t x_lane = static_cast<uint32_t>(C::W_BYTES + slot * p.xslot_bytes + g * XROW_BYTES + c * 64);
+    const uint32_t x_lane = XBF ? static_cast<uint32_t>(C::W_BYTES + slot * p.xslot_bytes + g * XROW_BYTES + c * 64)
+                                : static_cast<uint32_t>(C::W_BYTES + slot * p.xslot_bytes + g * XSTR + c * 64);
     const uint32_t s_lane = static_cast<uint32_t>(row0 * G * 2);
     const uint32_t sbuf0 = smem_addr(sbuf);
     const uint32_t smem0 = smem_addr(smem);
 
-    // Resident activations: x[t] is stored once per CTA as rows of 16-byte
-    // chunks, each chunk holding its 8 values in B-fragment order
-    // (x0,x4, x1,x5, x2,x6, x3,x7), chunk index XOR-swizzled (bit 1 ^= bit 3)
-    // and rows padded to 16 (mod 128) bytes, so that the B loads below are
-    // conflict-free and need no byte permutes.  Row T is zeros, read by the
-    // lanes of absent tokens.
+    // Activations reach the B loads as rows of 16-byte chunks, each chunk
+    // holding its 8 values in B-fragment order (x0,x4, x1,x5, x2,x6, x3,x7),
+    // chunk index XOR-swizzled (chunk_slot) and rows padded to 16 (mod 128)
+    // bytes, so that the B loads are conflict-free and need no byte permutes:
+    // resident in shared memory for the whole kernel (XRES; row T is zeros,
+    // read by the lanes of absent tokens), or as ready-made group blocks
+    // copied into each stage (xprep_kernel; rows T..TP-1 are zeros).
     //
-    // The resident rows are fp16, not bf16: row t holds x[t] * 2^s_t, with
+    // The rows are fp16, not bf16: row t holds x[t] * 2^s_t, with
     // s_t chosen so that the row's largest magnitude lands in [2^14, 2^15).
     // A bf16 value has 8 significant bits and fp16 11, so every element of
     // magnitude >= 2^-32 of the row maximum converts exactly (smaller ones
@@ -685,9 +800,16 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
     // a power-of-two scale commutes with fp32 rounding, so multiplying each
     // token's sums by 2^-s_t at the end of a tile gives exactly the sums of
     // the unscaled bf16 products.
-    uint32_t xr_lane = 0, xr_off[4] = {0, 0, 0, 0};
-    float xinv[2] = {1.f, 1.f};        // 2^-s of tokens 2c and 2c+1
-    if constexpr (XRES) {
+    // chunk_slot(4c + m) * 16 = 64c + ((16m) ^ xsw): the m-dependent part is
+    // a compile-time offset XOR one lane constant
+    const uint32_t xsw = static_cast<uint32_t>((c & 2) * 16);
+    uint32_t xr_lane = 0;
+    // 2^-s of tokens 2c and 2c+1 (resident rows; streamed rows read
+    // p.xinv at the end of each tile instead of holding 2*NT registers)
+    float xinv[2] = {1.f, 1.f};
+    if constexpr (XPREP) {
+        pdl_wait_prior();              // p.xinv comes from the conversion kernel
+    } else if constexpr (XRES) {
         pdl_wait_prior();                  // activations may come from the previous kernel
         // Token-major: the warps of token tt (wpt of them) load its row,
         // XB 16-byte chunks per thread in flight at once, and reduce the
@@ -716,13 +838,7 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
                 r[u] = (loader && j < cpr) ? xrow[j] : make_uint4(0u, 0u, 0u, 0u);
             }
 #pragma unroll
-            for (int u = 0; u < XB; ++u) {
-                const unsigned hi = max(max(r[u].x & 0x7FFF0000u, r[u].y & 0x7FFF0000u),
-                                        max(r[u].z & 0x7FFF0000u, r[u].w & 0x7FFF0000u)) >> 16;
-                const unsigned lo = max(max(r[u].x & 0x7FFFu, r[u].y & 0x7FFFu),
-                                        max(r[u].z & 0x7FFFu, r[u].w & 0x7FFFu));
-                mx = max(mx, max(hi, lo));
-            }
+            for (int u = 0; u < XB; ++u) mx = max(mx, chunk_absmax(r[u]));
             if (one_batch) break;
         }
 #pragma unroll
@@ -745,20 +861,7 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
 #pragma unroll
                 for (int u = 0; u < XB; ++u) {
                     const int j = jb + u * nthr;
-                    if (j < cpr) {
-                        // (x0,x4) (x1,x5) (x2,x6) (x3,x7) as fp16 pairs
-                        const uint32_t lo0 = r[u].x << 16, hi0 = r[u].x & 0xFFFF0000u;
-                        const uint32_t lo1 = r[u].y << 16, hi1 = r[u].y & 0xFFFF0000u;
-                        const uint32_t lo2 = r[u].z << 16, hi2 = r[u].z & 0xFFFF0000u;
-                        const uint32_t lo3 = r[u].w << 16, hi3 = r[u].w & 0xFFFF0000u;
-                        uint4 v;
-                        v.x = pack_f16x2(__uint_as_float(lo0) * sc, __uint_as_float(lo2) * sc);
-                        v.y = pack_f16x2(__uint_as_float(hi0) * sc, __uint_as_float(hi2) * sc);
-                        v.z = pack_f16x2(__uint_as_float(lo1) * sc, __uint_as_float(lo3) * sc);
-                        v.w = pack_f16x2(__uint_as_float(hi1) * sc, __uint_as_float(hi3) * sc);
-                        const int sw = j ^ ((j >> 2) & 2);
-                        sts128(smem_addr(xdst + sw * 16), v);
-                    }
+                    if (j < cpr) sts128(smem_addr(xdst + ((j & ~15) + chunk_slot(j & 15)) * 16), chunk_to_f16(r[u], sc));
                 }
             }
         }
@@ -766,11 +869,9 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             const int tok = 2 * c + e;
-            if (tok < T) xinv[e] = __uint_as_float(static_cast<uint32_t>(127 - xres_shift(xmax[tok])) << 23);
+            xinv[e] = tok < T ? __uint_as_float(static_cast<uint32_t>(127 - xres_shift(xmax[tok])) << 23) : 1.f;
         }
-        xr_lane = smem_addr(xr) + static_cast<uint32_t>((g < T ? g : T) * p.xres_stride);
-#pragma unroll
-        for (int m = 0; m < 4; ++m) xr_off[m] = static_cast<uint32_t>((4 * c + (m ^ (c & 2))) * 16);
+        xr_lane = smem_addr(xr) + static_cast<uint32_t>((g < T ? g : T) * p.xres_stride + c * 64);
     }
 
     float acc[C::R][NT][4];
@@ -813,59 +914,58 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
                 uint32_t bx[NT][4];
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    if constexpr (XRES) {
-                        const uint4 v = lds128(xbase + xr_off[m]);
-                        bx[nt][0] = v.x;
-                        bx[nt][1] = v.y;
-                        bx[nt][2] = v.z;
-                        bx[nt][3] = v.w;
-                    } else {
-                        const uint4 v = lds128(xbase + nt * 8 * XROW_BYTES + m * 16);
+                    if constexpr (XBF) {
+                        const uint4 v = lds128(xbase + m * 16);
                         bx[nt][0] = __byte_perm(v.x, v.z, 0x5410);   // (x0, x4)
                         bx[nt][1] = __byte_perm(v.x, v.z, 0x7632);   // (x1, x5)
                         bx[nt][2] = __byte_perm(v.y, v.w, 0x5410);   // (x2, x6)
                         bx[nt][3] = __byte_perm(v.y, v.w, 0x7632);   // (x3, x7)
+                    } else {
+                        const uint4 v = lds128(xbase + (XRES ? 0 : nt * 8 * XSTR) + ((16u * m) ^ xsw));
+                        bx[nt][0] = v.x;
+                        bx[nt][1] = v.y;
+                        bx[nt][2] = v.z;
+                        bx[nt][3] = v.w;
                     }
                 }
 #pragma unroll
                 for (int r = 0; r < C::R; ++r) {
                     const uint32_t wA = (m == 0) ? wa[r].x : (m == 1) ? wa[r].y : (m == 2) ? wa[r].z : wa[r].w;
                     const uint32_t wB = (m == 0) ? wb[r].x : (m == 1) ? wb[r].y : (m == 2) ? wb[r].z : wb[r].w;
-                    if constexpr (XRES) {
-                        // fp16: k-step 2m takes nibble pairs (0,4) and (1,5),
-                        // k-step 2m+1 pairs (2,6) and (3,7) of the word >> 8
-                        uint32_t a0 = dequant2_f16_lo(wA), a1 = dequant2_f16_lo(wB);
-                        uint32_t a2 = dequant2_f16_hi(wA), a3 = dequant2_f16_hi(wB);
+                    if constexpr (XBF) {
+                        // bf16 activations: bf16 levels, three shifts per word
+                        uint32_t a0 = dequant2(wA), a1 = dequant2(wB);
+                        uint32_t a2 = dequant2(wA >> 4), a3 = dequant2(wB >> 4);
                         if (m == 0)
-                            mma_f16_16816_zc(gacc[r][0], a0, a1, a2, a3, bx[0][0], bx[0][1]);
+                            mma_bf16_16816_zc(gacc[r][0], a0, a1, a2, a3, bx[0][0], bx[0][1]);
                         else
-                            mma_f16_16816(gacc[r][0], a0, a1, a2, a3, bx[0][0], bx[0][1]);
-                        const uint32_t wA8 = wA >> 8, wB8 = wB >> 8;
-                        a0 = dequant2_f16_lo(wA8);
-                        a1 = dequant2_f16_lo(wB8);
-                        a2 = dequant2_f16_hi(wA8);
-                        a3 = dequant2_f16_hi(wB8);
-                        mma_f16_16816(gacc[r][0], a0, a1, a2, a3, bx[0][2], bx[0][3]);
+                            mma_bf16_16816(gacc[r][0], a0, a1, a2, a3, bx[0][0], bx[0][1]);
+                        a0 = dequant2(wA >> 8);
+                        a1 = dequant2(wB >> 8);
+                        a2 = dequant2(wA >> 12);
+                        a3 = dequant2(wB >> 12);
+                        mma_bf16_16816(gacc[r][0], a0, a1, a2, a3, bx[0][2], bx[0][3]);
                         continue;
                     }
-                    // k-step 2m: nibble pairs (0,4) and (1,5)
-                    uint32_t a0 = dequant2(wA), a1 = dequant2(wB);
-                    uint32_t a2 = dequant2(wA >> 4), a3 = dequant2(wB >> 4);
+                    // k-step 2m: nibble pairs (0,4) and (1,5); k-step 2m+1:
+                    // pairs (2,6) and (3,7) of the word >> 8
+                    uint32_t a0 = dequant2_f16_lo(wA), a1 = dequant2_f16_lo(wB);
+                    uint32_t a2 = dequant2_f16_hi(wA), a3 = dequant2_f16_hi(wB);
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
                         if (m == 0)
-                            mma_bf16_16816_zc(gacc[r][nt], a0, a1, a2, a3, bx[nt][0], bx[nt][1]);
+                            mma_f16_16816_zc(gacc[r][nt], a0, a1, a2, a3, bx[nt][0], bx[nt][1]);
                         else
-                            mma_bf16_16816(gacc[r][nt], a0, a1, a2, a3, bx[nt][0], bx[nt][1]);
+                            mma_f16_16816(gacc[r][nt], a0, a1, a2, a3, bx[nt][0], bx[nt][1]);
                     }
-                    // k-step 2m+1: nibble pairs (2,6) and (3,7)
-                    a0 = dequant2(wA >> 8);
-                    a1 = dequant2(wB >> 8);
-                    a2 = dequant2(wA >> 12);
-                    a3 = dequant2(wB >> 12);
+                    const uint32_t wA8 = wA >> 8, wB8 = wB >> 8;
+                    a0 = dequant2_f16_lo(wA8);
+                    a1 = dequant2_f16_lo(wB8);
+                    a2 = dequant2_f16_hi(wA8);
+                    a3 = dequant2_f16_hi(wB8);
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt)
-                        mma_bf16_16816(gacc[r][nt], a0, a1, a2, a3, bx[nt][2], bx[nt][3]);
+                        mma_f16_16816(gacc[r][nt], a0, a1, a2, a3, bx[nt][2], bx[nt][3]);
                 }
             }
             // group scales of this lane's rows (staged in shared memory)
@@ -901,7 +1001,8 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
                     for (int e = 0; e < 4; ++e) {
                         const int row = (mset * C::R + r) * 16 + g + 8 * (e >> 1);
                         const int tok = nt * 8 + 2 * c + (e & 1);
-                        red[(slot * C::TP + tok) * ROWS + row] = XRES ? acc[r][nt][e] * xinv[e & 1] : acc[r][nt][e];
+                        red[(slot * C::TP + tok) * ROWS + row] =
+                            XBF ? acc[r][nt][e] : acc[r][nt][e] * (XRES ? xinv[e & 1] : __ldg(p.xinv + tok));
                         acc[r][nt][e] = 0.f;
                     }
             __syncwarp();

@@ -41,7 +41,8 @@ def _p(t):
     return ctypes.c_void_p(t.data_ptr())
 
 
-@pytest.mark.parametrize("V,K,n_draft,n_map", [(30011, 1024, 3, 0), (20000, 512, 7, 5000)])
+@pytest.mark.parametrize("V,K,n_draft,n_map", [(30011, 1024, 3, 0), (20000, 512, 7, 5000),
+                                                 (9000, 1280, 15, 0), (7000, 768, 31, 3000)])
 def test_noalloc_matches_regular_entry_point(lib, oracle, V, K, n_draft, n_map):
     rng = np.random.default_rng(4242 + V + n_map)
     Wq, sc = gen.weights(rng, V, K)
@@ -87,3 +88,16 @@ def test_noalloc_rejects_too_many_drafts(lib):
     rc = lib.lmhead_verify_noalloc(_p(buf), _p(buf), _p(buf), 128, _p(buf), 32, None, 0, 16,
                                    _p(buf), _p(buf), None)
     assert rc == -2
+
+
+def test_noalloc_rejects_long_rows_with_more_than_7_drafts(lib):
+    """With more than 7 drafts the activations go through the library's
+    fixed conversion buffer, sized for K <= 16384: a longer row is refused
+    before any kernel launch."""
+    buf = torch.zeros(64, dtype=torch.int32, device="cuda")
+    out = torch.full((2,), -7, dtype=torch.int32, device="cuda")
+    rc = lib.lmhead_verify_noalloc(_p(buf), _p(buf), _p(buf), 16384 + 128, _p(buf), 15, None, 0, 16,
+                                   _p(out), _p(out[1:]), None)
+    assert rc == -2
+    torch.cuda.synchronize()
+    assert out.tolist() == [-7, -7]
