@@ -161,7 +161,7 @@ int plan_layout(Params &p, int smem_optin, int *smem_total)
     using C = Cfg<NT, GATHER>;
     auto up = [](int v, int a) { return (v + a - 1) / a * a; };
     p.xslot_bytes = NT > 1 ? C::TP * XSTR                 // one group block of xprep_kernel
-                           : up(C::TP * XROW_BYTES, 128);    // a bf16 activation box
+                           : up(p.T * XROW_BYTES, 128);      // a bf16 activation box of the T rows
     p.stage_bytes = XRES ? C::W_BYTES : up(C::W_BYTES + C::GPS * p.xslot_bytes, 128);
     p.sbuf_bytes = up(ROWS * p.G * 2, 128);
     p.xres_stride = 2 * p.K + 16;                     // = 16 (mod 128)
@@ -169,7 +169,8 @@ int plan_layout(Params &p, int smem_optin, int *smem_total)
     const int ids_bytes = up(2 * ROWS * 4, 128);
     const int red_bytes = up(C::RED_FLOATS * 4, 128);
     const int bk_bytes = HEAD ? up(32 * BK_STRIDE * 8, 128) : 0;
-    const int fixed = xres_bytes + 2 * p.sbuf_bytes + ids_bytes + red_bytes + 128 + ROWS * 8 * 4 + bk_bytes + 7 * 8 + 8;
+    const int fixed = xres_bytes + 2 * p.sbuf_bytes + ids_bytes + red_bytes + 128 + ROWS * 8 * 4 + bk_bytes + 256 +
+                      7 * 8 + 8;
     int nst = (smem_optin - fixed - 1024) / (p.stage_bytes + 16);
     if (nst > 8) nst = 8;
     if (nst < 2) return SV_ERR_SHAPE;
@@ -189,6 +190,8 @@ int plan_layout(Params &p, int smem_optin, int *smem_total)
     off += ROWS * 8 * 4;
     p.off_bk = off;
     off += bk_bytes;
+    p.off_xzero = off;
+    off += 256;
     p.off_bars = off;
     off += (2 * nst + 6) * 8 + 8;
     *smem_total = off;

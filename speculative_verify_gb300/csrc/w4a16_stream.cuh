@@ -98,6 +98,7 @@ struct Params {
     int off_xsc;                // XRES: per-token largest |x| (bf16 bits), [8] u32
     int off_pre;                // prefetched partial of a split last tile, [ROWS][8] floats
     int off_bk;                 // HEAD: running best key per lane and token, [32][BK_STRIDE] u64
+    int off_xzero;              // XBF: 256 zero bytes, the activation row of absent tokens
     // GEMM output
     uint16_t *y;                // [T][N]
     // HEAD outputs
@@ -361,20 +362,10 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
             for (int t = 0; t < 8; ++t) reinterpret_cast<unsigned *>(smem + p.off_xsc)[t] = 0u;
         fence_barrier_init();
     }
-    // XBF: token rows T..TP-1 of every stage's activation slots stay zero for
-    // the whole kernel (the tensor copies only write rows 0..T-1).
-    if (XBF && T < C::TP) {
-        const int per_slot = (C::TP - T) * XROW_BYTES / 16;
-        const int total = nst * C::GPS * per_slot;
-        for (int i = threadIdx.x; i < total; i += NTHREADS) {
-            const int st = i / (C::GPS * per_slot), rest = i % (C::GPS * per_slot);
-            const int sl = rest / per_slot, q = rest % per_slot;
-            uint4 *d = reinterpret_cast<uint4 *>(smem + static_cast<size_t>(st) * p.stage_bytes + C::W_BYTES +
-                                                 sl * p.xslot_bytes + T * XROW_BYTES) + q;
-            *d = make_uint4(0u, 0u, 0u, 0u);
-        }
-        fence_proxy_async();
-    }
+    // XBF: the stages hold only the T real token rows; lanes of absent
+    // tokens read this zero row instead.
+    if (XBF && threadIdx.x < 16)
+        reinterpret_cast<uint4 *>(smem + p.off_xzero)[threadIdx.x] = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
     pdl_launch_dependents();
 
@@ -779,6 +770,7 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
     const uint32_t x_lane = XBF ? static_cast<uint32_t>(C::W_BYTES + slot * p.xslot_bytes + g * XROW_BYTES + c * 64)
                                 : static_cast<uint32_t>(C::W_BYTES + slot * p.xslot_bytes + g * XSTR + c * 64);
     const uint32_t s_lane = static_cast<uint32_t>(row0 * G * 2);
+    const uint32_t xzero_lane = smem_addr(smem + p.off_xzero) + static_cast<uint32_t>(c * 64);
     const uint32_t sbuf0 = smem_addr(sbuf);
     const uint32_t smem0 = smem_addr(smem);
 
@@ -905,7 +897,9 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
             }
             float gacc[C::R][NT][4];     // first k-step writes, later ones accumulate
 
-            const uint32_t xbase = XRES ? xr_lane + gs * 256 : stage + x_lane;
+            const uint32_t xbase = XRES ? xr_lane + gs * 256
+                                   : (XBF && g >= T) ? xzero_lane
+                                                     : stage + x_lane;
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
                 // B fragments: token (nt*8 + g), the 8 activations of word
