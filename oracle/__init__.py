@@ -190,3 +190,62 @@ def lmhead_verify(x, Wq, scales, K, V, drafts, n_streams=1, vocab_map=None):
     margin = (best.astype(np.float64) - second.astype(np.float64))
     return VerifyResult(acc, nxt, a, margin, logits)
 
+
+
+# ----------------------------------------------------------------------------
+# Dynamic draft list (list maintenance for the restricted draft head)
+#
+# Sources: "OpenJet Engine: CUDA LLM inference for Qwen3.8-27B" -- "How it
+# gets its speed" (the draft lm_head scores a static list of the most
+# frequent tokens plus the tokens of the current sequence missing from it,
+# added on the fly); "Tesla P100 (sm_60) llama.cpp patches for
+# Qwen3.5/3.6-35B-A3B: ~2x decode and prompt processing over the shinbunbun
+# baseline" -- "MTP draft vocabulary (patch 17)" and "The draft vocabulary
+# file" (the draft head also scores every token that has appeared in the
+# conversation, up to 4096 of them).
+#
+# The pages fix what the list contains (static ids, then sequence tokens not
+# already in it, at most `cap` of them); the order of the added tokens and
+# what happens past the cap are readings: added tokens keep their order of
+# first appearance, and once `cap` tokens were added, later new tokens are
+# not added.  Tokens outside [0, V) are ignored.  The list always has
+# n_static + cap entries: unused dynamic slots repeat static_ids[0], which
+# changes no argmax (a duplicate candidate ties with itself).
+
+
+@dataclass
+class DraftList:
+    V: int
+    static: list
+    cap: int
+    added: list
+
+    def ids(self) -> np.ndarray:
+        pad = self.static[0]
+        dyn = self.added + [pad] * (self.cap - len(self.added))
+        return np.array(self.static + dyn, dtype=np.int32)
+
+    @property
+    def count(self) -> int:
+        return len(self.added)
+
+
+def draft_list_init(static_ids, V: int, cap: int) -> DraftList:
+    static = [int(t) for t in np.asarray(static_ids).ravel()]
+    assert len(static) >= 1 and cap >= 0
+    assert all(0 <= t < V for t in static)
+    return DraftList(V=V, static=static, cap=cap, added=[])
+
+
+def draft_list_add(dl: DraftList, tokens) -> DraftList:
+    """Append, in order, every token of `tokens` that is in [0, V), not in
+    the static list and not already added, while fewer than cap were added."""
+    member = set(dl.static) | set(dl.added)
+    for t in np.asarray(tokens).ravel():
+        t = int(t)
+        if len(dl.added) >= dl.cap:
+            break
+        if 0 <= t < dl.V and t not in member:
+            dl.added.append(t)
+            member.add(t)
+    return dl

@@ -361,3 +361,54 @@ def test_fp32_oracle_within_rounding_of_its_fp64_twin(oracle):
     y32, _, y64 = oracle.w4a16_gemm(x, Wq, sc, T, K, N, want64=True)
     rel = np.abs(y32 - y64).max() / np.abs(y64).max()
     assert rel < 1e-5
+
+
+# --------------------------------------------------------------------------
+# dynamic draft list (list maintenance of the restricted draft head)
+
+
+def test_draft_list_hand_case(oracle):
+    """Static [5, 9, 2], V = 20, cap 4.  Adding 9 (static), 7, 7 (repeat),
+    25 and -1 (out of range), 3, 5 (static), 11, 12, 13: the list gains
+    7, 3, 11, 12 in that order and 13 finds it full."""
+    dl = oracle.draft_list_init([5, 9, 2], 20, 4)
+    oracle.draft_list_add(dl, [9, 7, 7, 25, -1, 3, 5, 11, 12, 13])
+    assert dl.count == 4
+    assert dl.ids().tolist() == [5, 9, 2, 7, 3, 11, 12]
+
+
+def test_draft_list_unused_slots_repeat_first_static_id(oracle):
+    dl = oracle.draft_list_init([8, 1], 10, 3)
+    assert dl.ids().tolist() == [8, 1, 8, 8, 8]
+    oracle.draft_list_add(dl, [4])
+    assert dl.ids().tolist() == [8, 1, 4, 8, 8]
+    dl0 = oracle.draft_list_init([8, 1], 10, 0)
+    oracle.draft_list_add(dl0, [4, 5])
+    assert dl0.ids().tolist() == [8, 1]
+
+
+def test_draft_list_matches_first_occurrence_definition(oracle):
+    """Independent formulation with numpy: the added tokens are the in-range
+    tokens of the concatenated sequence outside the static list, at their
+    first occurrence, in sequence order, truncated to cap; adding in several
+    calls equals adding the concatenation."""
+    rng = np.random.default_rng(31)
+    for trial in range(20):
+        V = int(rng.integers(50, 400))
+        static = rng.choice(V, size=int(rng.integers(1, 40)), replace=False)
+        cap = int(rng.integers(0, 60))
+        seq = rng.integers(-5, V + 5, size=int(rng.integers(0, 300)))
+        inr = seq[(seq >= 0) & (seq < V)]
+        inr = inr[~np.isin(inr, static)]
+        _, first = np.unique(inr, return_index=True)
+        expect = inr[np.sort(first)][:cap]
+        dl = oracle.draft_list_init(static, V, cap)
+        cuts = np.sort(rng.integers(0, seq.size + 1, size=3))
+        for a, b in zip(np.r_[0, cuts], np.r_[cuts, seq.size]):
+            oracle.draft_list_add(dl, seq[a:b])
+        assert dl.count == expect.size
+        ids = dl.ids()
+        assert ids.size == static.size + cap
+        assert ids[:static.size].tolist() == static.tolist()
+        assert ids[static.size:static.size + expect.size].tolist() == expect.tolist()
+        assert np.all(ids[static.size + expect.size:] == static[0])
