@@ -497,8 +497,35 @@ def per_kernel_breakdown(torch, sv, device, stream, reps=50):
     for T, S in ((1, 1), (4, 1), (8, 1), (32, 4)):
         cases.append(("head", "lm_head", gen.HIDDEN, gen.VOCAB, (T, S)))
     cases.append(("head_map", "restricted", gen.HIDDEN, gen.VOCAB, (4, 1)))
+    # the greedy draft step over a full dynamic draft list (32,768 static ids
+    # + 4,096 sequence tokens), and the list maintenance call itself
+    cases.append(("draft_step", "list_32768+4096", gen.HIDDEN, gen.VOCAB, 1))
+    cases.append(("draft_list_add", "32_tokens", 0, gen.VOCAB, 32))
+    cases.append(("draft_list_add", "4096_tokens", 0, gen.VOCAB, 4096))
     for kind, label, K, N, T in cases:
-        if kind == "gemm":
+        if kind in ("draft_step", "draft_list_add"):
+            ids = rng.permutation(N).astype(np.int32)
+            static = dev(ids[:32768], np.int32)
+            dl = sv.DraftList(static, N, 4096)
+            if kind == "draft_step":
+                dl.add(dev(ids[32768:32768 + 4096], np.int32))
+                Wq, sc = gen.weights(rng, N, K)
+                Ws = [(dev(Wq, np.int32), dev(sc, np.int16)) for _ in range(2)]
+                copies = 2
+                x = dev(gen.activations(rng, 1, K), np.int16)
+                a_ids = torch.empty(1, dtype=torch.int32, device=device)
+                a_vals = torch.empty(1, dtype=torch.float32, device=device)
+                fn = lambda i: sv.lmhead_argmax(x, Ws[i % copies][0], Ws[i % copies][1], vocab_map=dl.ids,
+                                                ids=a_ids, vals=a_vals)
+                nbytes = gen.lmhead_bytes(N, K, 1, n_map=32768 + 4096, n_streams=1, n_draft=0)
+            else:
+                # tokens that are all in the static list: every round of the
+                # scan runs (worst case of one call)
+                Ws = []
+                toks = dev(ids[:T], np.int32)
+                fn = lambda i: dl.add(toks)
+                nbytes = None
+        elif kind == "gemm":
             wbytes = N * K // 2
             copies = max(2, int(np.ceil(2 * l2 / wbytes)))
             Wq, sc = gen.weights(rng, N, K)
@@ -542,9 +569,12 @@ def per_kernel_breakdown(torch, sv, device, stream, reps=50):
         e1.record(stream)
         torch.cuda.synchronize()
         us = e0.elapsed_time(e1) * 1e3 / reps
-        gbs = nbytes / (us * 1e-6) / 1e9
-        out.append({"kernel": kind, "shape": label, "K": K, "N": N, "T": T, "us": round(us, 2),
-                    "GB/s": round(gbs, 1), "frac_8TBps": round(gbs / NOMINAL_HBM_GBS, 3)})
+        if nbytes is None:
+            out.append({"kernel": kind, "shape": label, "V": N, "tokens": T, "us": round(us, 2)})
+        else:
+            gbs = nbytes / (us * 1e-6) / 1e9
+            out.append({"kernel": kind, "shape": label, "K": K, "N": N, "T": T, "us": round(us, 2),
+                        "GB/s": round(gbs, 1), "frac_8TBps": round(gbs / NOMINAL_HBM_GBS, 3)})
         del Ws, graph
         torch.cuda.empty_cache()
     return out

@@ -37,6 +37,7 @@
 #ifndef SPECVERIFY_H
 #define SPECVERIFY_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -170,6 +171,41 @@ int lmhead_verify_noalloc(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *s
                           const int32_t *drafts, int n_draft,
                           const int32_t *vocab_map, int n_map, int V,
                           int32_t *accept_len, int32_t *next_token, sv_stream stream);
+
+/*
+ * Dynamic draft list -- the candidate list of the restricted draft head: a
+ * static list of token ids (the most frequent tokens) plus the tokens of the
+ * current sequence that are missing from it, added as the sequence grows,
+ * at most `cap` of them (page "OpenJet Engine: CUDA LLM inference for
+ * Qwen3.8-27B", section "How it gets its speed"; page "Tesla P100 (sm_60)
+ * llama.cpp patches for Qwen3.5/3.6-35B-A3B: ~2x decode and prompt
+ * processing over the shinbunbun baseline", sections "MTP draft vocabulary
+ * (patch 17)" and "The draft vocabulary file": up to 4096 sequence tokens).
+ * Added tokens keep their order of first appearance; once `cap` were added
+ * the list stays as it is; tokens outside [0, V) are ignored.
+ *   The list lives in a caller-owned device workspace of
+ *   draft_list_bytes(V, n_static, cap) bytes (16-byte aligned; 0 means
+ *   invalid sizes: V < 1, n_static < 1, cap < 0, or more than 2^28 entries).
+ *   draft_list_ids(ws, V) is the device address of its id array, always
+ *   n_static + cap entries: the static ids, the added tokens, then copies
+ *   of the first static id in the unused slots (a repeated candidate ties
+ *   with itself and changes no argmax).  It is a ready vocab_map for
+ *   lmhead_argmax / lmhead_verify with n_map = n_static + cap; the greedy
+ *   draft step is lmhead_argmax over it with T = 1.
+ *   draft_list_init: static_ids [n_static] int32 device (ids outside [0, V)
+ *   are copied but not marked; the head skips them and reports
+ *   SV_DEVERR_BAD_MAP_ID); clears the list's membership bitmap and writes
+ *   the header and ids.  draft_list_add: tokens [n_tokens] int32 device;
+ *   one kernel of one warp, 32 tokens per round.  Both are asynchronous on
+ *   `stream`; calls on one workspace must be stream-ordered.
+ *   draft_list_count: *out (host) = number of added tokens; synchronous.
+ *   Errors: SV_ERR_NULL, SV_ERR_SHAPE, SV_ERR_ALIGN, SV_ERR_CUDA.
+ */
+size_t draft_list_bytes(int V, int n_static, int cap);
+int32_t *draft_list_ids(void *ws, int V);
+int draft_list_init(void *ws, const int32_t *static_ids, int n_static, int V, int cap, sv_stream stream);
+int draft_list_add(void *ws, const int32_t *tokens, int n_tokens, sv_stream stream);
+int draft_list_count(const void *ws, int32_t *out);
 
 /* A static, human-readable name for a status code. */
 const char *sv_status_string(int status);

@@ -59,6 +59,16 @@ def load(path: str | None = None):
     lib.lmhead_verify_noalloc.restype = ci
     lib.lmhead_argmax.argtypes = [vp, vp, vp, ci, ci, vp, ci, ci, vp, vp, vp]
     lib.lmhead_argmax.restype = ci
+    lib.draft_list_bytes.argtypes = [ci, ci, ci]
+    lib.draft_list_bytes.restype = ctypes.c_size_t
+    lib.draft_list_ids.argtypes = [vp, ci]
+    lib.draft_list_ids.restype = vp
+    lib.draft_list_init.argtypes = [vp, vp, ci, ci, ci, vp]
+    lib.draft_list_init.restype = ci
+    lib.draft_list_add.argtypes = [vp, vp, ci, vp]
+    lib.draft_list_add.restype = ci
+    lib.draft_list_count.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
+    lib.draft_list_count.restype = ci
     lib.sv_status_string.argtypes = [ci]
     lib.sv_status_string.restype = ctypes.c_char_p
     lib.sv_last_device_error.argtypes = [ctypes.POINTER(ctypes.c_int32)]
@@ -254,6 +264,36 @@ def lmhead_argmax(x, Wq, scales, vocab_map=None, ids=None, vals=None, stream=Non
         _ptr(x), _ptr(Wq), _ptr(scales), K, T, _ptr(vocab_map), n_map, V, _ptr(ids), _ptr(vals),
         _stream(stream)))
     return ids, vals
+
+
+class DraftList:
+    """A dynamic draft list in a device workspace (see draft_list_* in
+    include/specverify.h).  ``ids`` is the n_static + cap entry int32 view
+    to pass as vocab_map."""
+
+    def __init__(self, static_ids, V, cap, stream=None):
+        torch = _torch()
+        _i32(static_ids, "static_ids")
+        self.V, self.n_static, self.cap = int(V), static_ids.numel(), int(cap)
+        nbytes = load().draft_list_bytes(self.V, self.n_static, self.cap)
+        if nbytes == 0:
+            raise ValueError("invalid draft list sizes")
+        self.ws = torch.empty(nbytes, dtype=torch.uint8, device=static_ids.device)
+        _check("draft_list_init", load().draft_list_init(_ptr(self.ws), _ptr(static_ids), self.n_static,
+                                                         self.V, self.cap, _stream(stream)))
+        off = load().draft_list_ids(_ptr(self.ws), self.V) - self.ws.data_ptr()
+        self.ids = self.ws[off:off + 4 * (self.n_static + self.cap)].view(torch.int32)
+
+    def add(self, tokens, stream=None):
+        if tokens.numel():
+            _i32(tokens, "tokens")
+        _check("draft_list_add", load().draft_list_add(_ptr(self.ws), _ptr(tokens) if tokens.numel() else None,
+                                                       tokens.numel(), _stream(stream)))
+
+    def count(self) -> int:
+        out = ctypes.c_int32(0)
+        _check("draft_list_count", load().draft_list_count(_ptr(self.ws), ctypes.byref(out)))
+        return int(out.value)
 
 
 def last_device_error() -> int:

@@ -10,6 +10,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "draft_list.cuh"
 #include "specverify.h"
 #include "w4a16_stream.cuh"
 
@@ -553,6 +554,65 @@ int sv_last_device_error(int32_t *out)
     if (cudaMemset(st->err, 0, sizeof v) != cudaSuccess) return SV_ERR_CUDA;
     if (cudaDeviceSynchronize() != cudaSuccess) return SV_ERR_CUDA;
     *out = v;
+    return SV_OK;
+}
+
+// ----------------------------------------------------------------------------
+// Dynamic draft list (draft_list.cuh)
+
+size_t draft_list_bytes(int V, int n_static, int cap)
+{
+    if (V < 1 || n_static < 1 || cap < 0 || static_cast<long long>(n_static) + cap > (1LL << 28)) return 0;
+    return sv::draft_list_ids_offset(V) + 4 * (static_cast<size_t>(n_static) + cap);
+}
+
+int32_t *draft_list_ids(void *ws, int V)
+{
+    if (!ws || V < 1) return nullptr;
+    return reinterpret_cast<int32_t *>(static_cast<uint8_t *>(ws) + sv::draft_list_ids_offset(V));
+}
+
+int draft_list_init(void *ws, const int32_t *static_ids, int n_static, int V, int cap, sv_stream stream)
+{
+    using namespace sv;
+    if (!ws || !static_ids) return SV_ERR_NULL;
+    if (draft_list_bytes(V, n_static, cap) == 0) return SV_ERR_SHAPE;
+    if (!aligned16(ws) || !aligned4(static_ids)) return SV_ERR_ALIGN;
+    const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t *base = static_cast<uint8_t *>(ws);
+    if (cudaMemsetAsync(base + sizeof(DraftListHeader), 0, 4 * draft_list_bitmap_words(V), cs) != cudaSuccess) {
+        cudaGetLastError();
+        return SV_ERR_CUDA;
+    }
+    const int n = n_static + cap;
+    draft_list_init_kernel<<<(n + 255) / 256, 256, 0, cs>>>(base, static_ids, n_static, V, cap);
+    if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+    return SV_OK;
+}
+
+int draft_list_add(void *ws, const int32_t *tokens, int n_tokens, sv_stream stream)
+{
+    using namespace sv;
+    if (!ws) return SV_ERR_NULL;
+    if (n_tokens < 0) return SV_ERR_SHAPE;
+    if (n_tokens == 0) return SV_OK;
+    if (!tokens) return SV_ERR_NULL;
+    if (!aligned16(ws) || !aligned4(tokens)) return SV_ERR_ALIGN;
+    draft_list_add_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(static_cast<uint8_t *>(ws), tokens,
+                                                                                n_tokens);
+    if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+    return SV_OK;
+}
+
+int draft_list_count(const void *ws, int32_t *out)
+{
+    using namespace sv;
+    if (!ws || !out) return SV_ERR_NULL;
+    const auto *h = static_cast<const DraftListHeader *>(ws);
+    if (cudaMemcpy(out, &h->count, sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return SV_ERR_CUDA;
+    }
     return SV_OK;
 }
 

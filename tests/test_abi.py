@@ -39,7 +39,7 @@ def test_status_strings(lib):
 
 
 def test_binding_has_same_names_as_abi():
-    for name in ("w4a16_gemm", "lmhead_verify", "lmhead_verify_batched", "lmhead_argmax"):
+    for name in ("w4a16_gemm", "lmhead_verify", "lmhead_verify_batched", "lmhead_argmax", "DraftList"):
         assert callable(getattr(sv, name))
 
 
@@ -109,3 +109,33 @@ def test_argmax_rejects_bad_arguments(lib):
 
 def test_last_device_error_rejects_null(lib):
     assert lib.sv_last_device_error(None) == -1
+
+
+def test_draft_list_sizes_and_ids_address(lib):
+    """Workspace size = 32-byte header + membership bitmap (V bits, padded
+    to 16 bytes) + 4 bytes per list entry; the id array follows the bitmap."""
+    assert lib.draft_list_bytes(0, 1, 1) == 0
+    assert lib.draft_list_bytes(100, 0, 1) == 0
+    assert lib.draft_list_bytes(100, 1, -1) == 0
+    V = 248320
+    words = (V + 31) // 32                       # 7760, already a multiple of 4
+    assert lib.draft_list_bytes(V, 32768, 4096) == 32 + 4 * words + 4 * (32768 + 4096)
+    assert lib.draft_list_bytes(33, 1, 0) == 32 + 16 + 4
+    assert lib.draft_list_ids(ctypes.c_void_p(0x10000), V) == 0x10000 + 32 + 4 * words
+    assert lib.draft_list_ids(None, V) is None
+
+
+@nogpu
+def test_draft_list_rejects_bad_arguments(lib):
+    assert lib.draft_list_init(NUL, A, 4, 100, 8, None) == -1
+    assert lib.draft_list_init(A, NUL, 4, 100, 8, None) == -1
+    assert lib.draft_list_init(A, A2, 0, 100, 8, None) == -2
+    assert lib.draft_list_init(A, A2, 4, 0, 8, None) == -2
+    assert lib.draft_list_init(MIS, A2, 4, 100, 8, None) == -3
+    assert lib.draft_list_init(A, ctypes.c_void_p(0x20002), 4, 100, 8, None) == -3
+    assert lib.draft_list_add(NUL, A2, 4, None) == -1
+    assert lib.draft_list_add(A, NUL, 4, None) == -1
+    assert lib.draft_list_add(A, A2, -1, None) == -2
+    assert lib.draft_list_add(A, A2, 0, None) == 0          # nothing to add: no launch
+    assert lib.draft_list_add(MIS, A2, 4, None) == -3
+    assert lib.draft_list_count(NUL, None) == -1
