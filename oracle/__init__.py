@@ -68,6 +68,9 @@ def _load():
     lib.or_lmhead_logits.restype = c_int
     lib.or_lmhead_logits.argtypes = [_u16p, _u32p, _u16p, c_int, c_int, ctypes.c_void_p,
                                      c_int, c_int, ctypes.c_void_p, ctypes.c_void_p]
+    lib.or_bf16_logits.restype = c_int
+    lib.or_bf16_logits.argtypes = [_u16p, _u16p, c_int, c_int, ctypes.c_void_p, c_int, c_int,
+                                   ctypes.c_void_p]
     lib.or_argmax.restype = c_int
     lib.or_argmax.argtypes = [_f32p, c_int, c_int, ctypes.c_void_p, _i32p,
                               ctypes.c_void_p, ctypes.c_void_p]
@@ -159,6 +162,72 @@ def verify(a, drafts):
     if rc != 0:
         raise ValueError("oracle verify rejected its arguments")
     return int(acc.value), int(nxt.value)
+
+
+def bf16_logits(x, Wbf, K, T, V, rows=None):
+    """fp32 logits [T][n_rows] of bf16 weight rows (Wbf [V][K] bf16 bits):
+    exact products summed in ascending k."""
+    lib = _load()
+    x = _c(x, np.uint16).reshape(-1)
+    Wbf = _c(Wbf, np.uint16).reshape(-1)
+    rows_a = None if rows is None else _c(rows, np.int32)
+    n_rows = V if rows is None else int(rows_a.size)
+    out = np.empty((T, n_rows), np.float32)
+    rc = lib.or_bf16_logits(x, Wbf, K, T, _ptr(rows_a), n_rows, V, _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle bf16_logits rejected its arguments")
+    return out
+
+
+def topk(logits, k, ids=None):
+    """Per row the k candidates of largest logit, ties to the lowest token
+    id, ordered best first.  Returns token ids [T][k] and values [T][k]."""
+    logits = np.asarray(logits, np.float32)
+    T, n = logits.shape
+    ids_a = np.arange(n, dtype=np.int64) if ids is None else np.asarray(ids, np.int64)
+    out_ids = np.empty((T, k), np.int32)
+    out_val = np.empty((T, k), np.float32)
+    for t in range(T):
+        order = np.lexsort((ids_a, -logits[t].astype(np.float64)))[:k]
+        out_ids[t] = ids_a[order]
+        out_val[t] = logits[t][order]
+    return out_ids, out_val
+
+
+@dataclass
+class RescoredResult:
+    accept_len: np.ndarray   # [n_streams] int32
+    next_token: np.ndarray   # [n_streams] int32
+    a: np.ndarray            # [T] rescored argmax token id per row
+    cand: np.ndarray         # [T][k] int4 candidates, best first
+    cand_gap: np.ndarray     # [T] k-th minus (k+1)-th int4 logit (inf when k = V)
+    bf16: np.ndarray         # [T][k] bf16 logits of the candidates
+    margin: np.ndarray       # [T] best - runner-up bf16 logit among the candidates
+
+
+def lmhead_verify_rescored(x, Wq, scales, Wbf, K, V, drafts, k):
+    """Greedy verify with the int4 head's top-k candidates rescored by the
+    bf16 head: int4 fp32 logits -> top k per row (ties to the lowest id) ->
+    bf16 fp32 logits of those candidates -> argmax among them (ties to the
+    lowest id) -> first mismatch with the drafts."""
+    drafts = np.asarray(drafts, np.int32).reshape(-1)
+    T = drafts.size + 1
+    l4 = lmhead_logits(x, Wq, scales, K, T, V)
+    cand, cval = topk(l4, k)
+    gap = np.full(T, np.inf)
+    if k < V:
+        _, cval1 = topk(l4, k + 1)
+        gap = cval1[:, k - 1].astype(np.float64) - cval1[:, k].astype(np.float64)
+    b16 = np.empty((T, k), np.float32)
+    a = np.empty(T, np.int32)
+    margin = np.empty(T)
+    for t in range(T):
+        b16[t] = bf16_logits(x[t:t + 1], Wbf, K, 1, V, rows=cand[t])[0]
+        at, best, second = argmax(b16[t:t + 1], ids=cand[t])
+        a[t] = at[0]
+        margin[t] = float(best[0]) - float(second[0])
+    acc, nxt = verify(a, drafts)
+    return RescoredResult(np.array([acc], np.int32), np.array([nxt], np.int32), a, cand, gap, b16, margin)
 
 
 @dataclass

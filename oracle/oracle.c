@@ -211,6 +211,42 @@ int or_lmhead_logits(const uint16_t *x, const uint32_t *Wq, const uint16_t *scal
 }
 
 /*
+ * bf16 lm_head logits over a row list: logits[t][j] = sum_k
+ * float(Wbf[rows[j]][k]) * float(x[t][k]), each product exact in fp32 (two
+ * 8-bit significands), summed in fp32 in ascending k.  The head the
+ * quantized lm_head's candidates are rescored with (page "qwen-warp and
+ * llamAmpere: two RTX 3090 engines for Qwen3.8, and what each one calls the
+ * same answer", section "What each one calls the same answer"; table "What
+ * one cycle reads from VRAM": 16 to 64 candidates).  rows == NULL means
+ * rows[j] = j.
+ */
+int or_bf16_logits(const uint16_t *x, const uint16_t *Wbf, int K, int T, const int32_t *rows,
+                   int n_rows, int V, float *logits32)
+{
+    if (!x || !Wbf || !logits32 || T < 1 || K < 1 || n_rows < 1 || V < 1)
+        return OR_EINVAL;
+    if (!rows && n_rows > V)
+        return OR_EINVAL;
+    for (int j = 0; rows && j < n_rows; ++j)
+        if (rows[j] < 0 || rows[j] >= V)
+            return OR_EINVAL;
+#pragma omp parallel for schedule(static)
+    for (int j = 0; j < n_rows; ++j) {
+        size_t v = rows ? (size_t)rows[j] : (size_t)j;
+        const uint16_t *w = Wbf + v * (size_t)K;
+        for (int t = 0; t < T; ++t) {
+            float acc = 0.0f;
+            for (int k = 0; k < K; ++k) {
+                float p = bf16_to_float(w[k]) * bf16_to_float(x[(size_t)t * K + k]);   /* exact */
+                acc = acc + p;
+            }
+            logits32[(size_t)t * n_rows + j] = acc;
+        }
+    }
+    return OR_OK;
+}
+
+/*
  * Row-wise argmax of logits[T][n] with the lowest token id winning ties.
  * ids[j] is the token id of column j (NULL: ids[j] = j).  Also returns the
  * best value, the runner-up value over the other columns (-INFINITY when

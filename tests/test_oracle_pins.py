@@ -412,3 +412,97 @@ def test_draft_list_matches_first_occurrence_definition(oracle):
         assert ids[:static.size].tolist() == static.tolist()
         assert ids[static.size:static.size + expect.size].tolist() == expect.tolist()
         assert np.all(ids[static.size + expect.size:] == static[0])
+
+
+# --------------------------------------------------------------------------
+# top-k candidates rescored by the bf16 head
+
+
+def _bf16(a):
+    return gen.f32_to_bf16_bits(np.asarray(a, np.float32))
+
+
+def test_bf16_logits_one_hot_reads_the_weight(oracle):
+    rng = np.random.default_rng(40)
+    V, K = 50, 64
+    Wbf = _bf16(rng.standard_normal((V, K)))
+    for k in (0, 17, 63):
+        x = np.zeros((1, K), np.uint16)
+        x[0, k] = _bf16(1.0)
+        lg = oracle.bf16_logits(x, Wbf, K, 1, V)
+        assert np.array_equal(lg[0], gen.bf16_bits_to_f32(Wbf[:, k]))
+
+
+def test_bf16_logits_within_fp32_bound_of_fp64_matmul(oracle):
+    rng = np.random.default_rng(41)
+    V, K, T = 64, 1000, 3
+    Wbf = _bf16(rng.standard_normal((V, K)))
+    x = _bf16(rng.standard_normal((T, K)))
+    lg = oracle.bf16_logits(x, Wbf, K, T, V).astype(np.float64)
+    w = gen.bf16_bits_to_f32(Wbf).astype(np.float64)
+    xv = gen.bf16_bits_to_f32(x).astype(np.float64)
+    ref = xv @ w.T
+    bound = K * 2.0 ** -24 * (np.abs(xv) @ np.abs(w).T)
+    assert np.all(np.abs(lg - ref) <= bound)
+
+
+def test_topk_orders_by_value_then_lowest_id(oracle):
+    lg = np.array([[1.0, 3.0, 2.0, 3.0, 0.5, 2.0]], np.float32)
+    ids, vals = oracle.topk(lg, 4)
+    assert ids[0].tolist() == [1, 3, 2, 5]
+    assert vals[0].tolist() == [3.0, 3.0, 2.0, 2.0]
+    ids, _ = oracle.topk(lg, 4, ids=np.array([60, 10, 50, 20, 30, 40]))
+    assert ids[0].tolist() == [10, 20, 40, 50]
+
+
+def test_rescoring_with_every_candidate_is_the_bf16_argmax(oracle):
+    rng = np.random.default_rng(42)
+    V, K = 200, 256
+    Wq, sc = gen.weights(rng, V, K)
+    Wbf = _bf16(rng.standard_normal((V, K)) * 0.05)
+    x = gen.activations(rng, 3, K)
+    r = oracle.lmhead_verify_rescored(x, Wq, sc, Wbf, K, V, [0, 0], V)
+    full = gen.bf16_bits_to_f32(x).astype(np.float64) @ gen.bf16_bits_to_f32(Wbf).astype(np.float64).T
+    for t in range(3):
+        s = np.sort(full[t])
+        if s[-1] - s[-2] > 1e-3:
+            assert r.a[t] == int(np.argmax(full[t]))
+
+
+def test_rescoring_planted_flip(oracle):
+    """Row 5 wins the int4 head by a wide margin, row 9 is second; the bf16
+    head gives row 9 the larger logit.  One candidate keeps 5, two or more
+    return 9."""
+    V, K = 16, 128
+    Wq = np.full((V, K // 8), 0x88888888, np.uint32)          # level 0 everywhere
+    Wq[5] = 0xFFFFFFFF                                        # level +7
+    Wq[9] = 0xEEEEEEEE                                        # level +6
+    sc = np.full((V, 1), _bf16(1.0), np.uint16)
+    Wbf = np.zeros((V, K), np.uint16)
+    Wbf[5] = _bf16(1.0)
+    Wbf[9] = _bf16(2.0)
+    x = np.full((1, K), _bf16(1.0), np.uint16)
+    assert oracle.lmhead_verify_rescored(x, Wq, sc, Wbf, K, V, [], 1).a.tolist() == [5]
+    for k in (2, 3, 16):
+        r = oracle.lmhead_verify_rescored(x, Wq, sc, Wbf, K, V, [], k)
+        assert r.a.tolist() == [9]
+        assert r.cand[0][:2].tolist() == [5, 9]
+
+
+def test_rescoring_agrees_with_int4_when_heads_hold_the_same_weights(oracle):
+    """bf16 weights equal to the int4 levels times a power-of-two scale hold
+    the same numbers as the int4 head, so the rescored argmax is the int4
+    argmax wherever the margin is clear of fp32 reordering."""
+    rng = np.random.default_rng(43)
+    V, K = 300, 512
+    Wq, _ = gen.weights(rng, V, K)
+    sc = np.full((V, K // 128), _bf16(2.0 ** -6), np.uint16)
+    lv = ((Wq[:, :, None] >> (4 * np.arange(8))) & 0xF).astype(np.int64).reshape(V, K) - 8
+    Wbf = _bf16(lv * 2.0 ** -6)
+    x = gen.activations(rng, 4, K)
+    r = oracle.lmhead_verify_rescored(x, Wq, sc, Wbf, K, V, [0, 0, 0], 8)
+    l4 = oracle.lmhead_logits(x, Wq, sc, K, 4, V)
+    a4, b4, s4 = oracle.argmax(l4)
+    for t in range(4):
+        if b4[t] - s4[t] > 1e-3:
+            assert r.a[t] == a4[t]
