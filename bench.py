@@ -500,10 +500,26 @@ def per_kernel_breakdown(torch, sv, device, stream, reps=50):
     # the greedy draft step over a full dynamic draft list (32,768 static ids
     # + 4,096 sequence tokens), and the list maintenance call itself
     cases.append(("draft_step", "list_32768+4096", gen.HIDDEN, gen.VOCAB, 1))
+    # the verify whose ids are the bf16 head's: top-k of the int4 head rescored
+    for k in (16, 64):
+        cases.append(("head_rescored", "top%d" % k, gen.HIDDEN, gen.VOCAB, (4, k)))
     cases.append(("draft_list_add", "32_tokens", 0, gen.VOCAB, 32))
     cases.append(("draft_list_add", "4096_tokens", 0, gen.VOCAB, 4096))
     for kind, label, K, N, T in cases:
-        if kind in ("draft_step", "draft_list_add"):
+        if kind == "head_rescored":
+            Tt, k = T
+            Wq, sc = gen.weights(rng, N, K)
+            Ws = [(dev(Wq, np.int32), dev(sc, np.int16)) for _ in range(2)]
+            copies = 2
+            Wbf = (torch.randn((N, K), dtype=torch.float32, device=device) * 0.02).to(torch.bfloat16)
+            x = dev(gen.activations(rng, Tt, K), np.int16)
+            drafts = torch.zeros(Tt - 1, dtype=torch.int32, device=device)
+            fn = lambda i: sv.lmhead_verify_rescored(x, Ws[i % copies][0], Ws[i % copies][1], Wbf, drafts,
+                                                     top_k=k)
+            # int4 head read once, plus the bf16 rows of the candidates
+            nbytes = gen.lmhead_bytes(N, K, Tt, n_streams=1, n_draft=Tt - 1) + Tt * k * K * 2
+            T = Tt
+        elif kind in ("draft_step", "draft_list_add"):
             ids = rng.permutation(N).astype(np.int32)
             static = dev(ids[:32768], np.int32)
             dl = sv.DraftList(static, N, 4096)

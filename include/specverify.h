@@ -173,6 +173,43 @@ int lmhead_verify_noalloc(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *s
                           int32_t *accept_len, int32_t *next_token, sv_stream stream);
 
 /*
+ * lmhead_verify_rescored / lmhead_argmax_rescored -- the greedy verify (or
+ * the per-row argmax) with the ids of the bf16 head: the int4 lm_head pass
+ * gives every verify row its top_k candidates by fp32 int4 logit (ties to
+ * the lowest id), the bf16 head rescores just those rows, and the argmax is
+ * taken among them (page "qwen-warp and llamAmpere: two RTX 3090 engines
+ * for Qwen3.8, and what each one calls the same answer", section "What each
+ * one calls the same answer": the rescoring head reads the quantized
+ * lm_head's top candidates and rescores them with the bf16 head; table
+ * "What one cycle reads from VRAM": 16 to 64 candidates).
+ *   logit_bf16[t][c] = sum_k float(Wbf[c][k]) * float(x[t][k]) in fp32
+ *   (products exact, summed in a fixed tree order); a[t] = argmax over the
+ *   candidates, lowest id on ties; accept_len / next_token as in
+ *   lmhead_verify.  ids / vals (argmax variant): a[t] and its bf16 logit.
+ *   x [T][K] (T = 1 + n_draft for the verify, T <= 8); Wq [V][K/8] and
+ *   scales [V][K/128] the int4 head; Wbf [V][K] bf16 the bf16 head
+ *   (16-byte aligned); 1 <= top_k <= min(64, V).  No vocab_map.
+ *   Launches three kernels on `stream`: the int4 head writing fp32 logits
+ *   to a per-device buffer, a pass taking the largest logit of every
+ *   128-row slice of V, and ceil(top_k / 16) blocks per verify row that
+ *   select the row's top_k (threshold: the top_k-th largest slice maximum),
+ *   rescore them and, in the last block, verify.  The first call on a
+ *   device, or the first with a larger V, allocates that buffer (about
+ *   32 * V bytes) after synchronising `stream`: make it outside stream
+ *   capture.
+ *   Errors: SV_ERR_NULL, SV_ERR_SHAPE (T outside 1..8, K as for
+ *   w4a16_gemm and at most 65536, V < 1, top_k out of range),
+ *   SV_ERR_ALIGN, SV_ERR_CUDA, SV_ERR_NOMEM.
+ */
+int lmhead_verify_rescored(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales,
+                           const sv_bf16 *Wbf, int K, const int32_t *drafts, int n_draft,
+                           int top_k, int V, int32_t *accept_len, int32_t *next_token,
+                           sv_stream stream);
+int lmhead_argmax_rescored(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales,
+                           const sv_bf16 *Wbf, int K, int T, int top_k, int V,
+                           int32_t *ids, float *vals, sv_stream stream);
+
+/*
  * Dynamic draft list -- the candidate list of the restricted draft head: a
  * static list of token ids (the most frequent tokens) plus the tokens of the
  * current sequence that are missing from it, added as the sequence grows,

@@ -59,6 +59,10 @@ def load(path: str | None = None):
     lib.lmhead_verify_noalloc.restype = ci
     lib.lmhead_argmax.argtypes = [vp, vp, vp, ci, ci, vp, ci, ci, vp, vp, vp]
     lib.lmhead_argmax.restype = ci
+    lib.lmhead_verify_rescored.argtypes = [vp, vp, vp, vp, ci, vp, ci, ci, ci, vp, vp, vp]
+    lib.lmhead_verify_rescored.restype = ci
+    lib.lmhead_argmax_rescored.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, vp, vp, vp]
+    lib.lmhead_argmax_rescored.restype = ci
     lib.draft_list_bytes.argtypes = [ci, ci, ci]
     lib.draft_list_bytes.restype = ctypes.c_size_t
     lib.draft_list_ids.argtypes = [vp, ci]
@@ -263,6 +267,48 @@ def lmhead_argmax(x, Wq, scales, vocab_map=None, ids=None, vals=None, stream=Non
     _check("lmhead_argmax", load().lmhead_argmax(
         _ptr(x), _ptr(Wq), _ptr(scales), K, T, _ptr(vocab_map), n_map, V, _ptr(ids), _ptr(vals),
         _stream(stream)))
+    return ids, vals
+
+
+def lmhead_verify_rescored(x, Wq, scales, Wbf, drafts, top_k=16, accept_len=None, next_token=None,
+                           stream=None):
+    """Greedy verify whose ids are the bf16 head's: the int4 head's top_k
+    candidates of every row rescored with Wbf [V][K] bf16."""
+    torch = _torch()
+    _bits16(x, "x"), _words(Wq, "Wq"), _bits16(scales, "scales"), _bits16(Wbf, "Wbf")
+    T, K = x.shape
+    V = Wq.shape[0]
+    n_draft = drafts.numel()
+    if T != n_draft + 1:
+        raise ValueError("x must have 1 + n_draft rows")
+    if tuple(Wbf.shape) != (V, K):
+        raise ValueError("Wbf must be [V][K]")
+    if n_draft:
+        _i32(drafts, "drafts")
+    if accept_len is None:
+        accept_len = torch.empty(1, dtype=torch.int32, device=x.device)
+    if next_token is None:
+        next_token = torch.empty(1, dtype=torch.int32, device=x.device)
+    _check("lmhead_verify_rescored", load().lmhead_verify_rescored(
+        _ptr(x), _ptr(Wq), _ptr(scales), _ptr(Wbf), K, _ptr(drafts) if n_draft else None, n_draft, int(top_k),
+        V, _ptr(accept_len), _ptr(next_token), _stream(stream)))
+    return accept_len, next_token
+
+
+def lmhead_argmax_rescored(x, Wq, scales, Wbf, top_k=16, ids=None, vals=None, stream=None):
+    """Per-row argmax among the int4 head's top_k candidates by bf16 logit."""
+    torch = _torch()
+    _bits16(x, "x"), _words(Wq, "Wq"), _bits16(scales, "scales"), _bits16(Wbf, "Wbf")
+    T, K = x.shape
+    V = Wq.shape[0]
+    if tuple(Wbf.shape) != (V, K):
+        raise ValueError("Wbf must be [V][K]")
+    if ids is None:
+        ids = torch.empty(T, dtype=torch.int32, device=x.device)
+    if vals is None:
+        vals = torch.empty(T, dtype=torch.float32, device=x.device)
+    _check("lmhead_argmax_rescored", load().lmhead_argmax_rescored(
+        _ptr(x), _ptr(Wq), _ptr(scales), _ptr(Wbf), K, T, int(top_k), V, _ptr(ids), _ptr(vals), _stream(stream)))
     return ids, vals
 
 

@@ -11,6 +11,7 @@
 #include <mutex>
 
 #include "draft_list.cuh"
+#include "rescore.cuh"
 #include "specverify.h"
 #include "w4a16_stream.cuh"
 
@@ -18,6 +19,10 @@ namespace sv {
 namespace {
 
 constexpr int MAX_DEVICES = 64;
+
+// Room left for rescore_kernel's static shared memory under the opt-in limit.
+constexpr int RS_STATIC_SMEM_SLACK = 10240;
+constexpr size_t RS_SCRATCH_BYTES = static_cast<size_t>(RS_TMAX) * RS_KMAX * 8 + 256;
 
 struct DeviceState {
     bool ready = false;
@@ -31,6 +36,13 @@ struct DeviceState {
     uint8_t *x16 = nullptr;     // streamed activations, X16_MAX_GROUPS x TMAX x XSTR bytes
     float *xinv = nullptr;      // [TMAX]
     int x16_max_groups = 0;
+    // rescoring (rescore.cuh); the logits and candidate buffers grow on demand
+    float *cand_lg = nullptr;             // [RS_TMAX][RS_KMAX] rescored logits
+    int32_t *cand_id = nullptr;           // [RS_TMAX][RS_KMAX] their ids
+    unsigned *rdone = nullptr;            // CTA counter, left at 0
+    float *rs_logits = nullptr;           // [RS_TMAX][rs_v_cap]
+    unsigned long long *rs_smax = nullptr;   // [RS_TMAX][rs_s_cap] slice maxima
+    long long rs_v_cap = 0, rs_s_cap = 0;
 };
 
 // Activations of calls with more than one token tile (T > 8) are converted
@@ -97,7 +109,7 @@ int device_state(DeviceState **out)
         const size_t keys_bytes = TMAX * sizeof(unsigned long long);
         const size_t x16_bytes = static_cast<size_t>(X16_MAX_GROUPS) * TMAX * XSTR;
         const size_t total = part_bytes + ctr_bytes + keys_bytes + 2 * sizeof(unsigned) + 256 + x16_bytes +
-                             TMAX * sizeof(float) + 256;
+                             TMAX * sizeof(float) + 256 + RS_SCRATCH_BYTES;
         uint8_t *base = nullptr;
         if (cudaMalloc(&base, total) != cudaSuccess) {
             cudaGetLastError();
@@ -123,6 +135,11 @@ int device_state(DeviceState **out)
         st.x16 = base + off;
         off += x16_bytes;
         st.xinv = reinterpret_cast<float *>(base + off);
+        off += TMAX * sizeof(float);
+        off = (off + 255) & ~static_cast<size_t>(255);
+        st.cand_lg = reinterpret_cast<float *>(base + off);
+        st.cand_id = reinterpret_cast<int32_t *>(base + off + RS_TMAX * RS_KMAX * sizeof(float));
+        st.rdone = reinterpret_cast<unsigned *>(base + off + RS_TMAX * RS_KMAX * 8);
         st.x16_max_groups = X16_MAX_GROUPS;
         cudaError_t e = cudaSuccess;
         e = e != cudaSuccess ? e : raise_smem_limit<1, false, false, false>(optin);
@@ -137,6 +154,9 @@ int device_state(DeviceState **out)
         e = e != cudaSuccess ? e : raise_smem_limit<1, true, true, true>(optin);
         e = e != cudaSuccess ? e : raise_smem_limit<2, true, true, false>(optin);
         e = e != cudaSuccess ? e : raise_smem_limit<4, true, true, false>(optin);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(rescore_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     optin - RS_STATIC_SMEM_SLACK);
         if (e != cudaSuccess || tensor_map_fn() != SV_OK) {
             cudaFree(base);
             return SV_ERR_CUDA;
@@ -338,6 +358,120 @@ int head_call(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, int K
     p.ids = ids;
     p.vals = vals;
     return vocab_map ? dispatch<true, true>(p, *st, stream) : dispatch<true, false>(p, *st, stream);
+}
+
+// ----------------------------------------------------------------------------
+// Top-k candidates of the int4 head rescored by the bf16 head (rescore.cuh):
+// pass 1 is the head kernel as a GEMM with fp32 outputs, pass 2
+// slicemax_kernel, pass 3 rescore_kernel.
+
+int rescored_call(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, const sv_bf16 *Wbf, int K, int T,
+                  int top_k, int V, int mode, const int32_t *drafts, int n_draft, int32_t *accept_len,
+                  int32_t *next_token, int32_t *ids, float *vals, cudaStream_t stream)
+{
+    int rc = check_common(x, Wq, scales, T, K);
+    if (rc != SV_OK) return rc;
+    if (!Wbf) return SV_ERR_NULL;
+    if (!aligned16(Wbf)) return SV_ERR_ALIGN;
+    if (T > RS_TMAX || V < 1 || top_k < 1 || top_k > RS_KMAX || top_k > V) return SV_ERR_SHAPE;
+    if (mode == 0) {
+        if (!accept_len || !next_token) return SV_ERR_NULL;
+        if (n_draft > 0 && !drafts) return SV_ERR_NULL;
+        if ((drafts && !aligned4(drafts)) || !aligned4(accept_len) || !aligned4(next_token)) return SV_ERR_ALIGN;
+    } else {
+        if (!ids) return SV_ERR_NULL;
+        if (!aligned4(ids) || (vals && !aligned4(vals))) return SV_ERR_ALIGN;
+    }
+    DeviceState *st = nullptr;
+    rc = device_state(&st);
+    if (rc != SV_OK) return rc;
+    // slices of RS_SLICE rows of V
+    const long long nS = (static_cast<long long>(V) + RS_SLICE - 1) / RS_SLICE;
+    const long long limit = st->smem_optin - RS_STATIC_SMEM_SLACK;
+    if (K > 65536 || RS_SEL_MAX * 8LL + 2LL * K > limit) return SV_ERR_SHAPE;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (V > st->rs_v_cap || nS > st->rs_s_cap) {
+            // first call with a larger head on this device: (re)allocate
+            if (cudaStreamSynchronize(stream) != cudaSuccess) return SV_ERR_CUDA;
+            cudaFree(st->rs_logits);
+            cudaFree(st->rs_smax);
+            st->rs_logits = nullptr;
+            st->rs_smax = nullptr;
+            st->rs_v_cap = st->rs_s_cap = 0;
+            if (cudaMalloc(&st->rs_logits, static_cast<size_t>(RS_TMAX) * V * sizeof(float)) != cudaSuccess ||
+                cudaMalloc(&st->rs_smax, static_cast<size_t>(nS) * RS_TMAX * 8) != cudaSuccess) {
+                cudaGetLastError();
+                return SV_ERR_NOMEM;
+            }
+            st->rs_v_cap = V;
+            st->rs_s_cap = nS;
+        }
+    }
+    // pass 1: the int4 head's fp32 logits [T][V]
+    Params p{};
+    p.x = x;
+    p.Wq = Wq;
+    p.scales = scales;
+    p.T = T;
+    p.K = K;
+    p.G = K / 128;
+    p.n_rows = V;
+    p.V = V;
+    const long long tiles = (static_cast<long long>(V) + ROWS - 1) / ROWS;
+    p.U = tiles * p.G;
+    p.y32 = st->rs_logits;
+    rc = dispatch<false, false>(p, *st, stream);
+    if (rc != SV_OK) return rc;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.blockDim = dim3(RS_THREADS);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // pass 2: every slice's largest key per row
+    SliceMaxParams mp{};
+    mp.logits = st->rs_logits;
+    mp.T = T;
+    mp.V = V;
+    mp.nS = static_cast<int>(nS);
+    mp.smax = st->rs_smax;
+    cfg.gridDim = dim3(static_cast<unsigned>((nS + RS_WARPS - 1) / RS_WARPS));
+    cfg.dynamicSmemBytes = 0;
+    if (cudaLaunchKernelEx(&cfg, slicemax_kernel, mp) != cudaSuccess) {
+        cudaGetLastError();
+        return SV_ERR_CUDA;
+    }
+    // pass 3: threshold, gather, rescore with the bf16 head, argmax, verify
+    RescoreParams rp{};
+    rp.x = x;
+    rp.Wbf = Wbf;
+    rp.logits = st->rs_logits;
+    rp.smax = st->rs_smax;
+    rp.nS = static_cast<int>(nS);
+    rp.T = T;
+    rp.K = K;
+    rp.V = V;
+    rp.k = top_k;
+    rp.mode = mode;
+    rp.drafts = drafts;
+    rp.accept_len = accept_len;
+    rp.next_token = next_token;
+    rp.ids = ids;
+    rp.vals = vals;
+    rp.cand_lg = st->cand_lg;
+    rp.cand_id = st->cand_id;
+    rp.done = st->rdone;
+    cfg.gridDim = dim3(static_cast<unsigned>((top_k + RS_PER_CTA - 1) / RS_PER_CTA), static_cast<unsigned>(T));
+    cfg.dynamicSmemBytes = static_cast<size_t>(RS_SEL_MAX) * 8 + 2 * static_cast<size_t>(K);
+    if (cudaLaunchKernelEx(&cfg, rescore_kernel, rp) != cudaSuccess) {
+        cudaGetLastError();
+        return SV_ERR_CUDA;
+    }
+    return SV_OK;
 }
 
 // ----------------------------------------------------------------------------
@@ -555,6 +689,22 @@ int sv_last_device_error(int32_t *out)
     if (cudaDeviceSynchronize() != cudaSuccess) return SV_ERR_CUDA;
     *out = v;
     return SV_OK;
+}
+
+int lmhead_verify_rescored(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, const sv_bf16 *Wbf, int K,
+                           const int32_t *drafts, int n_draft, int top_k, int V, int32_t *accept_len,
+                           int32_t *next_token, sv_stream stream)
+{
+    if (n_draft < 0 || n_draft > sv::RS_TMAX - 1) return SV_ERR_SHAPE;
+    return sv::rescored_call(x, Wq, scales, Wbf, K, n_draft + 1, top_k, V, 0, drafts, n_draft, accept_len,
+                             next_token, nullptr, nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int lmhead_argmax_rescored(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, const sv_bf16 *Wbf, int K,
+                           int T, int top_k, int V, int32_t *ids, float *vals, sv_stream stream)
+{
+    return sv::rescored_call(x, Wq, scales, Wbf, K, T, top_k, V, 1, nullptr, 0, nullptr, nullptr, ids, vals,
+                             reinterpret_cast<cudaStream_t>(stream));
 }
 
 // ----------------------------------------------------------------------------

@@ -390,6 +390,14 @@ __device__ __forceinline__ int32_t key_id(unsigned long long k)
     return static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(k & 0xFFFFFFFFull));
 }
 
+__device__ __forceinline__ unsigned long long shfl_u64(unsigned long long v, int src)
+{
+    uint32_t lo = static_cast<uint32_t>(v), hi = static_cast<uint32_t>(v >> 32);
+    lo = __shfl_sync(0xFFFFFFFFu, lo, src);
+    hi = __shfl_sync(0xFFFFFFFFu, hi, src);
+    return (static_cast<unsigned long long>(hi) << 32) | lo;
+}
+
 __device__ __forceinline__ unsigned long long shfl_xor_u64(unsigned long long v, int m)
 {
     uint32_t lo = static_cast<uint32_t>(v), hi = static_cast<uint32_t>(v >> 32);

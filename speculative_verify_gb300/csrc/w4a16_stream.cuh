@@ -100,7 +100,8 @@ struct Params {
     int off_bk;                 // HEAD: running best key per lane and token, [32][BK_STRIDE] u64
     int off_xzero;              // XBF: 256 zero bytes, the activation row of absent tokens
     // GEMM output
-    uint16_t *y;                // [T][N]
+    uint16_t *y;                // [T][N] bf16, or
+    float *y32;                 // [T][N] fp32 when not null (the lm_head's logits for rescoring)
     // HEAD outputs
     int mode;                   // 0: verify, 1: argmax
     const int32_t *drafts;      // [n_streams][n_draft]
@@ -484,6 +485,7 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
         unsigned long long *bk = reinterpret_cast<unsigned long long *>(smem + p.off_bk) + lane * BK_STRIDE;
         if (HEAD)
             for (int t = 0; t < T; ++t) bk[t] = 0ull;
+
         // Contributors of the only tiles that can be split, the first and
         // the last: CTAs bf .. bf+nc-1, and whether the tile is bf's first
         // tile (its partial then sits in slot 0).  Worked out once here
@@ -679,9 +681,13 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
                             const long long rg = static_cast<long long>(tile) * ROWS + lane + 32 * h;
-                            if (rg < p.n_rows)
-                                p.y[static_cast<size_t>(t) * p.n_rows + rg] =
-                                    __bfloat16_as_ushort(__float2bfloat16_rn(v[j][h]));
+                            if (rg < p.n_rows) {
+                                if (p.y32)
+                                    p.y32[static_cast<size_t>(t) * p.n_rows + rg] = v[j][h];
+                                else
+                                    p.y[static_cast<size_t>(t) * p.n_rows + rg] =
+                                        __bfloat16_as_ushort(__float2bfloat16_rn(v[j][h]));
+                            }
                         }
                     } else {
                         const unsigned long long k0 = id0 >= 0 ? make_key(v[j][0], static_cast<uint32_t>(id0)) : 0ull;
