@@ -318,3 +318,216 @@ def draft_list_add(dl: DraftList, tokens) -> DraftList:
             dl.added.append(t)
             member.add(t)
     return dl
+
+
+# ----------------------------------------------------------------------------
+# Exact speculative sampling verify over the 32 best logits of each row
+#
+# Sources: "OpenJet Engine: CUDA LLM inference for Qwen3.8-27B" -- "How it
+# gets its speed" (sampling keeps the 32 best logits of each verified row; a
+# draft is accepted with probability p(draft), a rejected one is resampled
+# from the rest of the distribution, so the sampled distribution is exact)
+# and "Limitations" (temperature, top-k <= 32, top-p and min-p, in
+# llama.cpp's order); "qwen-warp and llamAmpere: two RTX 3090 engines for
+# Qwen3.8, and what each one calls the same answer" -- "What each one calls
+# the same answer" (standard speculative sampling: accept, else draw from the
+# residual; that keeps the output distributed exactly as the target).
+#
+# Readings where the pages leave a step open:
+#  * The drafter is a point mass on its draft d, so the acceptance
+#    probability min(1, p(d) / q(d)) is p(d) and the residual
+#    norm(max(0, p - q)) is p with d removed and renormalised.
+#  * llama.cpp's order is top-k, top-p, min-p, then temperature: top-p and
+#    min-p see the temperature-1 distribution of the surviving candidates.
+#  * All arithmetic is fp32 in a fixed order (the kernel's precision): with
+#    m the best logit and d_j = l_j - m,
+#      top-p keeps the shortest prefix whose running sum of exp(d_j) reaches
+#      top_p times the sum over the candidates (all of them if rounding
+#      never reaches it);
+#      min-p keeps the prefix of candidates with exp(d_j) >= min_p (the best
+#      one always);
+#      the weights are w_j = exp(d_j / temperature), W their sum in order;
+#      accept iff u_accept * W < w_d;
+#      a sample walks the candidates best first, running sum c, and takes
+#      the first with u_sample * W' < c (W' the sum over the candidates it
+#      may take; the last of them if rounding never gets there).
+#  * temperature <= 0 is greedy: the distribution is the point mass on the
+#    best candidate.
+#  * Row i uses the uniforms u[2 i] (accept) and u[2 i + 1] (sample), each
+#    in [0, 1); they are inputs, drawn by the caller.
+
+SAMPLE_KEEP = 32
+
+
+@dataclass
+class SamplingDist:
+    ids: np.ndarray          # [n] token ids of the candidates kept, best first
+    logits: np.ndarray       # [n] their fp32 logits
+    w: np.ndarray            # [n] fp32 weights
+    W: np.float32            # their fp32 sum, in order
+    cut_margin: float        # relative distance of the top-p / min-p cuts from their thresholds
+    cut_index: list          # candidate positions next to which a cut fell
+
+
+def _f32(v):
+    return np.float32(v)
+
+
+def _sum_f32(vals):
+    s = _f32(0.0)
+    for v in vals:
+        s = _f32(s + _f32(v))
+    return s
+
+
+def sampling_dist(vals, ids, temperature, top_k=0, top_p=1.0, min_p=0.0) -> SamplingDist:
+    """The sampling distribution of one row from its kept candidates
+    (fp32 logits best first, ties to the lowest id)."""
+    vals = np.asarray(vals, np.float32)
+    ids = np.asarray(ids, np.int32)
+    n = vals.size
+    if top_k > 0:
+        n = min(n, int(top_k))
+    if temperature <= 0:
+        return SamplingDist(ids[:1].copy(), vals[:1].copy(), np.ones(1, np.float32), _f32(1.0), np.inf, [])
+    m = vals[0]
+    d = np.array([_f32(vals[j] - m) for j in range(n)], np.float32)
+    e = np.exp(d).astype(np.float32)
+    cut_margin = np.inf
+    cut_index = []
+    if top_p < 1.0:
+        S = _sum_f32(e[:n])
+        thr = _f32(_f32(top_p) * S)
+        c = _f32(0.0)
+        prev = _f32(0.0)
+        keep = n
+        for j in range(n):
+            prev = c
+            c = _f32(c + e[j])
+            if c >= thr:
+                keep = j + 1
+                break
+        if keep < n or c >= thr:
+            cut_margin = min(cut_margin, float(c - thr) / float(S), float(thr - prev) / float(S) if keep > 1 else np.inf)
+            cut_index.append(keep - 1)
+        n = keep
+    if min_p > 0.0:
+        mp = _f32(min_p)
+        keep = 1
+        while keep < n and e[keep] >= mp:
+            keep += 1
+        cut_margin = min(cut_margin, float(e[keep - 1] - mp) if keep > 1 else np.inf)
+        if keep < n:
+            cut_margin = min(cut_margin, float(mp - e[keep]))
+            cut_index.append(keep - 1)
+        n = keep
+    t = _f32(temperature)
+    w = np.exp(np.array([_f32(d[j] / t) for j in range(n)], np.float32)).astype(np.float32)
+    return SamplingDist(ids[:n].copy(), vals[:n].copy(), w, _sum_f32(w), cut_margin, cut_index)
+
+
+def sample_from(dist: SamplingDist, u, exclude=None):
+    """Inverse-CDF draw over the candidates best first, skipping position
+    `exclude`.  Returns (token id, position, relative margin of the draw
+    from the nearest boundary of the chosen interval)."""
+    order = [j for j in range(dist.ids.size) if j != exclude]
+    if not order:
+        return int(dist.ids[exclude]), exclude, np.inf
+    Wx = _sum_f32(dist.w[order])
+    target = _f32(_f32(u) * Wx)
+    c = _f32(0.0)
+    for j in order:
+        lo = c
+        c = _f32(c + dist.w[j])
+        if target < c:
+            margin = min(float(c - target), float(target - lo) if j != order[0] else np.inf) / float(Wx)
+            return int(dist.ids[j]), j, margin
+    return int(dist.ids[order[-1]]), order[-1], float(target - c) / float(Wx) if float(Wx) > 0 else np.inf
+
+
+@dataclass
+class SampledResult:
+    accept_len: int
+    next_token: int
+    dists: list              # [T] SamplingDist
+    clear: bool              # every decision that fixed the outcome is clear of rounding
+    margin: float            # smallest relative decision margin on the path
+    sel_gap: np.ndarray      # [T] 32nd minus 33rd fp32 logit (inf when V <= 32)
+
+
+def verify_sampled_from_logits(logits, drafts, u, temperature, top_k=0, top_p=1.0, min_p=0.0,
+                               eps_rel=1e-4, eps_logit=1e-3) -> SampledResult:
+    """Speculative sampling verify of T = 1 + n_draft rows of fp32 logits
+    [T][n] with point-mass drafts.  `clear` says whether every decision on
+    the path taken (the kept set, the cuts, each accept test and the final
+    draw) is at least eps_rel (relative) and every candidate order that
+    matters at least eps_logit (logit units) away from flipping."""
+    logits = np.asarray(logits, np.float32)
+    drafts = np.asarray(drafts, np.int32).reshape(-1)
+    u = np.asarray(u, np.float32).reshape(-1)
+    T, n = logits.shape
+    assert T == drafts.size + 1 and u.size >= 2 * T
+    keep = min(SAMPLE_KEEP, n)
+    cid, cval = topk(logits, keep)
+    sel_gap = np.full(T, np.inf)
+    if keep < n:
+        _, cval1 = topk(logits, keep + 1)
+        sel_gap = cval1[:, keep - 1].astype(np.float64) - cval1[:, keep].astype(np.float64)
+    dists = [sampling_dist(cval[i], cid[i], temperature, top_k, top_p, min_p) for i in range(T)]
+    margin = np.inf
+    clear = True
+
+    def order_gap(i, j):
+        v = dists[i].logits
+        g = np.inf
+        if j > 0:
+            g = min(g, float(v[j - 1]) - float(v[j]))
+        if j + 1 < v.size:
+            g = min(g, float(v[j]) - float(v[j + 1]))
+        return g
+
+    def row_checks(i):
+        nonlocal margin, clear
+        dist = dists[i]
+        margin = min(margin, dist.cut_margin)
+        if dist.cut_margin < eps_rel:
+            clear = False
+        for j in dist.cut_index:
+            if order_gap(i, j) < eps_logit:
+                clear = False
+        if dist.ids.size == keep and keep < n and sel_gap[i] < eps_logit and temperature > 0:
+            clear = False
+
+    for i in range(T - 1):
+        dist = dists[i]
+        row_checks(i)
+        hit = np.nonzero(dist.ids == drafts[i])[0]
+        jd = int(hit[0]) if hit.size else None
+        if jd is not None:
+            lhs = _f32(u[2 * i] * dist.W)
+            mg = abs(float(lhs) - float(dist.w[jd])) / float(dist.W)
+            margin = min(margin, mg)
+            if mg < eps_rel:
+                clear = False
+            if lhs < dist.w[jd]:
+                continue
+        tok, j, mg = sample_from(dist, u[2 * i + 1], exclude=jd)
+        margin = min(margin, mg)
+        if mg < eps_rel or order_gap(i, j) < eps_logit:
+            clear = False
+        return SampledResult(i, tok, dists, clear, margin, sel_gap)
+    i = T - 1
+    row_checks(i)
+    tok, j, mg = sample_from(dists[i], u[2 * i + 1])
+    margin = min(margin, mg)
+    if mg < eps_rel or order_gap(i, j) < eps_logit:
+        clear = False
+    return SampledResult(i, tok, dists, clear, margin, sel_gap)
+
+
+def lmhead_verify_sampled(x, Wq, scales, K, V, drafts, u, temperature, top_k=0, top_p=1.0, min_p=0.0):
+    """The int4 head's fp32 logits, then verify_sampled_from_logits."""
+    drafts = np.asarray(drafts, np.int32).reshape(-1)
+    T = drafts.size + 1
+    logits = lmhead_logits(x, Wq, scales, K, T, V)
+    return verify_sampled_from_logits(logits, drafts, u, temperature, top_k, top_p, min_p)
