@@ -503,6 +503,8 @@ def per_kernel_breakdown(torch, sv, device, stream, reps=50):
     # the verify whose ids are the bf16 head's: top-k of the int4 head rescored
     for k in (16, 64):
         cases.append(("head_rescored", "top%d" % k, gen.HIDDEN, gen.VOCAB, (4, k)))
+    # the exact speculative sampling verify (temperature 0.7, top-k 20, top-p 0.95)
+    cases.append(("head_sampled", "t0.7_k20_p0.95", gen.HIDDEN, gen.VOCAB, 4))
     cases.append(("draft_list_add", "32_tokens", 0, gen.VOCAB, 32))
     cases.append(("draft_list_add", "4096_tokens", 0, gen.VOCAB, 4096))
     for kind, label, K, N, T in cases:
@@ -519,6 +521,16 @@ def per_kernel_breakdown(torch, sv, device, stream, reps=50):
             # int4 head read once, plus the bf16 rows of the candidates
             nbytes = gen.lmhead_bytes(N, K, Tt, n_streams=1, n_draft=Tt - 1) + Tt * k * K * 2
             T = Tt
+        elif kind == "head_sampled":
+            Wq, sc = gen.weights(rng, N, K)
+            Ws = [(dev(Wq, np.int32), dev(sc, np.int16)) for _ in range(2)]
+            copies = 2
+            x = dev(gen.activations(rng, T, K), np.int16)
+            drafts = torch.zeros(T - 1, dtype=torch.int32, device=device)
+            u = torch.rand(2 * T, dtype=torch.float32, device=device)
+            fn = lambda i: sv.lmhead_verify_sampled(x, Ws[i % copies][0], Ws[i % copies][1], drafts, u,
+                                                    temperature=0.7, top_k=20, top_p=0.95)
+            nbytes = gen.lmhead_bytes(N, K, T, n_streams=1, n_draft=T - 1)
         elif kind in ("draft_step", "draft_list_add"):
             ids = rng.permutation(N).astype(np.int32)
             static = dev(ids[:32768], np.int32)

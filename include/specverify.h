@@ -210,6 +210,56 @@ int lmhead_argmax_rescored(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *
                            int32_t *ids, float *vals, sv_stream stream);
 
 /*
+ * lmhead_verify_sampled -- exact speculative sampling verify over the 32
+ * best int4 logits of each verify row (page "OpenJet Engine: CUDA LLM
+ * inference for Qwen3.8-27B", sections "How it gets its speed": sampling
+ * keeps the 32 best logits of each verified row, a draft is accepted with
+ * probability p(draft) and a rejected one is resampled from the rest of the
+ * distribution; "Limitations": temperature, top-k <= 32, top-p and min-p
+ * in llama.cpp's order; page "qwen-warp and llamAmpere: two RTX 3090
+ * engines for Qwen3.8, and what each one calls the same answer", section
+ * "What each one calls the same answer": accept, else draw from the
+ * residual, keeps the output distributed exactly as the target).
+ *   Row i's distribution p_i: its 32 best fp32 int4 logits (ties to the
+ *   lowest id), best first; then, in fp32 with m the best logit and
+ *   d_j = l_j - m: top-k keeps the first min(top_k, 32) (top_k <= 0: all);
+ *   top-p the shortest prefix whose running sum of exp(d_j) reaches
+ *   top_p times their sum (top_p >= 1: no cut); min-p the prefix with
+ *   exp(d_j) >= min_p (min_p <= 0: no cut); weights
+ *   w_j = exp(d_j / temperature), W their sum in order (temperature <= 0:
+ *   the point mass on the best candidate, i.e. the greedy verify).
+ *   Drafts are point masses: row i < n_draft accepts drafts[i] iff it is
+ *   kept and u[2i] * W < w_{drafts[i]}; the first rejected row draws
+ *   next_token from p_i without drafts[i], and if all are accepted row
+ *   n_draft draws it from p_{n_draft}: walk the candidates best first with
+ *   running sum c and take the first with u[2i+1] * W' < c (W' the sum over
+ *   the candidates it may take).
+ *   u [2 (n_draft + 1)] fp32 device: uniforms in [0, 1), drawn by the
+ *   caller for every call (row i uses u[2i] and u[2i+1]).  x [n_draft+1][K],
+ *   n_draft 0..7; Wq / scales as for lmhead_verify; no vocab_map.
+ *   Launches three kernels on `stream`: the int4 head's fp32 logits into
+ *   the per-device buffer of lmhead_verify_rescored (same first-call
+ *   allocation), the slice maxima, and one block per row that selects the
+ *   row's 32 best, runs the chain and the accept test; the last block
+ *   writes accept_len and next_token.
+ *   Errors: SV_ERR_NULL, SV_ERR_SHAPE (n_draft out of range, K as for
+ *   w4a16_gemm, V < 1, top_k > 32, NaN parameters, min_p > 1),
+ *   SV_ERR_ALIGN, SV_ERR_CUDA, SV_ERR_NOMEM.
+ *
+ * lmhead_sampling_dist -- the distributions p_t themselves, for T rows
+ * (1..8): ids [T][32] int32 (candidates kept, best first, then -1) and
+ * probs [T][32] fp32 (w_j / W, then 0).  Same kernels, no verify.
+ */
+int lmhead_verify_sampled(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, int K,
+                          const int32_t *drafts, int n_draft, int V,
+                          float temperature, int top_k, float top_p, float min_p,
+                          const float *u, int32_t *accept_len, int32_t *next_token,
+                          sv_stream stream);
+int lmhead_sampling_dist(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, int K,
+                         int T, int V, float temperature, int top_k, float top_p, float min_p,
+                         int32_t *ids, float *probs, sv_stream stream);
+
+/*
  * Dynamic draft list -- the candidate list of the restricted draft head: a
  * static list of token ids (the most frequent tokens) plus the tokens of the
  * current sequence that are missing from it, added as the sequence grows,

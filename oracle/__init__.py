@@ -362,11 +362,36 @@ SAMPLE_KEEP = 32
 @dataclass
 class SamplingDist:
     ids: np.ndarray          # [n] token ids of the candidates kept, best first
-    logits: np.ndarray       # [n] their fp32 logits
+    logits: np.ndarray       # [n_cand] fp32 logits of all the candidates the chain started from
     w: np.ndarray            # [n] fp32 weights
     W: np.float32            # their fp32 sum, in order
     cut_margin: float        # relative distance of the top-p / min-p cuts from their thresholds
-    cut_index: list          # candidate positions next to which a cut fell
+    cut_index: list          # positions after which a cut fell
+    n_cand: int              # candidates the chain started from
+    sel_gap: float           # the last starting candidate's logit minus the first one left out
+
+    def order_gap(self, j):
+        """Logit distance of candidate j from its neighbours in the order."""
+        v = self.logits
+        g = np.inf
+        if j > 0:
+            g = min(g, float(v[j - 1]) - float(v[j]))
+        if j + 1 < v.size:
+            g = min(g, float(v[j]) - float(v[j + 1]))
+        return g
+
+    def cut_clear(self, eps_rel, eps_logit):
+        """Whether the kept set is the same under any rounding of the logits
+        below eps_logit and of the cut sums below eps_rel (a cut after
+        position j depends on the order of j and j + 1 only)."""
+        if self.cut_margin < eps_rel:
+            return False
+        v = self.logits
+        if any(j + 1 < v.size and float(v[j]) - float(v[j + 1]) < eps_logit for j in self.cut_index):
+            return False
+        if self.ids.size == self.n_cand and self.sel_gap < eps_logit:
+            return False
+        return True
 
 
 def _f32(v):
@@ -380,21 +405,25 @@ def _sum_f32(vals):
     return s
 
 
-def sampling_dist(vals, ids, temperature, top_k=0, top_p=1.0, min_p=0.0) -> SamplingDist:
+def sampling_dist(vals, ids, temperature, top_k=0, top_p=1.0, min_p=0.0, sel_gap=np.inf) -> SamplingDist:
     """The sampling distribution of one row from its kept candidates
     (fp32 logits best first, ties to the lowest id)."""
     vals = np.asarray(vals, np.float32)
     ids = np.asarray(ids, np.int32)
-    n = vals.size
-    if top_k > 0:
-        n = min(n, int(top_k))
+    n0 = n = vals.size
+    cut_index = []
+    if top_k > 0 and top_k < n:
+        n = int(top_k)
+        cut_index.append(n - 1)
     if temperature <= 0:
-        return SamplingDist(ids[:1].copy(), vals[:1].copy(), np.ones(1, np.float32), _f32(1.0), np.inf, [])
+        if n0 > 1:
+            cut_index = [0]
+        return SamplingDist(ids[:1].copy(), vals.copy(), np.ones(1, np.float32), _f32(1.0), np.inf,
+                            cut_index, n0, sel_gap)
     m = vals[0]
     d = np.array([_f32(vals[j] - m) for j in range(n)], np.float32)
     e = np.exp(d).astype(np.float32)
     cut_margin = np.inf
-    cut_index = []
     if top_p < 1.0:
         S = _sum_f32(e[:n])
         thr = _f32(_f32(top_p) * S)
@@ -423,7 +452,8 @@ def sampling_dist(vals, ids, temperature, top_k=0, top_p=1.0, min_p=0.0) -> Samp
         n = keep
     t = _f32(temperature)
     w = np.exp(np.array([_f32(d[j] / t) for j in range(n)], np.float32)).astype(np.float32)
-    return SamplingDist(ids[:n].copy(), vals[:n].copy(), w, _sum_f32(w), cut_margin, cut_index)
+    return SamplingDist(ids[:n].copy(), vals.copy(), w, _sum_f32(w), cut_margin, cut_index, n0,
+                        sel_gap)
 
 
 def sample_from(dist: SamplingDist, u, exclude=None):
@@ -452,7 +482,6 @@ class SampledResult:
     dists: list              # [T] SamplingDist
     clear: bool              # every decision that fixed the outcome is clear of rounding
     margin: float            # smallest relative decision margin on the path
-    sel_gap: np.ndarray      # [T] 32nd minus 33rd fp32 logit (inf when V <= 32)
 
 
 def verify_sampled_from_logits(logits, drafts, u, temperature, top_k=0, top_p=1.0, min_p=0.0,
@@ -473,34 +502,25 @@ def verify_sampled_from_logits(logits, drafts, u, temperature, top_k=0, top_p=1.
     if keep < n:
         _, cval1 = topk(logits, keep + 1)
         sel_gap = cval1[:, keep - 1].astype(np.float64) - cval1[:, keep].astype(np.float64)
-    dists = [sampling_dist(cval[i], cid[i], temperature, top_k, top_p, min_p) for i in range(T)]
+    dists = [sampling_dist(cval[i], cid[i], temperature, top_k, top_p, min_p, float(sel_gap[i])) for i in range(T)]
     margin = np.inf
     clear = True
 
-    def order_gap(i, j):
-        v = dists[i].logits
-        g = np.inf
-        if j > 0:
-            g = min(g, float(v[j - 1]) - float(v[j]))
-        if j + 1 < v.size:
-            g = min(g, float(v[j]) - float(v[j + 1]))
-        return g
-
-    def row_checks(i):
+    def draw(i, u_s, exclude=None):
         nonlocal margin, clear
+        tok, j, mg = sample_from(dists[i], u_s, exclude)
+        margin = min(margin, mg)
+        if mg < eps_rel or dists[i].order_gap(j) < eps_logit:
+            clear = False
+        return tok
+
+    for i in range(T):
         dist = dists[i]
         margin = min(margin, dist.cut_margin)
-        if dist.cut_margin < eps_rel:
+        if not dist.cut_clear(eps_rel, eps_logit):
             clear = False
-        for j in dist.cut_index:
-            if order_gap(i, j) < eps_logit:
-                clear = False
-        if dist.ids.size == keep and keep < n and sel_gap[i] < eps_logit and temperature > 0:
-            clear = False
-
-    for i in range(T - 1):
-        dist = dists[i]
-        row_checks(i)
+        if i == T - 1:
+            return SampledResult(i, draw(i, u[2 * i + 1]), dists, clear, margin)
         hit = np.nonzero(dist.ids == drafts[i])[0]
         jd = int(hit[0]) if hit.size else None
         if jd is not None:
@@ -511,18 +531,7 @@ def verify_sampled_from_logits(logits, drafts, u, temperature, top_k=0, top_p=1.
                 clear = False
             if lhs < dist.w[jd]:
                 continue
-        tok, j, mg = sample_from(dist, u[2 * i + 1], exclude=jd)
-        margin = min(margin, mg)
-        if mg < eps_rel or order_gap(i, j) < eps_logit:
-            clear = False
-        return SampledResult(i, tok, dists, clear, margin, sel_gap)
-    i = T - 1
-    row_checks(i)
-    tok, j, mg = sample_from(dists[i], u[2 * i + 1])
-    margin = min(margin, mg)
-    if mg < eps_rel or order_gap(i, j) < eps_logit:
-        clear = False
-    return SampledResult(i, tok, dists, clear, margin, sel_gap)
+        return SampledResult(i, draw(i, u[2 * i + 1], jd), dists, clear, margin)
 
 
 def lmhead_verify_sampled(x, Wq, scales, K, V, drafts, u, temperature, top_k=0, top_p=1.0, min_p=0.0):

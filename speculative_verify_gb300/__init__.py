@@ -63,6 +63,11 @@ def load(path: str | None = None):
     lib.lmhead_verify_rescored.restype = ci
     lib.lmhead_argmax_rescored.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, vp, vp, vp]
     lib.lmhead_argmax_rescored.restype = ci
+    cf = ctypes.c_float
+    lib.lmhead_verify_sampled.argtypes = [vp, vp, vp, ci, vp, ci, ci, cf, ci, cf, cf, vp, vp, vp, vp]
+    lib.lmhead_verify_sampled.restype = ci
+    lib.lmhead_sampling_dist.argtypes = [vp, vp, vp, ci, ci, ci, cf, ci, cf, cf, vp, vp, vp]
+    lib.lmhead_sampling_dist.restype = ci
     lib.draft_list_bytes.argtypes = [ci, ci, ci]
     lib.draft_list_bytes.restype = ctypes.c_size_t
     lib.draft_list_ids.argtypes = [vp, ci]
@@ -310,6 +315,46 @@ def lmhead_argmax_rescored(x, Wq, scales, Wbf, top_k=16, ids=None, vals=None, st
     _check("lmhead_argmax_rescored", load().lmhead_argmax_rescored(
         _ptr(x), _ptr(Wq), _ptr(scales), _ptr(Wbf), K, T, int(top_k), V, _ptr(ids), _ptr(vals), _stream(stream)))
     return ids, vals
+
+
+def lmhead_verify_sampled(x, Wq, scales, drafts, u, temperature=1.0, top_k=0, top_p=1.0, min_p=0.0,
+                          accept_len=None, next_token=None, stream=None):
+    """Exact speculative sampling verify over the 32 best logits of each
+    row; u holds 2 (n_draft + 1) fp32 uniforms in [0, 1) on the device."""
+    torch = _torch()
+    _bits16(x, "x"), _words(Wq, "Wq"), _bits16(scales, "scales")
+    T, K = x.shape
+    V = Wq.shape[0]
+    n_draft = drafts.numel()
+    if T != n_draft + 1:
+        raise ValueError("x must have 1 + n_draft rows")
+    if n_draft:
+        _i32(drafts, "drafts")
+    if not (u.is_cuda and u.dtype == torch.float32 and u.is_contiguous() and u.numel() >= 2 * T):
+        raise ValueError("u must be a contiguous CUDA float32 tensor of 2 (n_draft + 1) uniforms")
+    if accept_len is None:
+        accept_len = torch.empty(1, dtype=torch.int32, device=x.device)
+    if next_token is None:
+        next_token = torch.empty(1, dtype=torch.int32, device=x.device)
+    _check("lmhead_verify_sampled", load().lmhead_verify_sampled(
+        _ptr(x), _ptr(Wq), _ptr(scales), K, _ptr(drafts) if n_draft else None, n_draft, V, float(temperature),
+        int(top_k), float(top_p), float(min_p), _ptr(u), _ptr(accept_len), _ptr(next_token), _stream(stream)))
+    return accept_len, next_token
+
+
+def lmhead_sampling_dist(x, Wq, scales, temperature=1.0, top_k=0, top_p=1.0, min_p=0.0, stream=None):
+    """The rows' sampling distributions: ids [T][32] (-1 past the kept
+    candidates) and probs [T][32]."""
+    torch = _torch()
+    _bits16(x, "x"), _words(Wq, "Wq"), _bits16(scales, "scales")
+    T, K = x.shape
+    V = Wq.shape[0]
+    ids = torch.empty((T, 32), dtype=torch.int32, device=x.device)
+    probs = torch.empty((T, 32), dtype=torch.float32, device=x.device)
+    _check("lmhead_sampling_dist", load().lmhead_sampling_dist(
+        _ptr(x), _ptr(Wq), _ptr(scales), K, T, V, float(temperature), int(top_k), float(top_p), float(min_p),
+        _ptr(ids), _ptr(probs), _stream(stream)))
+    return ids, probs
 
 
 class DraftList:

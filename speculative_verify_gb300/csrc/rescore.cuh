@@ -151,6 +151,91 @@ __global__ void __launch_bounds__(RS_THREADS) slicemax_kernel(const __grid_const
     }
 }
 
+// Shared memory of select_row (static, in the calling kernel).
+struct SelectSmem {
+    unsigned long long wl[RS_WARPS][64];
+    int slist[RS_KMAX];
+    unsigned long long tau;
+    unsigned n_sel, n_sl;
+};
+
+// The k best (logit, id) keys of one row, descending, into sel[0..k) (keys
+// past the row's candidates are 0), by the whole CTA; sel holds RS_SEL_MAX
+// keys.  mx: the row's nS slice maxima; row: its V fp32 logits.  With tau
+// the k-th largest slice maximum, k slices hold a key >= tau, so the row's
+// k best keys are >= tau and lie in the (at most k) slices whose maximum is
+// >= tau; at most 128 k keys are gathered and sorted.
+__device__ __forceinline__ void select_row(const unsigned long long *mx, const float *row, int nS, int V, int k,
+                                           unsigned long long *sel, SelectSmem &sm)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) {
+        sm.n_sel = 0u;
+        sm.n_sl = 0u;
+    }
+    // tau: each warp keeps the 64 best maxima of its chunks of 128, then
+    // warp 0 merges the warps' lists
+    {
+        unsigned long long a0 = 0ull, a1 = 0ull;
+        for (int c = warp; c * RS_SLICE < nS; c += RS_WARPS) {
+            unsigned long long v[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int s = c * RS_SLICE + i * 32 + lane;
+                v[i] = s < nS ? __ldcg(mx + s) : 0ull;
+            }
+            warp_sort128_desc(v, lane);
+            warp_merge64_desc(a0, a1, v[0], v[1], lane);
+        }
+        sm.wl[warp][lane] = a0;
+        sm.wl[warp][32 + lane] = a1;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        unsigned long long a0 = sm.wl[0][lane], a1 = sm.wl[0][32 + lane];
+        for (int w = 1; w < RS_WARPS; ++w) warp_merge64_desc(a0, a1, sm.wl[w][lane], sm.wl[w][32 + lane], lane);
+        const int kk = k - 1;
+        const unsigned long long tk = shfl_u64(kk < 32 ? a0 : a1, kk & 31);
+        if (lane == 0) sm.tau = tk;
+    }
+    __syncthreads();
+    // the (at most k) slices whose maximum is >= tau; with fewer than k
+    // slices tau is 0 and every slice qualifies
+    const unsigned long long tau = sm.tau;
+    for (int s = tid; s < nS; s += RS_THREADS) {
+        const unsigned long long m = __ldcg(mx + s);
+        if (m != 0ull && m >= tau) {
+            const unsigned at = atomicAdd(&sm.n_sl, 1u);
+            if (at < static_cast<unsigned>(RS_KMAX)) sm.slist[at] = s;
+        }
+    }
+    __syncthreads();
+    // their keys >= tau (the order of sel is fixed below by sorting)
+    const int nsl = min(static_cast<int>(sm.n_sl), RS_KMAX);
+    for (int j = warp; j < nsl; j += RS_WARPS) {
+        const int v0 = sm.slist[j] * RS_SLICE;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int r = v0 + i * 32 + lane;
+            const unsigned long long key = r < V ? make_key(__ldcg(row + r), static_cast<uint32_t>(r)) : 0ull;
+            const bool keep = key != 0ull && key >= tau;
+            const unsigned bal = __ballot_sync(0xFFFFFFFFu, keep);
+            unsigned base = 0u;
+            if (lane == 0 && bal) base = atomicAdd(&sm.n_sel, static_cast<unsigned>(__popc(bal)));
+            base = __shfl_sync(0xFFFFFFFFu, base, 0);
+            const unsigned at = base + __popc(bal & ((1u << lane) - 1u));
+            if (keep && at < static_cast<unsigned>(RS_SEL_MAX)) sel[at] = key;
+        }
+    }
+    __syncthreads();
+    const int ns = min(static_cast<int>(sm.n_sel), RS_SEL_MAX);
+    int npad = 1;
+    while (npad < ns || npad < k) npad <<= 1;
+    for (int i = ns + tid; i < npad; i += RS_THREADS) sel[i] = 0ull;
+    __syncthreads();
+    cta_sort_desc(sel, npad);
+}
+
 struct RescoreParams {
     const uint16_t *x;                   // [T][K] bf16 bits
     const uint16_t *Wbf;                 // [V][K] bf16 bits
@@ -172,84 +257,17 @@ struct RescoreParams {
 __global__ void __launch_bounds__(RS_THREADS) rescore_kernel(const __grid_constant__ RescoreParams p)
 {
     extern __shared__ __align__(16) unsigned long long sel[];
-    __shared__ unsigned long long wl[RS_WARPS][64];
-    __shared__ int slist[RS_KMAX];
+    __shared__ SelectSmem sm;
     __shared__ float lg[RS_TMAX];
     __shared__ int lid[RS_TMAX];
-    __shared__ unsigned long long tau_s;
-    __shared__ unsigned n_sel, n_sl, is_last;
+    __shared__ unsigned is_last;
     const int t = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     uint16_t *xs = reinterpret_cast<uint16_t *>(sel + RS_SEL_MAX);
     pdl_wait_prior();                    // logits and slice maxima come from the passes before
-    if (tid == 0) {
-        n_sel = 0u;
-        n_sl = 0u;
-    }
-    const unsigned long long *mx = p.smax + static_cast<size_t>(t) * p.nS;
-    // tau: each warp keeps the 64 best maxima of its chunks of 128, then
-    // warp 0 merges the warps' lists
-    {
-        unsigned long long a0 = 0ull, a1 = 0ull;
-        for (int c = warp; c * RS_SLICE < p.nS; c += RS_WARPS) {
-            unsigned long long v[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int s = c * RS_SLICE + i * 32 + lane;
-                v[i] = s < p.nS ? __ldcg(mx + s) : 0ull;
-            }
-            warp_sort128_desc(v, lane);
-            warp_merge64_desc(a0, a1, v[0], v[1], lane);
-        }
-        wl[warp][lane] = a0;
-        wl[warp][32 + lane] = a1;
-    }
     const uint4 *xg = reinterpret_cast<const uint4 *>(p.x + static_cast<size_t>(t) * p.K);
     for (int c = tid; c < p.K / 8; c += RS_THREADS) reinterpret_cast<uint4 *>(xs)[c] = xg[c];
-    __syncthreads();
-    if (warp == 0) {
-        unsigned long long a0 = wl[0][lane], a1 = wl[0][32 + lane];
-        for (int w = 1; w < RS_WARPS; ++w) warp_merge64_desc(a0, a1, wl[w][lane], wl[w][32 + lane], lane);
-        const int kk = p.k - 1;
-        const unsigned long long tk = shfl_u64(kk < 32 ? a0 : a1, kk & 31);
-        if (lane == 0) tau_s = tk;
-    }
-    __syncthreads();
-    // the (at most k) slices whose maximum is >= tau; with fewer than k
-    // slices tau is 0 and every slice qualifies
-    const unsigned long long tau = tau_s;
-    for (int s = tid; s < p.nS; s += RS_THREADS) {
-        const unsigned long long m = __ldcg(mx + s);
-        if (m != 0ull && m >= tau) {
-            const unsigned at = atomicAdd(&n_sl, 1u);
-            if (at < static_cast<unsigned>(RS_KMAX)) slist[at] = s;
-        }
-    }
-    __syncthreads();
-    // their keys >= tau (the order of sel is fixed below by sorting)
-    const int nsl = min(static_cast<int>(n_sl), RS_KMAX);
-    const float *row = p.logits + static_cast<size_t>(t) * p.V;
-    for (int j = warp; j < nsl; j += RS_WARPS) {
-        const int v0 = slist[j] * RS_SLICE;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int r = v0 + i * 32 + lane;
-            const unsigned long long key = r < p.V ? make_key(__ldcg(row + r), static_cast<uint32_t>(r)) : 0ull;
-            const bool keep = key != 0ull && key >= tau;
-            const unsigned bal = __ballot_sync(0xFFFFFFFFu, keep);
-            unsigned base = 0u;
-            if (lane == 0 && bal) base = atomicAdd(&n_sel, static_cast<unsigned>(__popc(bal)));
-            base = __shfl_sync(0xFFFFFFFFu, base, 0);
-            const unsigned at = base + __popc(bal & ((1u << lane) - 1u));
-            if (keep && at < static_cast<unsigned>(RS_SEL_MAX)) sel[at] = key;
-        }
-    }
-    __syncthreads();
-    const int ns = min(static_cast<int>(n_sel), RS_SEL_MAX);
-    int npad = 1;
-    while (npad < ns || npad < p.k) npad <<= 1;
-    for (int i = ns + tid; i < npad; i += RS_THREADS) sel[i] = 0ull;
-    __syncthreads();
-    cta_sort_desc(sel, npad);
+    select_row(p.smax + static_cast<size_t>(t) * p.nS, p.logits + static_cast<size_t>(t) * p.V, p.nS, p.V, p.k,
+               sel, sm);
     // rescore candidate j = 16 r + warp: eight 16-byte weight loads per lane
     // in flight, x from shared memory
     const int j = blockIdx.x * RS_PER_CTA + warp;
@@ -344,6 +362,175 @@ __global__ void __launch_bounds__(RS_THREADS) rescore_kernel(const __grid_consta
         p.accept_len[0] = acc;
         p.next_token[0] = lid[acc];
     }
+    *p.done = 0u;                        // ready for the next call
+}
+
+// ---------------------------------------------------------------------------
+// Exact speculative sampling verify over the 32 best logits of each row
+// (page "OpenJet Engine: CUDA LLM inference for Qwen3.8-27B", sections "How
+// it gets its speed": sampling keeps the 32 best logits of each verified
+// row, accepts a draft with probability p(draft) and resamples a rejected
+// one from the rest of the distribution; "Limitations": temperature, top-k
+// <= 32, top-p and min-p in llama.cpp's order).
+//
+// The drafter is a point mass on its draft d: the acceptance probability
+// is p(d) and the residual distribution is p without d, renormalised.  Chain
+// per row, fp32, fixed order (m the best logit, d_j = l_j - m, candidates
+// best first):
+//   top-k:  the first min(top_k, 32) candidates (top_k <= 0: all 32);
+//   top-p:  the shortest prefix whose running sum of exp(d_j) reaches
+//           top_p times their sum (top_p >= 1: no cut);
+//   min-p:  the prefix with exp(d_j) >= min_p (min_p <= 0: no cut);
+//   temperature: w_j = exp(d_j / temperature), W = sum in order;
+//           temperature <= 0: the point mass on the best candidate.
+// Row i < n_draft accepts iff u[2i] * W < w_d; a rejected row draws from
+// the candidates other than d, and the last row from all of them: walk the
+// candidates best first with running sum c and take the first with
+// u[2i+1] * W' < c.
+
+constexpr int SAMPLE_KEEP = 32;
+
+struct SampleParams {
+    const float *logits;                 // [T][V] from the int4 pass
+    const unsigned long long *smax;      // [T][nS] from slicemax_kernel
+    int nS, T, V;
+    float temperature, top_p, min_p;
+    int top_k;
+    int mode;                            // 0: verify, 1: distributions only
+    const float *u;                      // [2T] uniforms in [0, 1) (verify)
+    const int32_t *drafts;               // [T-1] (verify)
+    int32_t *accept_len, *next_token;    // [1] (verify)
+    int32_t *out_ids;                    // [T][32] (distributions; -1 past the kept candidates)
+    float *out_probs;                    // [T][32] (distributions; w_j / W, 0 past them)
+    int32_t *row_acc, *row_tok;          // scratch [RS_TMAX]
+    unsigned *done;                      // scratch counter, left at 0
+};
+
+// One CTA per verify row.  Dynamic shared memory: RS_SEL_MAX keys.
+__global__ void __launch_bounds__(RS_THREADS) sample_kernel(const __grid_constant__ SampleParams p)
+{
+    extern __shared__ __align__(16) unsigned long long sel[];
+    __shared__ SelectSmem sm;
+    __shared__ float es[SAMPLE_KEEP], ds[SAMPLE_KEEP], ws[SAMPLE_KEEP];
+    __shared__ int ids[SAMPLE_KEEP];
+    __shared__ int n_keep;
+    __shared__ float Wsum;
+    __shared__ unsigned is_last;
+    const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
+    pdl_wait_prior();                    // logits and slice maxima come from the passes before
+    const int keep = min(SAMPLE_KEEP, p.V);
+    select_row(p.smax + static_cast<size_t>(t) * p.nS, p.logits + static_cast<size_t>(t) * p.V, p.nS, p.V, keep,
+               sel, sm);
+    if (tid < 32) {
+        // the chain, by warp 0: lane j holds candidate j
+        const unsigned long long key = lane < keep ? sel[lane] : 0ull;
+        const float l = key ? key_value(key) : 0.f;
+        ids[lane] = key ? key_id(key) : -1;
+        const float m = __shfl_sync(0xFFFFFFFFu, l, 0);
+        const float d = l - m;
+        es[lane] = expf(d);
+        ds[lane] = d;
+        __syncwarp();
+        if (lane == 0) {
+            int n = keep;
+            if (p.top_k > 0) n = min(n, p.top_k);
+            if (p.temperature > 0.f) {
+                if (p.top_p < 1.f) {
+                    float S = 0.f;
+                    for (int j = 0; j < n; ++j) S = S + es[j];
+                    const float thr = p.top_p * S;
+                    float c = 0.f;
+                    for (int j = 0; j < n; ++j) {
+                        c = c + es[j];
+                        if (c >= thr) {
+                            n = j + 1;
+                            break;
+                        }
+                    }
+                }
+                if (p.min_p > 0.f) {
+                    int k = 1;
+                    while (k < n && es[k] >= p.min_p) ++k;
+                    n = k;
+                }
+            } else {
+                n = 1;
+            }
+            n_keep = n;
+        }
+        __syncwarp();
+        const int n = n_keep;
+        if (lane < n) ws[lane] = p.temperature > 0.f ? expf(ds[lane] / p.temperature) : 1.f;
+        __syncwarp();
+        if (lane == 0) {
+            float W = 0.f;
+            for (int j = 0; j < n; ++j) W = W + ws[j];
+            Wsum = W;
+        }
+        __syncwarp();
+        if (p.mode == 1) {
+            p.out_ids[t * SAMPLE_KEEP + lane] = lane < n ? ids[lane] : -1;
+            p.out_probs[t * SAMPLE_KEEP + lane] = lane < n ? ws[lane] / Wsum : 0.f;
+        } else if (lane == 0) {
+            const bool draft_row = t < p.T - 1;
+            int jd = -1;
+            int acc = 0;
+            if (draft_row) {
+                const int dr = p.drafts[t];
+                for (int j = 0; j < n; ++j)
+                    if (ids[j] == dr) {
+                        jd = j;
+                        break;
+                    }
+                acc = (jd >= 0 && p.u[2 * t] * Wsum < ws[jd]) ? 1 : 0;
+            }
+            // the draw from the candidates other than jd (all of them on the
+            // last row); with none left the draft itself (then it was
+            // accepted with probability 1)
+            float Wx = 0.f;
+            int last = -1;
+            for (int j = 0; j < n; ++j)
+                if (j != jd) {
+                    Wx = Wx + ws[j];
+                    last = j;
+                }
+            int tok = jd >= 0 ? ids[jd] : ids[0];
+            if (last >= 0) {
+                const float target = p.u[2 * t + 1] * Wx;
+                float c = 0.f;
+                int pick = last;
+                for (int j = 0; j < n; ++j) {
+                    if (j == jd) continue;
+                    c = c + ws[j];
+                    if (target < c) {
+                        pick = j;
+                        break;
+                    }
+                }
+                tok = ids[pick];
+            }
+            p.row_acc[t] = acc;
+            p.row_tok[t] = tok;
+        }
+    }
+    if (p.mode == 1) return;
+    __syncthreads();
+    if (tid == 0) {
+        __threadfence();
+        is_last = atomicAdd(p.done, 1u) == gridDim.x - 1u;
+    }
+    __syncthreads();
+    if (!is_last || tid != 0) return;
+    __threadfence();
+    const int n_draft = p.T - 1;
+    int acc = n_draft;
+    for (int i = 0; i < n_draft; ++i)
+        if (!__ldcg(&p.row_acc[i])) {
+            acc = i;
+            break;
+        }
+    p.accept_len[0] = acc;
+    p.next_token[0] = __ldcg(&p.row_tok[acc]);
     *p.done = 0u;                        // ready for the next call
 }
 

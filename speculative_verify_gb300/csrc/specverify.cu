@@ -39,7 +39,10 @@ struct DeviceState {
     // rescoring (rescore.cuh); the logits and candidate buffers grow on demand
     float *cand_lg = nullptr;             // [RS_TMAX][RS_KMAX] rescored logits
     int32_t *cand_id = nullptr;           // [RS_TMAX][RS_KMAX] their ids
-    unsigned *rdone = nullptr;            // CTA counter, left at 0
+    unsigned *rdone = nullptr;            // rescore_kernel's CTA counter, left at 0
+    unsigned *sdone = nullptr;            // sample_kernel's CTA counter, left at 0
+    int32_t *row_acc = nullptr;           // [RS_TMAX] per-row accept flags of the sampled verify
+    int32_t *row_tok = nullptr;           // [RS_TMAX] per-row drawn tokens
     float *rs_logits = nullptr;           // [RS_TMAX][rs_v_cap]
     unsigned long long *rs_smax = nullptr;   // [RS_TMAX][rs_s_cap] slice maxima
     long long rs_v_cap = 0, rs_s_cap = 0;
@@ -140,6 +143,9 @@ int device_state(DeviceState **out)
         st.cand_lg = reinterpret_cast<float *>(base + off);
         st.cand_id = reinterpret_cast<int32_t *>(base + off + RS_TMAX * RS_KMAX * sizeof(float));
         st.rdone = reinterpret_cast<unsigned *>(base + off + RS_TMAX * RS_KMAX * 8);
+        st.sdone = st.rdone + 1;
+        st.row_acc = reinterpret_cast<int32_t *>(base + off + RS_TMAX * RS_KMAX * 8 + 16);
+        st.row_tok = st.row_acc + RS_TMAX;
         st.x16_max_groups = X16_MAX_GROUPS;
         cudaError_t e = cudaSuccess;
         e = e != cudaSuccess ? e : raise_smem_limit<1, false, false, false>(optin);
@@ -157,6 +163,9 @@ int device_state(DeviceState **out)
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(rescore_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      optin - RS_STATIC_SMEM_SLACK);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     RS_SEL_MAX * 8);
         if (e != cudaSuccess || tensor_map_fn() != SV_OK) {
             cudaFree(base);
             return SV_ERR_CUDA;
@@ -365,30 +374,18 @@ int head_call(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, int K
 // pass 1 is the head kernel as a GEMM with fp32 outputs, pass 2
 // slicemax_kernel, pass 3 rescore_kernel.
 
-int rescored_call(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, const sv_bf16 *Wbf, int K, int T,
-                  int top_k, int V, int mode, const int32_t *drafts, int n_draft, int32_t *accept_len,
-                  int32_t *next_token, int32_t *ids, float *vals, cudaStream_t stream)
+// Passes 1 and 2 shared by the rescored and the sampled calls: the int4
+// head's fp32 logits [T][V] into a per-device buffer, then every 128-row
+// slice's largest key.  On success *cfg is set up for the next PDL launch
+// on `stream` (block RS_THREADS) and *nS_out is the slice count.
+int logits_and_slice_maxima(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, int K, int T, int V,
+                            cudaStream_t stream, DeviceState **st_out, int *nS_out, cudaLaunchConfig_t *cfg,
+                            cudaLaunchAttribute *attr)
 {
-    int rc = check_common(x, Wq, scales, T, K);
-    if (rc != SV_OK) return rc;
-    if (!Wbf) return SV_ERR_NULL;
-    if (!aligned16(Wbf)) return SV_ERR_ALIGN;
-    if (T > RS_TMAX || V < 1 || top_k < 1 || top_k > RS_KMAX || top_k > V) return SV_ERR_SHAPE;
-    if (mode == 0) {
-        if (!accept_len || !next_token) return SV_ERR_NULL;
-        if (n_draft > 0 && !drafts) return SV_ERR_NULL;
-        if ((drafts && !aligned4(drafts)) || !aligned4(accept_len) || !aligned4(next_token)) return SV_ERR_ALIGN;
-    } else {
-        if (!ids) return SV_ERR_NULL;
-        if (!aligned4(ids) || (vals && !aligned4(vals))) return SV_ERR_ALIGN;
-    }
     DeviceState *st = nullptr;
-    rc = device_state(&st);
+    int rc = device_state(&st);
     if (rc != SV_OK) return rc;
-    // slices of RS_SLICE rows of V
     const long long nS = (static_cast<long long>(V) + RS_SLICE - 1) / RS_SLICE;
-    const long long limit = st->smem_optin - RS_STATIC_SMEM_SLACK;
-    if (K > 65536 || RS_SEL_MAX * 8LL + 2LL * K > limit) return SV_ERR_SHAPE;
     {
         std::lock_guard<std::mutex> lock(g_mu);
         if (V > st->rs_v_cap || nS > st->rs_s_cap) {
@@ -423,15 +420,13 @@ int rescored_call(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, c
     p.y32 = st->rs_logits;
     rc = dispatch<false, false>(p, *st, stream);
     if (rc != SV_OK) return rc;
-    cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cudaLaunchConfig_t cfg;
-    std::memset(&cfg, 0, sizeof cfg);
-    cfg.blockDim = dim3(RS_THREADS);
-    cfg.stream = stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    std::memset(cfg, 0, sizeof *cfg);
+    cfg->blockDim = dim3(RS_THREADS);
+    cfg->stream = stream;
+    cfg->attrs = attr;
+    cfg->numAttrs = 1;
     // pass 2: every slice's largest key per row
     SliceMaxParams mp{};
     mp.logits = st->rs_logits;
@@ -439,19 +434,54 @@ int rescored_call(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, c
     mp.V = V;
     mp.nS = static_cast<int>(nS);
     mp.smax = st->rs_smax;
-    cfg.gridDim = dim3(static_cast<unsigned>((nS + RS_WARPS - 1) / RS_WARPS));
-    cfg.dynamicSmemBytes = 0;
-    if (cudaLaunchKernelEx(&cfg, slicemax_kernel, mp) != cudaSuccess) {
+    cfg->gridDim = dim3(static_cast<unsigned>((nS + RS_WARPS - 1) / RS_WARPS));
+    cfg->dynamicSmemBytes = 0;
+    if (cudaLaunchKernelEx(cfg, slicemax_kernel, mp) != cudaSuccess) {
         cudaGetLastError();
         return SV_ERR_CUDA;
     }
-    // pass 3: threshold, gather, rescore with the bf16 head, argmax, verify
+    *st_out = st;
+    *nS_out = static_cast<int>(nS);
+    return SV_OK;
+}
+
+int rescored_call(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, const sv_bf16 *Wbf, int K, int T,
+                  int top_k, int V, int mode, const int32_t *drafts, int n_draft, int32_t *accept_len,
+                  int32_t *next_token, int32_t *ids, float *vals, cudaStream_t stream)
+{
+    int rc = check_common(x, Wq, scales, T, K);
+    if (rc != SV_OK) return rc;
+    if (!Wbf) return SV_ERR_NULL;
+    if (!aligned16(Wbf)) return SV_ERR_ALIGN;
+    if (T > RS_TMAX || V < 1 || top_k < 1 || top_k > RS_KMAX || top_k > V) return SV_ERR_SHAPE;
+    if (mode == 0) {
+        if (!accept_len || !next_token) return SV_ERR_NULL;
+        if (n_draft > 0 && !drafts) return SV_ERR_NULL;
+        if ((drafts && !aligned4(drafts)) || !aligned4(accept_len) || !aligned4(next_token)) return SV_ERR_ALIGN;
+    } else {
+        if (!ids) return SV_ERR_NULL;
+        if (!aligned4(ids) || (vals && !aligned4(vals))) return SV_ERR_ALIGN;
+    }
+    {
+        DeviceState *st0 = nullptr;
+        rc = device_state(&st0);
+        if (rc != SV_OK) return rc;
+        const long long limit = st0->smem_optin - RS_STATIC_SMEM_SLACK;
+        if (K > 65536 || RS_SEL_MAX * 8LL + 2LL * K > limit) return SV_ERR_SHAPE;
+    }
+    DeviceState *st = nullptr;
+    int nS = 0;
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[1];
+    rc = logits_and_slice_maxima(x, Wq, scales, K, T, V, stream, &st, &nS, &cfg, attr);
+    if (rc != SV_OK) return rc;
+    // pass 3: selection, rescoring with the bf16 head, argmax, verify
     RescoreParams rp{};
     rp.x = x;
     rp.Wbf = Wbf;
     rp.logits = st->rs_logits;
     rp.smax = st->rs_smax;
-    rp.nS = static_cast<int>(nS);
+    rp.nS = nS;
     rp.T = T;
     rp.K = K;
     rp.V = V;
@@ -468,6 +498,61 @@ int rescored_call(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, c
     cfg.gridDim = dim3(static_cast<unsigned>((top_k + RS_PER_CTA - 1) / RS_PER_CTA), static_cast<unsigned>(T));
     cfg.dynamicSmemBytes = static_cast<size_t>(RS_SEL_MAX) * 8 + 2 * static_cast<size_t>(K);
     if (cudaLaunchKernelEx(&cfg, rescore_kernel, rp) != cudaSuccess) {
+        cudaGetLastError();
+        return SV_ERR_CUDA;
+    }
+    return SV_OK;
+}
+
+// Exact speculative sampling verify (mode 0) or the rows' sampling
+// distributions (mode 1): passes 1 and 2 as above, then sample_kernel.
+int sampled_call(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, int K, int T, int V,
+                 float temperature, int top_k, float top_p, float min_p, int mode, const float *u,
+                 const int32_t *drafts, int32_t *accept_len, int32_t *next_token, int32_t *out_ids,
+                 float *out_probs, cudaStream_t stream)
+{
+    int rc = check_common(x, Wq, scales, T, K);
+    if (rc != SV_OK) return rc;
+    if (T > RS_TMAX || V < 1 || top_k > SAMPLE_KEEP) return SV_ERR_SHAPE;
+    if (temperature != temperature || top_p != top_p || min_p != min_p || min_p > 1.f) return SV_ERR_SHAPE;
+    if (mode == 0) {
+        if (!u || !accept_len || !next_token) return SV_ERR_NULL;
+        if (T > 1 && !drafts) return SV_ERR_NULL;
+        if (!aligned4(u) || (drafts && !aligned4(drafts)) || !aligned4(accept_len) || !aligned4(next_token))
+            return SV_ERR_ALIGN;
+    } else {
+        if (!out_ids || !out_probs) return SV_ERR_NULL;
+        if (!aligned4(out_ids) || !aligned4(out_probs)) return SV_ERR_ALIGN;
+    }
+    DeviceState *st = nullptr;
+    int nS = 0;
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[1];
+    rc = logits_and_slice_maxima(x, Wq, scales, K, T, V, stream, &st, &nS, &cfg, attr);
+    if (rc != SV_OK) return rc;
+    SampleParams sp{};
+    sp.logits = st->rs_logits;
+    sp.smax = st->rs_smax;
+    sp.nS = nS;
+    sp.T = T;
+    sp.V = V;
+    sp.temperature = temperature;
+    sp.top_p = top_p;
+    sp.min_p = min_p;
+    sp.top_k = top_k;
+    sp.mode = mode;
+    sp.u = u;
+    sp.drafts = drafts;
+    sp.accept_len = accept_len;
+    sp.next_token = next_token;
+    sp.out_ids = out_ids;
+    sp.out_probs = out_probs;
+    sp.row_acc = st->row_acc;
+    sp.row_tok = st->row_tok;
+    sp.done = st->sdone;
+    cfg.gridDim = dim3(static_cast<unsigned>(T));
+    cfg.dynamicSmemBytes = static_cast<size_t>(RS_SEL_MAX) * 8;
+    if (cudaLaunchKernelEx(&cfg, sample_kernel, sp) != cudaSuccess) {
         cudaGetLastError();
         return SV_ERR_CUDA;
     }
@@ -705,6 +790,23 @@ int lmhead_argmax_rescored(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *
 {
     return sv::rescored_call(x, Wq, scales, Wbf, K, T, top_k, V, 1, nullptr, 0, nullptr, nullptr, ids, vals,
                              reinterpret_cast<cudaStream_t>(stream));
+}
+
+int lmhead_verify_sampled(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, int K,
+                          const int32_t *drafts, int n_draft, int V, float temperature, int top_k, float top_p,
+                          float min_p, const float *u, int32_t *accept_len, int32_t *next_token, sv_stream stream)
+{
+    if (n_draft < 0 || n_draft > sv::RS_TMAX - 1) return SV_ERR_SHAPE;
+    return sv::sampled_call(x, Wq, scales, K, n_draft + 1, V, temperature, top_k, top_p, min_p, 0, u, drafts,
+                            accept_len, next_token, nullptr, nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int lmhead_sampling_dist(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, int K, int T, int V,
+                         float temperature, int top_k, float top_p, float min_p, int32_t *ids, float *probs,
+                         sv_stream stream)
+{
+    return sv::sampled_call(x, Wq, scales, K, T, V, temperature, top_k, top_p, min_p, 1, nullptr, nullptr, nullptr,
+                            nullptr, ids, probs, reinterpret_cast<cudaStream_t>(stream));
 }
 
 // ----------------------------------------------------------------------------

@@ -39,7 +39,9 @@ def test_status_strings(lib):
 
 
 def test_binding_has_same_names_as_abi():
-    for name in ("w4a16_gemm", "lmhead_verify", "lmhead_verify_batched", "lmhead_argmax", "DraftList"):
+    for name in ("w4a16_gemm", "lmhead_verify", "lmhead_verify_batched", "lmhead_argmax", "DraftList",
+                 "lmhead_verify_rescored", "lmhead_argmax_rescored", "lmhead_verify_sampled",
+                 "lmhead_sampling_dist"):
         assert callable(getattr(sv, name))
 
 
@@ -139,3 +141,48 @@ def test_draft_list_rejects_bad_arguments(lib):
     assert lib.draft_list_add(A, A2, 0, None) == 0          # nothing to add: no launch
     assert lib.draft_list_add(MIS, A2, 4, None) == -3
     assert lib.draft_list_count(NUL, None) == -1
+
+
+NAN = float("nan")
+
+
+@nogpu
+@pytest.mark.parametrize("kw,code", [
+    (dict(n_draft=8), -2),
+    (dict(n_draft=-1), -2),
+    (dict(top_k=33), -2),
+    (dict(temp=NAN), -2),
+    (dict(top_p=NAN), -2),
+    (dict(min_p=1.5), -2),
+    (dict(V=0), -2),
+    (dict(K=200), -2),
+    (dict(u=NUL), -1),
+    (dict(drafts=NUL), -1),
+    (dict(acc=NUL), -1),
+    (dict(u=ctypes.c_void_p(0x10002)), -3),
+    (dict(x=MIS), -3),
+])
+def test_sampled_verify_rejects_bad_arguments(lib, kw, code):
+    a = dict(x=A, W=A2, s=A3, K=512, drafts=A, n_draft=3, V=4096, temp=1.0, top_k=0, top_p=1.0, min_p=0.0,
+             u=A2, acc=A, nxt=A2)
+    a.update(kw)
+    rc = lib.lmhead_verify_sampled(a["x"], a["W"], a["s"], a["K"], a["drafts"], a["n_draft"], a["V"], a["temp"],
+                                   a["top_k"], a["top_p"], a["min_p"], a["u"], a["acc"], a["nxt"], None)
+    assert rc == code
+
+
+@nogpu
+def test_sampling_dist_rejects_bad_arguments(lib):
+    assert lib.lmhead_sampling_dist(A, A2, A3, 512, 4, 4096, 1.0, 0, 1.0, 0.0, NUL, A, None) == -1
+    assert lib.lmhead_sampling_dist(A, A2, A3, 512, 9, 4096, 1.0, 0, 1.0, 0.0, A, A2, None) == -2
+    assert lib.lmhead_sampling_dist(A, A2, A3, 512, 4, 4096, 1.0, 0, 1.0, 0.0, A, ctypes.c_void_p(0x20001),
+                                    None) == -3
+
+
+@nogpu
+def test_rescored_rejects_bad_arguments(lib):
+    assert lib.lmhead_verify_rescored(A, A2, A3, NUL, 512, A, 3, 16, 4096, A, A2, None) == -1
+    assert lib.lmhead_verify_rescored(A, A2, A3, A, 512, A, 3, 65, 4096, A, A2, None) == -2
+    assert lib.lmhead_verify_rescored(A, A2, A3, A, 512, A, 3, 16, 8, A, A2, None) == -2
+    assert lib.lmhead_verify_rescored(A, A2, A3, MIS, 512, A, 3, 16, 4096, A, A2, None) == -3
+    assert lib.lmhead_argmax_rescored(A, A2, A3, A, 512, 9, 16, 4096, A, A2, None) == -2
