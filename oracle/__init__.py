@@ -339,18 +339,23 @@ def draft_list_add(dl: DraftList, tokens) -> DraftList:
 #    norm(max(0, p - q)) is p with d removed and renormalised.
 #  * llama.cpp's order is top-k, top-p, min-p, then temperature: top-p and
 #    min-p see the temperature-1 distribution of the surviving candidates.
-#  * All arithmetic is fp32 in a fixed order (the kernel's precision): with
-#    m the best logit and d_j = l_j - m,
+#  * All arithmetic is fp32 in a fixed order (the kernel's precision).
+#    Running sums over the (at most 32) candidates, best first, are the
+#    inclusive prefix sums of a 32-slot scan that adds, for d = 1, 2, 4, 8,
+#    16 in turn, slot j - d into slot j (slots past the candidates taking
+#    part hold 0); a total is the last candidate's prefix sum.  With m the
+#    best logit and d_j = l_j - m,
 #      top-p keeps the shortest prefix whose running sum of exp(d_j) reaches
 #      top_p times the sum over the candidates (all of them if rounding
 #      never reaches it);
 #      min-p keeps the prefix of candidates with exp(d_j) >= min_p (the best
 #      one always);
-#      the weights are w_j = exp(d_j / temperature), W their sum in order;
+#      the weights are w_j = exp(d_j / temperature), W their total;
 #      accept iff u_accept * W < w_d;
-#      a sample walks the candidates best first, running sum c, and takes
-#      the first with u_sample * W' < c (W' the sum over the candidates it
-#      may take; the last of them if rounding never gets there).
+#      a sample takes the first candidate (best first) whose running sum c
+#      over the candidates it may take (the rejected draft's weight set to
+#      0) satisfies u_sample * W' < c, W' their total (the last of them if
+#      rounding never gets there).
 #  * temperature <= 0 is greedy: the distribution is the point mass on the
 #    best candidate.
 #  * Row i uses the uniforms u[2 i] (accept) and u[2 i + 1] (sample), each
@@ -398,11 +403,20 @@ def _f32(v):
     return np.float32(v)
 
 
+def _scan32_f32(vals):
+    """Inclusive prefix sums of up to 32 fp32 values in the scan order:
+    for d = 1, 2, 4, 8, 16, slot j += slot j - d (all slots at once)."""
+    c = np.zeros(SAMPLE_KEEP, np.float32)
+    c[:len(vals)] = np.asarray(vals, np.float32)
+    for d in (1, 2, 4, 8, 16):
+        prev = c.copy()
+        c[d:] = (prev[d:] + prev[:-d]).astype(np.float32)
+    return c[:len(vals)]
+
+
 def _sum_f32(vals):
-    s = _f32(0.0)
-    for v in vals:
-        s = _f32(s + _f32(v))
-    return s
+    """Total of up to 32 fp32 values in the scan order."""
+    return _f32(_scan32_f32(vals)[-1]) if len(vals) else _f32(0.0)
 
 
 def sampling_dist(vals, ids, temperature, top_k=0, top_p=1.0, min_p=0.0, sel_gap=np.inf) -> SamplingDist:
@@ -425,14 +439,15 @@ def sampling_dist(vals, ids, temperature, top_k=0, top_p=1.0, min_p=0.0, sel_gap
     e = np.exp(d).astype(np.float32)
     cut_margin = np.inf
     if top_p < 1.0:
-        S = _sum_f32(e[:n])
+        cs = _scan32_f32(e[:n])
+        S = cs[n - 1]
         thr = _f32(_f32(top_p) * S)
         c = _f32(0.0)
         prev = _f32(0.0)
         keep = n
         for j in range(n):
             prev = c
-            c = _f32(c + e[j])
+            c = cs[j]
             if c >= thr:
                 keep = j + 1
                 break
@@ -463,12 +478,16 @@ def sample_from(dist: SamplingDist, u, exclude=None):
     order = [j for j in range(dist.ids.size) if j != exclude]
     if not order:
         return int(dist.ids[exclude]), exclude, np.inf
-    Wx = _sum_f32(dist.w[order])
+    wx = dist.w.copy()
+    if exclude is not None:
+        wx[exclude] = 0.0
+    cs = _scan32_f32(wx)
+    Wx = cs[-1]
     target = _f32(_f32(u) * Wx)
     c = _f32(0.0)
     for j in order:
         lo = c
-        c = _f32(c + dist.w[j])
+        c = cs[j]
         if target < c:
             margin = min(float(c - target), float(target - lo) if j != order[0] else np.inf) / float(Wx)
             return int(dist.ids[j]), j, margin

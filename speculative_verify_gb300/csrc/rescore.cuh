@@ -11,14 +11,14 @@
 //     [T][V];
 //  2. slicemax_kernel: the largest (logit, id) key of every 128-row slice of
 //     V, per verify row;
-//  3. rescore_kernel, grid (ceil(k / 16), T): with tau the k-th largest of
-//     the row's slice maxima, k slices hold a key >= tau, so the row's k best
-//     keys are all >= tau and lie in the k slices whose maximum is >= tau.
-//     Every CTA of the row finds tau (warp sorts and merges of the maxima),
-//     re-reads those k slices, keeps their keys >= tau (at most 128 k),
-//     sorts them, and rescores its share of the k best: fp32 dot products of
-//     their bf16 rows with x.  The last CTA of the grid takes each row's
-//     argmax (lowest id on ties) and runs the greedy verify.
+//  3. rescore_kernel, grid (ceil(k / 16), T): with tau a threshold that at
+//     least k slice maxima reach, the row's k best keys are all >= tau and
+//     lie in the slices whose maximum is >= tau.  Every CTA of the row finds
+//     such a tau reached by at most 64 slices (select_row), re-reads those
+//     slices, keeps their keys >= tau (at most 128 per slice), sorts them,
+//     and rescores its share of the k best: fp32 dot products of their bf16
+//     rows with x.  The last CTA of the grid takes each row's argmax (lowest
+//     id on ties) and runs the greedy verify.
 #pragma once
 
 #include <cstdint>
@@ -36,6 +36,16 @@ constexpr int RS_PER_CTA = RS_WARPS;             // candidates rescored per CTA 
 constexpr int RS_SEL_MAX = RS_KMAX * RS_SLICE;   // keys >= tau, worst case
 
 __device__ __forceinline__ unsigned long long kmax(unsigned long long a, unsigned long long b) { return a > b ? a : b; }
+
+// Largest 64-bit key across the warp: the largest high word, then the
+// largest low word among the lanes holding it (two 32-bit reductions).
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v)
+{
+    const unsigned hi = static_cast<unsigned>(v >> 32);
+    const unsigned mh = __reduce_max_sync(0xFFFFFFFFu, hi);
+    const unsigned lo = __reduce_max_sync(0xFFFFFFFFu, hi == mh ? static_cast<unsigned>(v) : 0u);
+    return (static_cast<unsigned long long>(mh) << 32) | lo;
+}
 
 // Bitonic sort, descending, of the 128 keys a warp holds as v[i] = element
 // i*32 + lane.
@@ -145,8 +155,7 @@ __global__ void __launch_bounds__(RS_THREADS) slicemax_kernel(const __grid_const
             const int r = v0 + i * 32 + lane;
             if (r < p.V) m = kmax(m, make_key(f[t][i], static_cast<uint32_t>(r)));
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = kmax(m, shfl_xor_u64(m, o));
+        m = warp_max_u64(m);
         if (lane == 0) p.smax[static_cast<size_t>(t) * p.nS + sl] = m;
     }
 }
@@ -159,50 +168,49 @@ struct SelectSmem {
     unsigned n_sel, n_sl;
 };
 
-// The k best (logit, id) keys of one row, descending, into sel[0..k) (keys
-// past the row's candidates are 0), by the whole CTA; sel holds RS_SEL_MAX
-// keys.  mx: the row's nS slice maxima; row: its V fp32 logits.  With tau
-// the k-th largest slice maximum, k slices hold a key >= tau, so the row's
-// k best keys are >= tau and lie in the (at most k) slices whose maximum is
-// >= tau; at most 128 k keys are gathered and sorted.
-__device__ __forceinline__ void select_row(const unsigned long long *mx, const float *row, int nS, int V, int k,
-                                           unsigned long long *sel, SelectSmem &sm)
+// Exact threshold: the k-th largest of the nS slice maxima mx (k <= 64),
+// by the whole CTA.  Each warp keeps the 64 best maxima of its chunks of
+// 128 (register sort, then merge), the warps' lists are merged pairwise in
+// a tree.  Ends with __syncthreads; the result is in sm.tau.
+__device__ __forceinline__ void exact_tau(const unsigned long long *mx, int nS, int k, SelectSmem &sm)
 {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (tid == 0) {
-        sm.n_sel = 0u;
-        sm.n_sl = 0u;
-    }
-    // tau: each warp keeps the 64 best maxima of its chunks of 128, then
-    // warp 0 merges the warps' lists
-    {
-        unsigned long long a0 = 0ull, a1 = 0ull;
-        for (int c = warp; c * RS_SLICE < nS; c += RS_WARPS) {
-            unsigned long long v[4];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    unsigned long long a0 = 0ull, a1 = 0ull;
+    for (int c = warp; c * RS_SLICE < nS; c += RS_WARPS) {
+        unsigned long long v[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int s = c * RS_SLICE + i * 32 + lane;
-                v[i] = s < nS ? __ldcg(mx + s) : 0ull;
-            }
-            warp_sort128_desc(v, lane);
-            warp_merge64_desc(a0, a1, v[0], v[1], lane);
+        for (int i = 0; i < 4; ++i) {
+            const int s = c * RS_SLICE + i * 32 + lane;
+            v[i] = s < nS ? __ldcg(mx + s) : 0ull;
         }
-        sm.wl[warp][lane] = a0;
-        sm.wl[warp][32 + lane] = a1;
+        warp_sort128_desc(v, lane);
+        warp_merge64_desc(a0, a1, v[0], v[1], lane);
     }
-    __syncthreads();
+    sm.wl[warp][lane] = a0;
+    sm.wl[warp][32 + lane] = a1;
+#pragma unroll
+    for (int st = 1; st < RS_WARPS; st <<= 1) {
+        __syncthreads();
+        if ((warp & (2 * st - 1)) == 0) {
+            warp_merge64_desc(a0, a1, sm.wl[warp + st][lane], sm.wl[warp + st][32 + lane], lane);
+            sm.wl[warp][lane] = a0;
+            sm.wl[warp][32 + lane] = a1;
+        }
+    }
     if (warp == 0) {
-        unsigned long long a0 = sm.wl[0][lane], a1 = sm.wl[0][32 + lane];
-        for (int w = 1; w < RS_WARPS; ++w) warp_merge64_desc(a0, a1, sm.wl[w][lane], sm.wl[w][32 + lane], lane);
         const int kk = k - 1;
         const unsigned long long tk = shfl_u64(kk < 32 ? a0 : a1, kk & 31);
         if (lane == 0) sm.tau = tk;
     }
     __syncthreads();
-    // the (at most k) slices whose maximum is >= tau; with fewer than k
-    // slices tau is 0 and every slice qualifies
+}
+
+// The slices whose maximum is >= sm.tau into sm.slist (their number, which
+// may exceed RS_KMAX, in sm.n_sl).  Ends with __syncthreads.
+__device__ __forceinline__ void list_slices(const unsigned long long *mx, int nS, SelectSmem &sm)
+{
     const unsigned long long tau = sm.tau;
-    for (int s = tid; s < nS; s += RS_THREADS) {
+    for (int s = threadIdx.x; s < nS; s += RS_THREADS) {
         const unsigned long long m = __ldcg(mx + s);
         if (m != 0ull && m >= tau) {
             const unsigned at = atomicAdd(&sm.n_sl, 1u);
@@ -210,30 +218,135 @@ __device__ __forceinline__ void select_row(const unsigned long long *mx, const f
         }
     }
     __syncthreads();
-    // their keys >= tau (the order of sel is fixed below by sorting)
-    const int nsl = min(static_cast<int>(sm.n_sl), RS_KMAX);
-    for (int j = warp; j < nsl; j += RS_WARPS) {
-        const int v0 = sm.slist[j] * RS_SLICE;
+}
+
+// The k best (logit, id) keys of one row (k <= 64), descending, into
+// sel[0..k) (keys past the row's candidates are 0), by the whole CTA; sel
+// holds RS_SEL_MAX keys.  mx: the row's nS slice maxima; row: its V fp32
+// logits.  Any tau with at least k slice maxima >= tau is a valid
+// threshold: the row's k best keys are then >= tau, and each lies in a
+// slice whose maximum is >= tau.  The first try takes the k-th best of the
+// warps' m best maxima (one chunk of 128 per warp; m = 4 for k <= 32, else
+// 8); if more than RS_KMAX slices reach it, tau becomes the exact k-th
+// largest maximum, which exactly k slices reach.  The keys >= tau of those
+// slices (at most 128 per slice) are gathered and put in order.
+__device__ __forceinline__ void select_row(const unsigned long long *mx, const float *row, int nS, int V, int k,
+                                           unsigned long long *sel, SelectSmem &sm)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) {
+        sm.n_sel = 0u;
+        sm.n_sl = 0u;
+        sm.tau = 0ull;
+    }
+    bool exact = nS > RS_WARPS * RS_SLICE;
+    if (!exact) {
+        unsigned long long *top = &sm.wl[0][0];          // [RS_WARPS * 8]
+        unsigned long long kv[4], v[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const int r = v0 + i * 32 + lane;
-            const unsigned long long key = r < V ? make_key(__ldcg(row + r), static_cast<uint32_t>(r)) : 0ull;
+            const int s = warp * RS_SLICE + i * 32 + lane;
+            kv[i] = s < nS ? __ldcg(mx + s) : 0ull;
+            v[i] = kv[i];
+        }
+        const int rounds = k <= 32 ? 4 : 8;
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+            unsigned long long m = 0ull;
+            if (r < rounds) {
+                m = warp_max_u64(kmax(kmax(v[0], v[1]), kmax(v[2], v[3])));
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if (v[i] == m) v[i] = 0ull;           // keys are unique (0: none left)
+            }
+            if (lane == 0) top[warp * 8 + r] = m;
+        }
+        __syncthreads();
+        // tau: the one of the 128 whose rank is k - 1 (stays 0 if fewer
+        // than k are nonzero)
+        if (tid < RS_WARPS * 8) {
+            const unsigned long long key = top[tid];
+            int rank = 0;
+            for (int j = 0; j < RS_WARPS * 8; ++j) rank += top[j] > key;
+            if (key != 0ull && rank == k - 1) sm.tau = key;
+        }
+        __syncthreads();
+        // the slices that reach tau, from the maxima still in registers
+        const unsigned long long tau = sm.tau;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int s = warp * RS_SLICE + i * 32 + lane;
+            const bool in = s < nS && kv[i] != 0ull && kv[i] >= tau;
+            const unsigned bal = __ballot_sync(0xFFFFFFFFu, in);
+            if (bal) {
+                unsigned base = 0u;
+                if (lane == 0) base = atomicAdd(&sm.n_sl, static_cast<unsigned>(__popc(bal)));
+                base = __shfl_sync(0xFFFFFFFFu, base, 0);
+                const unsigned at = base + __popc(bal & ((1u << lane) - 1u));
+                if (in && at < static_cast<unsigned>(RS_KMAX)) sm.slist[at] = s;
+            }
+        }
+        __syncthreads();
+        if (sm.n_sl > static_cast<unsigned>(RS_KMAX)) {
+            exact = true;
+            __syncthreads();
+            if (tid == 0) sm.n_sl = 0u;
+        }
+    }
+    if (exact) {
+        exact_tau(mx, nS, k, sm);
+        list_slices(mx, nS, sm);
+    }
+    // the keys >= tau of the listed slices, two slices per warp in flight
+    const unsigned long long tau = sm.tau;
+    const int nsl = min(static_cast<int>(sm.n_sl), RS_KMAX);
+    for (int j0 = warp; j0 < nsl; j0 += 2 * RS_WARPS) {
+        float f[8];
+        int r0[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int j = j0 + h * RS_WARPS;
+            r0[h] = j < nsl ? sm.slist[j] * RS_SLICE : V;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int r = r0[h] + i * 32 + lane;
+                f[h * 4 + i] = r < V ? __ldcg(row + r) : 0.f;
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int r = r0[q >> 2] + (q & 3) * 32 + lane;
+            const unsigned long long key = r < V ? make_key(f[q], static_cast<uint32_t>(r)) : 0ull;
             const bool keep = key != 0ull && key >= tau;
             const unsigned bal = __ballot_sync(0xFFFFFFFFu, keep);
-            unsigned base = 0u;
-            if (lane == 0 && bal) base = atomicAdd(&sm.n_sel, static_cast<unsigned>(__popc(bal)));
-            base = __shfl_sync(0xFFFFFFFFu, base, 0);
-            const unsigned at = base + __popc(bal & ((1u << lane) - 1u));
-            if (keep && at < static_cast<unsigned>(RS_SEL_MAX)) sel[at] = key;
+            if (bal) {
+                unsigned base = 0u;
+                if (lane == 0) base = atomicAdd(&sm.n_sel, static_cast<unsigned>(__popc(bal)));
+                base = __shfl_sync(0xFFFFFFFFu, base, 0);
+                const unsigned at = base + __popc(bal & ((1u << lane) - 1u));
+                if (keep && at < static_cast<unsigned>(RS_SEL_MAX)) sel[at] = key;
+            }
         }
     }
     __syncthreads();
     const int ns = min(static_cast<int>(sm.n_sel), RS_SEL_MAX);
-    int npad = 1;
-    while (npad < ns || npad < k) npad <<= 1;
-    for (int i = ns + tid; i < npad; i += RS_THREADS) sel[i] = 0ull;
-    __syncthreads();
-    cta_sort_desc(sel, npad);
+    if (ns <= RS_THREADS) {
+        // keys are unique: each goes to its rank (the number of larger ones)
+        const unsigned long long key = tid < ns ? sel[tid] : 0ull;
+        int rank = 0;
+        if (tid < ns)
+            for (int j = 0; j < ns; ++j) rank += sel[j] > key;
+        __syncthreads();
+        if (tid < ns) sel[rank] = key;
+        for (int j = ns + tid; j < k; j += RS_THREADS) sel[j] = 0ull;
+        __syncthreads();
+    } else {
+        int npad = 1;
+        while (npad < ns || npad < k) npad <<= 1;
+        for (int i = ns + tid; i < npad; i += RS_THREADS) sel[i] = 0ull;
+        __syncthreads();
+        cta_sort_desc(sel, npad);
+    }
 }
 
 struct RescoreParams {
@@ -406,18 +519,36 @@ struct SampleParams {
     unsigned *done;                      // scratch counter, left at 0
 };
 
+// Inclusive prefix sums across the warp (lane j: sum of lanes 0..j), in
+// the order: for d = 1, 2, 4, 8, 16, lane j adds lane j - d.
+__device__ __forceinline__ float warp_scan_f32(float v, int lane)
+{
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const float o = __shfl_up_sync(0xFFFFFFFFu, v, d);
+        if (lane >= d) v = v + o;
+    }
+    return v;
+}
+
 // One CTA per verify row.  Dynamic shared memory: RS_SEL_MAX keys.
 __global__ void __launch_bounds__(RS_THREADS) sample_kernel(const __grid_constant__ SampleParams p)
 {
     extern __shared__ __align__(16) unsigned long long sel[];
     __shared__ SelectSmem sm;
-    __shared__ float es[SAMPLE_KEEP], ds[SAMPLE_KEEP], ws[SAMPLE_KEEP];
-    __shared__ int ids[SAMPLE_KEEP];
-    __shared__ int n_keep;
-    __shared__ float Wsum;
     __shared__ unsigned is_last;
     const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
     pdl_wait_prior();                    // logits and slice maxima come from the passes before
+    const bool verify = p.mode == 0;
+    const bool draft_row = verify && t < p.T - 1;
+    // the row's inputs, loaded now so that they arrive during the selection
+    int dr = -1;
+    float u_acc = 0.f, u_smp = 0.f;
+    if (tid < 32 && verify) {
+        if (draft_row) dr = p.drafts[t];
+        u_acc = p.u[2 * t];
+        u_smp = p.u[2 * t + 1];
+    }
     const int keep = min(SAMPLE_KEEP, p.V);
     select_row(p.smax + static_cast<size_t>(t) * p.nS, p.logits + static_cast<size_t>(t) * p.V, p.nS, p.V, keep,
                sel, sm);
@@ -425,113 +556,74 @@ __global__ void __launch_bounds__(RS_THREADS) sample_kernel(const __grid_constan
         // the chain, by warp 0: lane j holds candidate j
         const unsigned long long key = lane < keep ? sel[lane] : 0ull;
         const float l = key ? key_value(key) : 0.f;
-        ids[lane] = key ? key_id(key) : -1;
+        const int id = key ? key_id(key) : -1;
         const float m = __shfl_sync(0xFFFFFFFFu, l, 0);
         const float d = l - m;
-        es[lane] = expf(d);
-        ds[lane] = d;
-        __syncwarp();
-        if (lane == 0) {
-            int n = keep;
-            if (p.top_k > 0) n = min(n, p.top_k);
-            if (p.temperature > 0.f) {
-                if (p.top_p < 1.f) {
-                    float S = 0.f;
-                    for (int j = 0; j < n; ++j) S = S + es[j];
-                    const float thr = p.top_p * S;
-                    float c = 0.f;
-                    for (int j = 0; j < n; ++j) {
-                        c = c + es[j];
-                        if (c >= thr) {
-                            n = j + 1;
-                            break;
-                        }
-                    }
-                }
-                if (p.min_p > 0.f) {
-                    int k = 1;
-                    while (k < n && es[k] >= p.min_p) ++k;
-                    n = k;
-                }
-            } else {
-                n = 1;
+        int n = keep;
+        if (p.top_k > 0) n = min(n, p.top_k);
+        float w;
+        if (p.temperature > 0.f) {
+            const float e = lane < n ? expf(d) : 0.f;
+            if (p.top_p < 1.f) {
+                const float c = warp_scan_f32(e, lane);
+                const float thr = p.top_p * __shfl_sync(0xFFFFFFFFu, c, n - 1);
+                const unsigned hit = __ballot_sync(0xFFFFFFFFu, lane < n && c >= thr);
+                if (hit) n = __ffs(hit);
             }
-            n_keep = n;
+            if (p.min_p > 0.f) {
+                const unsigned low = __ballot_sync(0xFFFFFFFFu, lane >= 1 && lane < n && !(e >= p.min_p));
+                if (low) n = __ffs(low) - 1;
+            }
+            w = lane < n ? expf(d / p.temperature) : 0.f;
+        } else {
+            n = 1;
+            w = lane == 0 ? 1.f : 0.f;
         }
-        __syncwarp();
-        const int n = n_keep;
-        if (lane < n) ws[lane] = p.temperature > 0.f ? expf(ds[lane] / p.temperature) : 1.f;
-        __syncwarp();
-        if (lane == 0) {
-            float W = 0.f;
-            for (int j = 0; j < n; ++j) W = W + ws[j];
-            Wsum = W;
-        }
-        __syncwarp();
-        if (p.mode == 1) {
-            p.out_ids[t * SAMPLE_KEEP + lane] = lane < n ? ids[lane] : -1;
-            p.out_probs[t * SAMPLE_KEEP + lane] = lane < n ? ws[lane] / Wsum : 0.f;
-        } else if (lane == 0) {
-            const bool draft_row = t < p.T - 1;
-            int jd = -1;
-            int acc = 0;
-            if (draft_row) {
-                const int dr = p.drafts[t];
-                for (int j = 0; j < n; ++j)
-                    if (ids[j] == dr) {
-                        jd = j;
-                        break;
-                    }
-                acc = (jd >= 0 && p.u[2 * t] * Wsum < ws[jd]) ? 1 : 0;
+        const float W = __shfl_sync(0xFFFFFFFFu, warp_scan_f32(w, lane), n - 1);
+        if (!verify) {
+            p.out_ids[t * SAMPLE_KEEP + lane] = lane < n ? id : -1;
+            p.out_probs[t * SAMPLE_KEEP + lane] = lane < n ? w / W : 0.f;
+        } else {
+            // the draft's position among the kept candidates, the accept
+            // test, then the draw from the candidates other than it (all of
+            // them on the last row); with none left the draft itself (it
+            // was then accepted with probability 1)
+            const unsigned at = __ballot_sync(0xFFFFFFFFu, draft_row && lane < n && id == dr);
+            const int jd = at ? __ffs(at) - 1 : -1;
+            const float w_d = __shfl_sync(0xFFFFFFFFu, w, jd >= 0 ? jd : 0);
+            const int acc = (jd >= 0 && u_acc * W < w_d) ? 1 : 0;
+            const float wx = lane == jd ? 0.f : w;
+            const float cx = warp_scan_f32(wx, lane);
+            const float Wx = __shfl_sync(0xFFFFFFFFu, cx, n - 1);
+            const float target = u_smp * Wx;
+            const unsigned may = __ballot_sync(0xFFFFFFFFu, lane < n && lane != jd);
+            const unsigned below = __ballot_sync(0xFFFFFFFFu, lane < n && lane != jd && target < cx);
+            int pick = below ? __ffs(below) - 1 : (may ? 31 - __clz(may) : jd);
+            const int tok = __shfl_sync(0xFFFFFFFFu, id, pick);
+            if (lane == 0) {
+                p.row_acc[t] = acc;
+                p.row_tok[t] = tok;
             }
-            // the draw from the candidates other than jd (all of them on the
-            // last row); with none left the draft itself (then it was
-            // accepted with probability 1)
-            float Wx = 0.f;
-            int last = -1;
-            for (int j = 0; j < n; ++j)
-                if (j != jd) {
-                    Wx = Wx + ws[j];
-                    last = j;
-                }
-            int tok = jd >= 0 ? ids[jd] : ids[0];
-            if (last >= 0) {
-                const float target = p.u[2 * t + 1] * Wx;
-                float c = 0.f;
-                int pick = last;
-                for (int j = 0; j < n; ++j) {
-                    if (j == jd) continue;
-                    c = c + ws[j];
-                    if (target < c) {
-                        pick = j;
-                        break;
-                    }
-                }
-                tok = ids[pick];
-            }
-            p.row_acc[t] = acc;
-            p.row_tok[t] = tok;
         }
     }
-    if (p.mode == 1) return;
+    if (!verify) return;
     __syncthreads();
     if (tid == 0) {
         __threadfence();
         is_last = atomicAdd(p.done, 1u) == gridDim.x - 1u;
     }
     __syncthreads();
-    if (!is_last || tid != 0) return;
+    if (!is_last || tid >= 32) return;
     __threadfence();
     const int n_draft = p.T - 1;
-    int acc = n_draft;
-    for (int i = 0; i < n_draft; ++i)
-        if (!__ldcg(&p.row_acc[i])) {
-            acc = i;
-            break;
-        }
-    p.accept_len[0] = acc;
-    p.next_token[0] = __ldcg(&p.row_tok[acc]);
-    *p.done = 0u;                        // ready for the next call
+    const bool rejected = lane < n_draft && !__ldcg(&p.row_acc[lane]);
+    const unsigned rej = __ballot_sync(0xFFFFFFFFu, rejected);
+    const int acc = rej ? __ffs(rej) - 1 : n_draft;
+    if (lane == 0) {
+        p.accept_len[0] = acc;
+        p.next_token[0] = __ldcg(&p.row_tok[acc]);
+        *p.done = 0u;                    // ready for the next call
+    }
 }
 
 }  // namespace sv

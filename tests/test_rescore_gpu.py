@@ -135,3 +135,24 @@ def test_rescored_candidates_clustered_in_one_slice(sv, oracle):
     ids, vals = sv.lmhead_argmax_rescored(dev16(x), dev32(Wq), dev16(sc), dev16(Wbf), top_k=k)
     torch.cuda.synchronize()
     check_rows(ids.cpu().numpy(), vals.cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("k", [16, 64])
+def test_rescored_maxima_clustered_in_one_chunk(sv, oracle, k):
+    """Rows 0..16383 (the slices of the first chunk of 128 slice maxima) get
+    8x the scales: the first threshold (the k-th best of every chunk's 8
+    best maxima) is then reached by far more than 64 slices and the exact
+    threshold must take over."""
+    rng = np.random.default_rng(900 + k)
+    V, K, T = 248320, 256, 2
+    Wq, sc = gen.weights(rng, V, K)
+    f = (sc.astype(np.uint32) << 16).view(np.float32).copy()
+    f[:16384] *= 8.0
+    sc = gen.f32_to_bf16_bits(f)
+    Wbf = bf16_head(rng, V, K)
+    x = gen.activations(rng, T, K)
+    ref = oracle.lmhead_verify_rescored(x, Wq, sc, Wbf, K, V, np.zeros(T - 1, np.int32), k)
+    assert all(c < 16384 for c in ref.cand[0].tolist())
+    ids, vals = sv.lmhead_argmax_rescored(dev16(x), dev32(Wq), dev16(sc), dev16(Wbf), top_k=k)
+    torch.cuda.synchronize()
+    check_rows(ids.cpu().numpy(), vals.cpu().numpy(), ref)

@@ -58,7 +58,7 @@ def chain_args(c):
 
 
 @pytest.mark.parametrize("V,K,T,seed", [(3000, 256, 3, 1), (20000, 1024, 8, 2), (20, 128, 2, 3),
-                                        (7001, 640, 1, 4)])
+                                        (7001, 640, 1, 4), (300000, 128, 2, 5)])
 @pytest.mark.parametrize("ci", range(len(CHAINS)))
 def test_sampling_distribution_matches_oracle(sv, oracle, V, K, T, seed, ci):
     chain = CHAINS[ci]
@@ -194,3 +194,33 @@ def test_sampled_verify_full_size_head(sv, oracle):
             clear += 1
             assert (int(acc.item()), int(nxt.item())) == (ref.accept_len, ref.next_token)
     assert clear >= 4
+
+
+def test_sampling_distribution_with_maxima_clustered_in_one_chunk(sv, oracle):
+    """Rows 0..16383 get 8x the scales, so the row's 32 best logits all sit
+    in the first chunk of slice maxima: the exact threshold takes over."""
+    V, K, T = 248320, 256, 2
+    rng = np.random.default_rng(51)
+    Wq, sc = gen.weights(rng, V, K)
+    f = (sc.astype(np.uint32) << 16).view(np.float32).copy()
+    f[:16384] *= 8.0
+    sc = gen.f32_to_bf16_bits(f)
+    x = gen.activations(rng, T, K)
+    logits = oracle.lmhead_logits(x, Wq, sc, K, T, V)
+    ref = oracle.verify_sampled_from_logits(logits, np.zeros(T - 1, np.int32), np.zeros(2 * T), temperature=1.0)
+    ids, probs = sv.lmhead_sampling_dist(dev16(x), dev32(Wq), dev16(sc), 1.0, 0, 1.0, 0.0)
+    torch.cuda.synchronize()
+    ids, probs = ids.cpu().numpy(), probs.cpu().numpy()
+    checked = 0
+    for t in range(T):
+        d = ref.dists[t]
+        assert all(c < 16384 for c in d.ids.tolist())
+        if not d.cut_clear(1e-4, 1e-3):
+            continue
+        got = dict(zip(ids[t].tolist(), probs[t].tolist()))
+        want = dict(zip(d.ids.tolist(), (d.w / d.W).tolist()))
+        assert set(got) == set(want)
+        for k, v in want.items():
+            assert abs(got[k] - v) <= 1e-4
+        checked += 1
+    assert checked >= 1
