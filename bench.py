@@ -11,7 +11,7 @@ that model; the step streams 820 MB, more than the 129 MB L2, so every kernel
 reads its weights from HBM.
 
 Usage: python bench.py [--gpus N --steps K --warmup W] [--impl reference]
-                       [--ncu-case head|gemm] [--breakdown]
+                       [--ncu-case head|gemm|sampled|rescored] [--breakdown]
 One JSON line on stdout (rank 0).
 """
 from __future__ import annotations
@@ -616,14 +616,23 @@ def run_ncu_case(args):
     device = torch.device("cuda", 0)
     rng = np.random.default_rng(5)
     dev = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a).view(dt)).to(device)
-    if args.ncu_case == "head":
+    if args.ncu_case in ("head", "sampled", "rescored"):
         V, K, T = gen.VOCAB, gen.HIDDEN, T_STEP
         Wq, sc = gen.weights(rng, V, K)
         Wd, sd = dev(Wq, np.int32), dev(sc, np.int16)
         x = dev(gen.activations(rng, T, K), np.int16)
         drafts = torch.zeros(T - 1, dtype=torch.int32, device=device)
-        for _ in range(3):
-            sv.lmhead_verify(x, Wd, sd, drafts)
+        if args.ncu_case == "head":
+            for _ in range(3):
+                sv.lmhead_verify(x, Wd, sd, drafts)
+        elif args.ncu_case == "sampled":
+            u = torch.rand(2 * T, dtype=torch.float32, device=device)
+            for _ in range(3):
+                sv.lmhead_verify_sampled(x, Wd, sd, drafts, u, temperature=0.7, top_k=20, top_p=0.95)
+        else:
+            Wbf = (torch.randn((V, K), dtype=torch.float32, device=device) * 0.02).to(torch.bfloat16)
+            for _ in range(3):
+                sv.lmhead_verify_rescored(x, Wd, sd, Wbf, drafts, top_k=16)
     else:
         label, K, N = gen.GEMM_SHAPES[1]
         Wq, sc = gen.weights(rng, N, K)
@@ -644,7 +653,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--breakdown", action="store_true", help="also time each kernel alone at T=1..32")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--ncu-case", choices=["head", "gemm"], default=None)
+    ap.add_argument("--ncu-case", choices=["head", "gemm", "sampled", "rescored"], default=None)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
