@@ -45,6 +45,25 @@ N_DRAFT = 3
 # helpers
 
 
+def reduce_max(dist, x, device=None):
+    """The largest x over all ranks (a whole-job time is the slowest rank's);
+    x itself when there is no process group.  NCCL reduces a device tensor,
+    gloo a host one."""
+    if dist is None:
+        return float(x)
+    import torch
+    dev = device if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(world, bytes_per_step, steps, ms):
+    """Whole-job throughput (weak scaling: every rank streams one step's
+    bytes per step) over the slowest rank's time `ms` for `steps` steps."""
+    return world * bytes_per_step * steps / (ms * 1e-3) / 1e9
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -421,10 +440,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     barrier()
     head_ms = float(np.mean([a.elapsed_time(b) for a, b in zip(ev_mid, ev_end)]))
-    if dist is not None:
-        t = torch.tensor([ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = reduce_max(dist, ms, device)
     assert sv.last_device_error() == 0
 
     # end to end through the public API with host buffers: per step the
@@ -450,10 +466,7 @@ def run_ours(args, rank, world, local_rank):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = reduce_max(dist, e2e_ms, device)
 
     breakdown = per_kernel_breakdown(torch, sv, device, stream) if args.breakdown else None
 
@@ -461,7 +474,7 @@ def run_ours(args, rank, world, local_rank):
         return
     peak, peak_kind = measured_peaks()
     ms_per_step = ms / args.steps
-    value = world * wl.bytes_per_step * args.steps / (ms * 1e-3) / 1e9
+    value = job_gbs(world, wl.bytes_per_step, args.steps, ms)
     achieved = wl.head["bytes"] / (head_ms * 1e-3) / 1e9
     clocks = sampler.summary(t_host0, t_host1)
     cpu = cpu_baseline(wl.host) if (world == 1 and not args.no_cpu_baseline) else None
@@ -486,7 +499,7 @@ def run_ours(args, rank, world, local_rank):
                      "avg_launch_ms": head_ms,
                      "traffic": recorded_traffic("lmhead_verify_T4")},
         "clocks": clocks,
-        "e2e": {"value": wl.bytes_per_step / (e2e_ms * 1e-3) / 1e9 * world, "unit": "GB/s",
+        "e2e": {"value": job_gbs(world, wl.bytes_per_step, 1, e2e_ms), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms, "steps": e2e_steps,
                 "per_step": "one pinned host->device copy of the step's activations and drafts, the "

@@ -274,8 +274,7 @@ int launch(Params p, const DeviceState &st, cudaStream_t stream)
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cudaLaunchConfig_t cfg;
-    std::memset(&cfg, 0, sizeof cfg);
+    cudaLaunchConfig_t cfg = {};
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
@@ -422,7 +421,7 @@ int logits_and_slice_maxima(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 
     if (rc != SV_OK) return rc;
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
-    std::memset(cfg, 0, sizeof *cfg);
+    *cfg = cudaLaunchConfig_t{};
     cfg->blockDim = dim3(RS_THREADS);
     cfg->stream = stream;
     cfg->attrs = attr;
