@@ -249,6 +249,49 @@ __global__ void __launch_bounds__(XP_THREADS) xprep_kernel(const uint16_t *x, in
     if (tid == 0) xinv[t] = __uint_as_float(static_cast<uint32_t>(127 - sh) << 23);
 }
 
+// The consumers' hand-off buffer `red` holds one partial per group slot.
+// One token tile (NT == 1): [slot][ROWS][8 tokens], so that the epilogue
+// reads four tokens of a row with one 16-byte load; wider tiles:
+// [slot][TP tokens][ROWS].
+template <int NT, int GPS>
+__device__ __forceinline__ int red_index(int slot, int tok, int row)
+{
+    return NT == 1 ? (slot * ROWS + row) * 8 + tok : (slot * (8 * NT) + tok) * ROWS + row;
+}
+
+// Sums over the GPS group slots of tokens t0..t0+3 of tile row `row`
+// (pairwise, in a fixed order); tokens >= T give 0.
+template <int NT, int GPS>
+__device__ __forceinline__ float4 slot_sums4(const float *red, int t0, int row, int T)
+{
+    float4 v;
+    if constexpr (NT == 1) {
+        // slots in groups of four: ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7))
+        auto add = [](float4 a, float4 b) { return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w); };
+        auto ld = [&](int sl) { return *reinterpret_cast<const float4 *>(red + red_index<NT, GPS>(sl, t0, row)); };
+        v = add(add(ld(0), ld(1)), add(ld(2), ld(3)));
+#pragma unroll
+        for (int sl = 4; sl < GPS; sl += 4) v = add(v, add(add(ld(sl), ld(sl + 1)), add(ld(sl + 2), ld(sl + 3))));
+    } else {
+        float a[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            float sum = 0.f;
+            if (t0 + j < T) {
+                sum = red[red_index<NT, GPS>(0, t0 + j, row)];
+#pragma unroll
+                for (int sl = 1; sl < GPS; ++sl) sum += red[red_index<NT, GPS>(sl, t0 + j, row)];
+            }
+            a[j] = sum;
+        }
+        v = make_float4(a[0], a[1], a[2], a[3]);
+    }
+    if (t0 + 1 >= T) v.y = 0.f;
+    if (t0 + 2 >= T) v.z = 0.f;
+    if (t0 + 3 >= T) v.w = 0.f;
+    return v;
+}
+
 // Epilogue warp: stage the scales (and, for the head, the token ids) of one
 // tile into shared memory with cp.async, then arrive on `bar` (expected
 // arrivals: 32 cp.async completions + 1 plain arrival).  Rows that do not
@@ -574,19 +617,7 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
                             const int row = lane + 32 * h;
-                            float q[4];
-#pragma unroll
-                            for (int j = 0; j < 4; ++j) {
-                                const int t = t0 + j;
-                                float sum = 0.f;
-                                if (t < T) {
-                                    sum = red[t * ROWS + row];
-#pragma unroll
-                                    for (int sl = 1; sl < C::GPS; ++sl) sum += red[(sl * C::TP + t) * ROWS + row];
-                                }
-                                q[j] = sum;
-                            }
-                            *reinterpret_cast<float4 *>(mine + row * TMAX + t0) = make_float4(q[0], q[1], q[2], q[3]);
+                            *reinterpret_cast<float4 *>(mine + row * TMAX + t0) = slot_sums4<NT, C::GPS>(red, t0, row, T);
                         }
                     }
                     __threadfence();
@@ -618,18 +649,8 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const int row = lane + 32 * h;
-                    float own[4];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int t = t0 + j;
-                        float sum = 0.f;
-                        if (t < T) {
-                            sum = red[t * ROWS + row];
-#pragma unroll
-                            for (int sl = 1; sl < C::GPS; ++sl) sum += red[(sl * C::TP + t) * ROWS + row];
-                        }
-                        own[j] = sum;
-                    }
+                    const float4 o4 = slot_sums4<NT, C::GPS>(red, t0, row, T);
+                    const float own[4] = {o4.x, o4.y, o4.z, o4.w};
                     if (complete) {
 #pragma unroll
                         for (int j = 0; j < 4; ++j) v[j][h] = own[j];
@@ -998,12 +1019,26 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int row = (mset * C::R + r) * 16 + g + 8 * (e >> 1);
-                        const int tok = nt * 8 + 2 * c + (e & 1);
-                        red[(slot * C::TP + tok) * ROWS + row] =
-                            XBF ? acc[r][nt][e] : acc[r][nt][e] * (XRES ? xinv[e & 1] : __ldg(p.xinv + tok));
-                        acc[r][nt][e] = 0.f;
+                    for (int hh = 0; hh < 2; ++hh) {
+                        // tokens 2c and 2c+1 of row g (+8): elements 2hh, 2hh+1
+                        const int row = (mset * C::R + r) * 16 + g + 8 * hh;
+                        const int tok = nt * 8 + 2 * c;
+                        float v0 = acc[r][nt][2 * hh], v1 = acc[r][nt][2 * hh + 1];
+                        if constexpr (XRES) {
+                            v0 *= xinv[0];
+                            v1 *= xinv[1];
+                        } else if constexpr (!XBF) {
+                            v0 *= __ldg(p.xinv + tok);
+                            v1 *= __ldg(p.xinv + tok + 1);
+                        }
+                        if constexpr (NT == 1) {
+                            *reinterpret_cast<float2 *>(red + red_index<NT, C::GPS>(slot, tok, row)) = make_float2(v0, v1);
+                        } else {
+                            red[red_index<NT, C::GPS>(slot, tok, row)] = v0;
+                            red[red_index<NT, C::GPS>(slot, tok + 1, row)] = v1;
+                        }
+                        acc[r][nt][2 * hh] = 0.f;
+                        acc[r][nt][2 * hh + 1] = 0.f;
                     }
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_addr(red_full));
