@@ -100,6 +100,9 @@ def test_gpu_one_hot_pins_nibble_order_and_page_constant(sv, oracle):
     (2, 128, 64),
     (3, 1152, 1000),     # ragged last tile, 9 groups
     (4, 5120, 200),
+    (5, 896, 300),       # uneven warps per token row while staging, 7 groups
+    (6, 1664, 129),
+    (7, 2432, 65),       # a second token chunk with three real tokens, 19 groups
     (8, 2048, 777),
     (9, 640, 130),       # two n8 token tiles
     (13, 1280, 321),
@@ -283,6 +286,9 @@ def test_verify_tiny_configuration(sv, oracle):
     (5000, 768, 3, 1, 1234),     # restricted
     (5000, 768, 0, 1, 1),        # single-entry map
     (6000, 512, 3, 2, 4000),
+    (3333, 896, 4, 1, 0),        # five rows
+    (2049, 1664, 6, 1, 0),       # seven rows
+    (5000, 768, 7, 1, 2000),     # restricted, eight rows
 ])
 def test_verify_matches_oracle(sv, oracle, V, K, n_draft, n_streams, n_map):
     run_head_case(sv, oracle, 900 + V + K + n_draft, V, K, n_draft, n_streams, n_map)
