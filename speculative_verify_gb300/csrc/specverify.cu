@@ -228,8 +228,12 @@ int plan_layout(Params &p, int smem_optin, int *smem_total)
     return off <= smem_optin ? SV_OK : SV_ERR_SHAPE;
 }
 
-// Resident activations pay off when they fit with at least 3 weight stages.
+// Resident activations pay off when they fit with at least 3 weight stages,
+// and when each CTA's share is long enough (at least 6 stages of 8 units) to
+// amortise converting them before its first stage: with shorter shares
+// (QKV-sized GEMMs) the bf16 rows copied into every stage are faster.
 constexpr int XRES_MAX_BYTES = 100 * 1024;
+constexpr int XRES_MIN_UNITS = 48;
 
 template <int NT, bool HEAD, bool GATHER, bool XRES>
 int launch(Params p, const DeviceState &st, cudaStream_t stream)
@@ -305,7 +309,8 @@ template <bool HEAD, bool GATHER>
 int dispatch(Params &p, const DeviceState &st, cudaStream_t stream)
 {
     if (p.T <= 8) {
-        if (static_cast<long long>(p.T + 1) * (2LL * p.K + 16) <= XRES_MAX_BYTES)
+        if (static_cast<long long>(p.T + 1) * (2LL * p.K + 16) <= XRES_MAX_BYTES &&
+            p.U >= static_cast<long long>(XRES_MIN_UNITS) * st.sms)
             return launch<1, HEAD, GATHER, true>(p, st, stream);
         return launch<1, HEAD, GATHER, false>(p, st, stream);
     }

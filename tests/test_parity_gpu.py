@@ -125,6 +125,29 @@ def test_gemm_matches_oracle(sv, oracle, T, K, N):
     assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
 
 
+def resident_rows(K, ragged=17):
+    """A row count whose call keeps the activations resident in shared memory:
+    the kernels convert them once per CTA only when each CTA streams at least
+    48 units (64 rows x one 128-column group); smaller calls copy bf16 rows
+    into every stage.  Ragged last tile."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    G = K // 128
+    tiles = (48 * sms + G - 1) // G + 1
+    return tiles * 64 - ragged
+
+
+@pytest.mark.parametrize("T,K", [(1, 1152), (3, 5120), (5, 2432), (8, 1664)])
+def test_gemm_resident_activations_match_oracle(sv, oracle, T, K):
+    N = resident_rows(K)
+    rng = np.random.default_rng(7300 + 31 * T + K)
+    Wq, sc = gen.weights(rng, N, K)
+    x = gen.activations(rng, T, K)
+    y32, _ = oracle.w4a16_gemm(x, Wq, sc, T, K, N)
+    y = sv.w4a16_gemm(dev_bits16(x), dev_words(Wq), dev_bits16(sc))
+    torch.cuda.synchronize()
+    assert_gemm_close(y.view(torch.int16).cpu().numpy().view(np.uint16), y32)
+
+
 def wide_range_activations(rng, K):
     """Four bf16 rows far from N(0,1): scaled by 2^100, by 2^-100, with
     per-element magnitudes spread over 2^-40 .. 2^40, and N(0,1) with a few
@@ -140,8 +163,10 @@ def wide_range_activations(rng, K):
     return gen.f32_to_bf16_bits(z.astype(np.float32))
 
 
-@pytest.mark.parametrize("K,N", [(1152, 300), (5120, 64)])
+@pytest.mark.parametrize("K,N", [(1152, 300), (5120, 64), (1152, "resident"), (5120, "resident")])
 def test_gemm_activation_dynamic_range(sv, oracle, K, N):
+    if N == "resident":
+        N = resident_rows(K)
     rng = np.random.default_rng(4100 + K)
     Wq, sc = gen.weights(rng, N, K)
     x = wide_range_activations(rng, K)
@@ -152,11 +177,14 @@ def test_gemm_activation_dynamic_range(sv, oracle, K, N):
     assert_gemm_close(y.view(torch.int16).cpu().numpy().view(np.uint16), y32)
 
 
-def test_head_argmax_activation_dynamic_range(sv, oracle):
+@pytest.mark.parametrize("V", [3000, "resident"])
+def test_head_argmax_activation_dynamic_range(sv, oracle, V):
     """Rows scaled by 2^30, unscaled, by 2^-30 and the spread row: argmax
     ids bit-exact where the margin allows, chosen logits within reordering."""
     rng = np.random.default_rng(4242)
-    V, K = 3000, 768
+    K = 768
+    if V == "resident":
+        V = resident_rows(K, ragged=5)
     Wq, sc = gen.weights(rng, V, K)
     z = rng.standard_normal((4, K))
     z[0] *= 2.0 ** 30
