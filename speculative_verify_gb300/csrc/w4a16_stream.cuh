@@ -77,7 +77,10 @@ struct Cfg {
     // 2-way conflict on the weight loads, a few per 2 KB of weights).
     static constexpr int GROW = GPS * 64;           // one gathered row of a stage
     static constexpr int W_BYTES = GATHER ? ROWS * GROW : GPS * ROWS * 64;
-    static constexpr int RED_FLOATS = GPS * TP * ROWS;
+    // hand-off buffer row stride (floats): TP, padded by 8 for wider tiles
+    // (two-wavefront float2 stores by the consumers)
+    static constexpr int RSTR = (NT == 1) ? 8 : TP + 8;
+    static constexpr int RED_FLOATS = GPS * ROWS * RSTR;
 };
 
 struct Params {
@@ -249,14 +252,16 @@ __global__ void __launch_bounds__(XP_THREADS) xprep_kernel(const uint16_t *x, in
     if (tid == 0) xinv[t] = __uint_as_float(static_cast<uint32_t>(127 - sh) << 23);
 }
 
-// The consumers' hand-off buffer `red` holds one partial per group slot.
-// One token tile (NT == 1): [slot][ROWS][8 tokens], so that the epilogue
-// reads four tokens of a row with one 16-byte load; wider tiles:
-// [slot][TP tokens][ROWS].
+// The consumers' hand-off buffer `red` holds one partial per group slot as
+// [slot][ROWS][RSTR]: token t of row `row` at (slot * ROWS + row) * RSTR + t,
+// so that the epilogue reads four tokens of a row with one 16-byte load.
+// One token tile: RSTR = 8; wider tiles: TP + 8 (the padding keeps the
+// consumers' two-token stores at two wavefronts per warp).
 template <int NT, int GPS>
 __device__ __forceinline__ int red_index(int slot, int tok, int row)
 {
-    return NT == 1 ? (slot * ROWS + row) * 8 + tok : (slot * (8 * NT) + tok) * ROWS + row;
+    constexpr int RSTR = (NT == 1) ? 8 : 8 * NT + 8;
+    return (slot * ROWS + row) * RSTR + tok;
 }
 
 // Sums over the GPS group slots of tokens t0..t0+3 of tile row `row`
@@ -264,28 +269,13 @@ __device__ __forceinline__ int red_index(int slot, int tok, int row)
 template <int NT, int GPS>
 __device__ __forceinline__ float4 slot_sums4(const float *red, int t0, int row, int T)
 {
-    float4 v;
-    if constexpr (NT == 1) {
-        // slots in groups of four: ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7))
-        auto add = [](float4 a, float4 b) { return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w); };
-        auto ld = [&](int sl) { return *reinterpret_cast<const float4 *>(red + red_index<NT, GPS>(sl, t0, row)); };
-        v = add(add(ld(0), ld(1)), add(ld(2), ld(3)));
+    static_assert(GPS % 4 == 0, "slots are added in groups of four");
+    // slots in groups of four: ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7))
+    auto add = [](float4 a, float4 b) { return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w); };
+    auto ld = [&](int sl) { return *reinterpret_cast<const float4 *>(red + red_index<NT, GPS>(sl, t0, row)); };
+    float4 v = add(add(ld(0), ld(1)), add(ld(2), ld(3)));
 #pragma unroll
-        for (int sl = 4; sl < GPS; sl += 4) v = add(v, add(add(ld(sl), ld(sl + 1)), add(ld(sl + 2), ld(sl + 3))));
-    } else {
-        float a[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            float sum = 0.f;
-            if (t0 + j < T) {
-                sum = red[red_index<NT, GPS>(0, t0 + j, row)];
-#pragma unroll
-                for (int sl = 1; sl < GPS; ++sl) sum += red[red_index<NT, GPS>(sl, t0 + j, row)];
-            }
-            a[j] = sum;
-        }
-        v = make_float4(a[0], a[1], a[2], a[3]);
-    }
+    for (int sl = 4; sl < GPS; sl += 4) v = add(v, add(add(ld(sl), ld(sl + 1)), add(ld(sl + 2), ld(sl + 3))));
     if (t0 + 1 >= T) v.y = 0.f;
     if (t0 + 2 >= T) v.z = 0.f;
     if (t0 + 3 >= T) v.w = 0.f;
@@ -1031,12 +1021,7 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
                             v0 *= __ldg(p.xinv + tok);
                             v1 *= __ldg(p.xinv + tok + 1);
                         }
-                        if constexpr (NT == 1) {
-                            *reinterpret_cast<float2 *>(red + red_index<NT, C::GPS>(slot, tok, row)) = make_float2(v0, v1);
-                        } else {
-                            red[red_index<NT, C::GPS>(slot, tok, row)] = v0;
-                            red[red_index<NT, C::GPS>(slot, tok + 1, row)] = v1;
-                        }
+                        *reinterpret_cast<float2 *>(red + red_index<NT, C::GPS>(slot, tok, row)) = make_float2(v0, v1);
                         acc[r][nt][2 * hh] = 0.f;
                         acc[r][nt][2 * hh + 1] = 0.f;
                     }
