@@ -13,18 +13,19 @@
 //
 // Warp roles inside a CTA (all hand-offs are mbarriers; no CTA-wide barrier
 // after set-up):
-//  * warp 16, producer: fills each pipeline stage (up to GPS units of one
+// (NCW consumer warps, 16 or 8, see consumer_warps):
+//  * warp NCW, producer: fills each pipeline stage (up to GPS units of one
 //    tile) with tensor (TMA) copies -- one 64-row x 64-byte box of packed
 //    weights and one box of activations per group -- completing on the
 //    stage's mbarrier.  Gathered rows (a vocab_map) use one 1-D bulk copy per
 //    row segment instead.
-//  * warps 0..15, consumers: warp w takes group (w % GPS) of a stage for R
+//  * warps 0..NCW-1, consumers: warp w takes group (w % GPS) of a stage for R
 //    m16 tiles, dequantises its nibbles in registers and feeds them to the
 //    bf16 tensor cores as the A operand (mma.sync m16n8k16; tokens are the
 //    n8 B operand), and folds each group's fp32 sum into its accumulators
 //    with the group scale.  At the end of a tile each warp hands its partial
 //    sums to the epilogue warp through shared memory.
-//  * warp 17, epilogue: stages the scales (and token ids) of tile k+2 while
+//  * warp NCW+1, epilogue: stages the scales (and token ids) of tile k+2 while
 //    tile k+1 is being computed, adds the consumers' partials in a fixed
 //    order, finishes split tiles, and runs the GEMM store or the lm_head
 //    argmax; at the end it runs the grid-level argmax and the verify.
@@ -48,10 +49,15 @@
 namespace sv {
 
 constexpr int ROWS = 64;                        // rows per tile
-constexpr int NCW = 16;                         // consumer warps
-constexpr int PRODUCER_WARP = NCW;
-constexpr int EPILOGUE_WARP = NCW + 1;
-constexpr int NTHREADS = (NCW + 2) * 32;
+// Consumer warps of a launch: 16 (two m16 tiles each) when one token tile
+// reads resident activations; 8 (all four m16 tiles of a group, or two of
+// four token tiles) when activations are copied into every stage, where
+// fewer, wider warps measured faster.  The producer and epilogue warps
+// follow the consumers.
+__host__ __device__ constexpr int consumer_warps(int NT, bool XRES)
+{
+    return (NT == 1 && XRES) ? 16 : 8;
+}
 constexpr int TMAX = 32;                        // largest T
 constexpr int PART_FLOATS = TMAX * ROWS;        // one split-tile partial
 constexpr int XBOX = 144;                       // bf16 activation box width (elements), one token tile
@@ -63,8 +69,9 @@ constexpr int BK_STRIDE = TMAX + 1;             // u64 per lane in the best-key 
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;        // 2 s: only a broken run gets here
 constexpr uint64_t WAIT_LIMIT_AFTER_ERR_NS = 1000000ull;  // 1 ms once something failed
 
-template <int NT, bool GATHER>
+template <int NT, bool GATHER, int NCW_>
 struct Cfg {
+    static constexpr int NCW = NCW_;                // consumer warps
     static constexpr int GPS = (NT == 1) ? 8 : 4;   // 128-column groups per stage
     static constexpr int MSETS = NCW / GPS;         // warps sharing one group slot
     static constexpr int R = 4 / MSETS;             // m16 tiles per warp
@@ -343,11 +350,14 @@ __device__ __forceinline__ void stage_tile_meta(const Params &p, int tile, uint8
 }
 
 template <int NT, bool HEAD, bool GATHER, bool XRES>
-__global__ void __launch_bounds__(NTHREADS, 1)
+__global__ void __launch_bounds__((consumer_warps(NT, XRES) + 2) * 32, 1)
 w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tmW,
                     const __grid_constant__ CUtensorMap tmX)
 {
-    using C = Cfg<NT, GATHER>;
+    constexpr int NCW = consumer_warps(NT, XRES);
+    constexpr int PRODUCER_WARP = NCW;
+    constexpr int EPILOGUE_WARP = NCW + 1;
+    using C = Cfg<NT, GATHER, NCW>;
     static_assert(!XRES || NT == 1, "resident activations are laid out for one n8 token tile");
     // How activations reach the B loads: resident fp16 rows (XRES); raw bf16
     // rows copied into every stage by tensor copies (XBF: one token tile
