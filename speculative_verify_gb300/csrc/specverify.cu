@@ -188,7 +188,7 @@ bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0
 template <int NT, bool HEAD, bool GATHER, bool XRES>
 int plan_layout(Params &p, int smem_optin, int *smem_total)
 {
-    using C = Cfg<NT, GATHER, consumer_warps(NT, XRES)>;
+    using C = Cfg<NT, GATHER, consumer_warps(NT, XRES, GATHER)>;
     auto up = [](int v, int a) { return (v + a - 1) / a * a; };
     p.xslot_bytes = NT > 1 ? C::TP * XSTR                 // one group block of xprep_kernel
                            : up(p.T * XROW_BYTES, 128);      // a bf16 activation box of the T rows
@@ -254,7 +254,7 @@ int launch(Params p, const DeviceState &st, cudaStream_t stream)
         // gathered rows: boxes one row high, GPS groups wide (tile::gather4)
         rc = encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, p.Wq,
                        static_cast<unsigned long long>(p.K / 8), static_cast<unsigned long long>(p.V),
-                       static_cast<unsigned>(Cfg<NT, GATHER, consumer_warps(NT, XRES)>::GPS * 16), 1);
+                       static_cast<unsigned>(Cfg<NT, GATHER, consumer_warps(NT, XRES, GATHER)>::GPS * 16), 1);
     }
     if (rc != SV_OK) return rc;
     if (!XRES && NT == 1) {
@@ -286,17 +286,17 @@ int launch(Params p, const DeviceState &st, cudaStream_t stream)
         // several token tiles: convert x into ready-made group blocks first
         p.x16 = st.x16;
         p.xinv = st.xinv;
-        cfg.gridDim = dim3(static_cast<unsigned>(Cfg<NT, GATHER, consumer_warps(NT, XRES)>::TP));
+        cfg.gridDim = dim3(static_cast<unsigned>(Cfg<NT, GATHER, consumer_warps(NT, XRES, GATHER)>::TP));
         cfg.blockDim = dim3(XP_THREADS);
         cfg.dynamicSmemBytes = 0;
-        if (cudaLaunchKernelEx(&cfg, xprep_kernel, p.x, p.T, p.K, Cfg<NT, GATHER, consumer_warps(NT, XRES)>::TP, st.x16, st.xinv) !=
+        if (cudaLaunchKernelEx(&cfg, xprep_kernel, p.x, p.T, p.K, Cfg<NT, GATHER, consumer_warps(NT, XRES, GATHER)>::TP, st.x16, st.xinv) !=
             cudaSuccess) {
             cudaGetLastError();
             return SV_ERR_CUDA;
         }
     }
     cfg.gridDim = dim3(static_cast<unsigned>(B));
-    cfg.blockDim = dim3(static_cast<unsigned>((consumer_warps(NT, XRES) + 2) * 32));
+    cfg.blockDim = dim3(static_cast<unsigned>((consumer_warps(NT, XRES, GATHER) + 2) * 32));
     cfg.dynamicSmemBytes = static_cast<size_t>(smem);
     if (cudaLaunchKernelEx(&cfg, w4a16_stream_kernel<NT, HEAD, GATHER, XRES>, p, tmW, tmX) != cudaSuccess) {
         cudaGetLastError();

@@ -50,13 +50,13 @@ namespace sv {
 
 constexpr int ROWS = 64;                        // rows per tile
 // Consumer warps of a launch: 16 (two m16 tiles each) when one token tile
-// reads resident activations; 8 (all four m16 tiles of a group, or two of
-// four token tiles) when activations are copied into every stage, where
-// fewer, wider warps measured faster.  The producer and epilogue warps
-// follow the consumers.
-__host__ __device__ constexpr int consumer_warps(int NT, bool XRES)
+// of contiguous rows reads resident activations; otherwise 8 (all four m16
+// tiles of a group, or two of four token tiles) -- activations copied into
+// every stage, or gathered rows -- where fewer, wider warps measured faster.
+// The producer and epilogue warps follow the consumers.
+__host__ __device__ constexpr int consumer_warps(int NT, bool XRES, bool GATHER)
 {
-    return (NT == 1 && XRES) ? 16 : 8;
+    return (NT == 1 && XRES && !GATHER) ? 16 : 8;
 }
 constexpr int TMAX = 32;                        // largest T
 constexpr int PART_FLOATS = TMAX * ROWS;        // one split-tile partial
@@ -350,11 +350,11 @@ __device__ __forceinline__ void stage_tile_meta(const Params &p, int tile, uint8
 }
 
 template <int NT, bool HEAD, bool GATHER, bool XRES>
-__global__ void __launch_bounds__((consumer_warps(NT, XRES) + 2) * 32, 1)
+__global__ void __launch_bounds__((consumer_warps(NT, XRES, GATHER) + 2) * 32, 1)
 w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tmW,
                     const __grid_constant__ CUtensorMap tmX)
 {
-    constexpr int NCW = consumer_warps(NT, XRES);
+    constexpr int NCW = consumer_warps(NT, XRES, GATHER);
     constexpr int PRODUCER_WARP = NCW;
     constexpr int EPILOGUE_WARP = NCW + 1;
     using C = Cfg<NT, GATHER, NCW>;
