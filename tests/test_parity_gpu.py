@@ -148,6 +148,30 @@ def test_gemm_resident_activations_match_oracle(sv, oracle, T, K):
     assert_gemm_close(y.view(torch.int16).cpu().numpy().view(np.uint16), y32)
 
 
+def test_gemm_resident_activations_two_staging_passes(sv, oracle):
+    """Eight token rows of 5,632 columns: each of the two warps per row holds
+    fewer chunks than the row has, so the resident rows are staged in two
+    passes over global memory (maximum, then conversion)."""
+    T, K = 8, 5632
+    N = resident_rows(K)
+    rng = np.random.default_rng(7411)
+    Wq, sc = gen.weights(rng, N, K)
+    x = gen.activations(rng, T, K)
+    y32, _ = oracle.w4a16_gemm(x, Wq, sc, T, K, N)
+    y = sv.w4a16_gemm(dev_bits16(x), dev_words(Wq), dev_bits16(sc))
+    torch.cuda.synchronize()
+    assert_gemm_close(y.view(torch.int16).cpu().numpy().view(np.uint16), y32)
+
+
+def test_restricted_head_eight_rows_resident(sv, oracle):
+    """Gathered rows with resident activations at T = 8 and K = 5,120: one warp
+    per token row, staged in two passes; 12,000 candidate rows so that each
+    CTA's share keeps the activations resident."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    n_map = max(12000, (48 * sms + 39) // 40 * 64 + 64)
+    run_head_case(sv, oracle, 9173, n_map + 4000, 5120, 7, 1, n_map)
+
+
 def wide_range_activations(rng, K):
     """Four bf16 rows far from N(0,1): scaled by 2^100, by 2^-100, with
     per-element magnitudes spread over 2^-40 .. 2^40, and N(0,1) with a few
