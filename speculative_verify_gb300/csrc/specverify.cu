@@ -229,11 +229,12 @@ int plan_layout(Params &p, int smem_optin, int *smem_total)
 }
 
 // Resident activations pay off when they fit with at least 3 weight stages,
-// and when each CTA's share is long enough (at least 6 stages of 8 units) to
-// amortise converting them before its first stage: with shorter shares
-// (QKV-sized GEMMs) the bf16 rows copied into every stage are faster.
+// and when each CTA's share is long enough (at least 10 stages of 8 units)
+// to amortise converting them before its first stage: with shorter shares
+// (the QKV and down GEMMs of a 27B-class layer) the bf16 rows copied into
+// every stage are faster.
 constexpr int XRES_MAX_BYTES = 100 * 1024;
-constexpr int XRES_MIN_UNITS = 48;
+constexpr int XRES_MIN_UNITS = 80;
 
 template <int NT, bool HEAD, bool GATHER, bool XRES>
 int launch(Params p, const DeviceState &st, cudaStream_t stream)

@@ -125,14 +125,17 @@ def test_gemm_matches_oracle(sv, oracle, T, K, N):
     assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
 
 
+RESIDENT_MIN_UNITS = 80      # the library's threshold for resident activations
+
+
 def resident_rows(K, ragged=17):
     """A row count whose call keeps the activations resident in shared memory:
     the kernels convert them once per CTA only when each CTA streams at least
-    48 units (64 rows x one 128-column group); smaller calls copy bf16 rows
+    80 units (64 rows x one 128-column group); smaller calls copy bf16 rows
     into every stage.  Ragged last tile."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     G = K // 128
-    tiles = (48 * sms + G - 1) // G + 1
+    tiles = (RESIDENT_MIN_UNITS * sms + G - 1) // G + 1
     return tiles * 64 - ragged
 
 
@@ -165,10 +168,10 @@ def test_gemm_resident_activations_two_staging_passes(sv, oracle):
 
 def test_restricted_head_eight_rows_resident(sv, oracle):
     """Gathered rows with resident activations at T = 8 and K = 5,120: one warp
-    per token row, staged in two passes; 12,000 candidate rows so that each
+    per token row, staged in two passes; enough candidate rows that each
     CTA's share keeps the activations resident."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    n_map = max(12000, (48 * sms + 39) // 40 * 64 + 64)
+    n_map = (RESIDENT_MIN_UNITS * sms + 39) // 40 * 64 + 64
     run_head_case(sv, oracle, 9173, n_map + 4000, 5120, 7, 1, n_map)
 
 
