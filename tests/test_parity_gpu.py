@@ -52,7 +52,7 @@ def assert_gemm_close(y_gpu_bits, y32):
     y32 = y32.astype(np.float64)
     rowmax = np.abs(y32).max(axis=1, keepdims=True)
     err = np.abs(yg - y32)
-    assert np.all(err <= 1e-2 * rowmax), "north-star tolerance violated: max rel %.3g" % (
+    assert np.all(err <= 1e-2 * rowmax), "specified tolerance (1e-2 of the row maximum) violated: max rel %.3g" % (
         (err / np.maximum(rowmax, 1e-30)).max())
     assert np.all(err <= 2.0 ** -8 * np.abs(y32) + 1e-5 * rowmax)
 
