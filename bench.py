@@ -552,7 +552,8 @@ def per_kernel_breakdown(torch, sv, device, stream, reps=50):
             cases.append(("gemm", label, K, N, T))
     for T, S in ((1, 1), (4, 1), (8, 1), (32, 4)):
         cases.append(("head", "lm_head", gen.HIDDEN, gen.VOCAB, (T, S)))
-    cases.append(("head_map", "restricted", gen.HIDDEN, gen.VOCAB, (4, 1)))
+    for T in (1, 4):
+        cases.append(("head_map", "restricted", gen.HIDDEN, gen.VOCAB, (T, 1)))
     # the greedy draft step over a full dynamic draft list (32,768 static ids
     # + 4,096 sequence tokens), and the list maintenance call itself
     cases.append(("draft_step", "list_32768+4096", gen.HIDDEN, gen.VOCAB, 1))
