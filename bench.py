@@ -11,7 +11,7 @@ that model; the step streams 820 MB, more than the 129 MB L2, so every kernel
 reads its weights from HBM.
 
 Usage: python bench.py [--gpus N --steps K --warmup W] [--impl reference]
-                       [--ncu-case head|gemm|sampled|rescored] [--breakdown]
+                       [--ncu-case head|gemm|sampled|rescored|restricted] [--breakdown]
 One JSON line on stdout (rank 0).
 """
 from __future__ import annotations
@@ -673,7 +673,16 @@ def run_ncu_case(args):
     device = torch.device("cuda", 0)
     rng = np.random.default_rng(5)
     dev = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a).view(dt)).to(device)
-    if args.ncu_case in ("head", "sampled", "rescored"):
+    if args.ncu_case == "restricted":
+        V, K, T = gen.VOCAB, gen.HIDDEN, T_STEP
+        Wq, sc = gen.weights(rng, V, K)
+        Wd, sd = dev(Wq, np.int32), dev(sc, np.int16)
+        x = dev(gen.activations(rng, T, K), np.int16)
+        vm = dev(gen.vocab_map(rng, V, gen.DRAFT_VOCAB), np.int32)
+        drafts = torch.zeros(T - 1, dtype=torch.int32, device=device)
+        for _ in range(3):
+            sv.lmhead_verify(x, Wd, sd, drafts, vocab_map=vm)
+    elif args.ncu_case in ("head", "sampled", "rescored"):
         V, K, T = gen.VOCAB, gen.HIDDEN, T_STEP
         Wq, sc = gen.weights(rng, V, K)
         Wd, sd = dev(Wq, np.int32), dev(sc, np.int16)
@@ -710,7 +719,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--breakdown", action="store_true", help="also time each kernel alone at T=1..32")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--ncu-case", choices=["head", "gemm", "sampled", "rescored"], default=None)
+    ap.add_argument("--ncu-case", choices=["head", "gemm", "sampled", "rescored", "restricted"], default=None)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
