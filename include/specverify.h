@@ -145,23 +145,24 @@ int lmhead_argmax(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, i
 
 /*
  * lmhead_verify_noalloc -- the same greedy verify as lmhead_verify, for
- * callers that must not allocate GPU memory: code running under CUDA-graph
- * stream capture (where a first-call cudaMalloc is not allowed), serving
- * runtimes that own every byte of device memory through their own arena
- * and forbid stray allocations, and latency-critical paths that cannot
- * afford cudaMalloc's implicit device synchronisation.  No source page has
- * a counterpart to this entry point; it exists for this library's users.
+ * callers that must not allocate GPU memory when they call: serving
+ * runtimes that hand out every byte of device memory from their own arena
+ * and forbid allocations behind their back, and latency-critical paths
+ * that cannot take the implicit device synchronisation of cudaMalloc.
+ * No source page has a counterpart to this entry point; it exists for this
+ * library's users.
  *   Arguments, layouts and results are those of lmhead_verify.
- *   Scratch: a fixed device array inside the library (about 3.8 MB per
+ *   Scratch: a fixed device array inside the library (about 3.7 MB per
  *   device, held until the process exits), sized for at most 160 thread
  *   blocks, 32 verify rows and, with more than 7 drafts, K <= 16384; the
  *   call launches at most 160 blocks and rejects more than 31 drafts, or
- *   more than 7 drafts with K > 16384, with SV_ERR_SHAPE.  It calls no
- *   cudaMalloc, cudaFree or other allocating routine.
+ *   more than 7 drafts with K > 16384, with SV_ERR_SHAPE before it
+ *   enqueues anything.  It calls no cudaMalloc, cudaFree or other
+ *   allocating routine.
  *   The first call on a device resolves the array's device address and
- *   sets kernel attributes (no allocation, but make that first call outside
- *   stream capture).  Each call clears the array's counters with an
- *   asynchronous memset on `stream` before its kernel.
+ *   sets kernel attributes (no allocation); make that first call before
+ *   any stream capture.  Each call clears the array's counters with an
+ *   asynchronous memset on `stream` right before its kernels.
  *   All calls share the one array: calls that overlap on the GPU (two
  *   streams, or two host threads) race on it and must be ordered by the
  *   caller.  Device-side problems (a bad vocab_map id is skipped) are not
@@ -304,6 +305,22 @@ const char *sv_status_string(int status);
  * SV_ERR_NULL or SV_ERR_CUDA.
  */
 int sv_last_device_error(int32_t *out);
+/*   When the word holds SV_DEVERR_TIMEOUT, the call also puts the
+ *   per-device scratch counters (split-tile arrivals, argmax keys, CTA
+ *   completions) back to zero, so that a run which gave up on a wait cannot
+ *   affect later calls. */
+
+/*
+ * sv_debug_set_wait_stall -- a test hook for the bounded waits.  With
+ * ns > 0, every later launch of the stream kernel makes the epilogue warp
+ * of its first thread block wait up to ns nanoseconds on a shared-memory
+ * barrier that nothing completes; the wait runs out, the kernel sets
+ * SV_DEVERR_TIMEOUT and carries on (its outputs are still computed).  0
+ * turns it off.  Process-wide, not per device.  No source page has a
+ * counterpart: it exists to test the error path without a GPU fault.
+ *   Errors: SV_ERR_SHAPE if ns > 10^9 (one second).
+ */
+int sv_debug_set_wait_stall(uint32_t ns);
 
 #ifdef __cplusplus
 }

@@ -339,12 +339,10 @@ def draft_list_add(dl: DraftList, tokens) -> DraftList:
 #    norm(max(0, p - q)) is p with d removed and renormalised.
 #  * llama.cpp's order is top-k, top-p, min-p, then temperature: top-p and
 #    min-p see the temperature-1 distribution of the surviving candidates.
-#  * All arithmetic is fp32 in a fixed order (the kernel's precision).
-#    Running sums over the (at most 32) candidates, best first, are the
-#    inclusive prefix sums of a 32-slot scan that adds, for d = 1, 2, 4, 8,
-#    16 in turn, slot j - d into slot j (slots past the candidates taking
-#    part hold 0); a total is the last candidate's prefix sum.  With m the
-#    best logit and d_j = l_j - m,
+#  * All arithmetic is fp32.  The pages fix no summation order, so the
+#    plainest one is taken: running sums over the (at most 32) candidates
+#    are accumulated one candidate at a time, best first, and a total is
+#    the last running sum.  With m the best logit and d_j = l_j - m,
 #      top-p keeps the shortest prefix whose running sum of exp(d_j) reaches
 #      top_p times the sum over the candidates (all of them if rounding
 #      never reaches it);
@@ -403,20 +401,20 @@ def _f32(v):
     return np.float32(v)
 
 
-def _scan32_f32(vals):
-    """Inclusive prefix sums of up to 32 fp32 values in the scan order:
-    for d = 1, 2, 4, 8, 16, slot j += slot j - d (all slots at once)."""
-    c = np.zeros(SAMPLE_KEEP, np.float32)
-    c[:len(vals)] = np.asarray(vals, np.float32)
-    for d in (1, 2, 4, 8, 16):
-        prev = c.copy()
-        c[d:] = (prev[d:] + prev[:-d]).astype(np.float32)
-    return c[:len(vals)]
+def _running_f32(vals):
+    """Running sums of fp32 values, added one at a time in the given order
+    (c_0 = v_0, c_j = fl(c_{j-1} + v_j))."""
+    out = np.zeros(len(vals), np.float32)
+    c = _f32(0.0)
+    for j, v in enumerate(vals):
+        c = _f32(c + _f32(v))
+        out[j] = c
+    return out
 
 
 def _sum_f32(vals):
-    """Total of up to 32 fp32 values in the scan order."""
-    return _f32(_scan32_f32(vals)[-1]) if len(vals) else _f32(0.0)
+    """Total of fp32 values added one at a time in the given order."""
+    return _f32(_running_f32(vals)[-1]) if len(vals) else _f32(0.0)
 
 
 def sampling_dist(vals, ids, temperature, top_k=0, top_p=1.0, min_p=0.0, sel_gap=np.inf) -> SamplingDist:
@@ -439,7 +437,7 @@ def sampling_dist(vals, ids, temperature, top_k=0, top_p=1.0, min_p=0.0, sel_gap
     e = np.exp(d).astype(np.float32)
     cut_margin = np.inf
     if top_p < 1.0:
-        cs = _scan32_f32(e[:n])
+        cs = _running_f32(e[:n])
         S = cs[n - 1]
         thr = _f32(_f32(top_p) * S)
         c = _f32(0.0)
@@ -481,7 +479,7 @@ def sample_from(dist: SamplingDist, u, exclude=None):
     wx = dist.w.copy()
     if exclude is not None:
         wx[exclude] = 0.0
-    cs = _scan32_f32(wx)
+    cs = _running_f32(wx)
     Wx = cs[-1]
     target = _f32(_f32(u) * Wx)
     c = _f32(0.0)

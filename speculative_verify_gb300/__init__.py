@@ -82,6 +82,8 @@ def load(path: str | None = None):
     lib.sv_status_string.restype = ctypes.c_char_p
     lib.sv_last_device_error.argtypes = [ctypes.POINTER(ctypes.c_int32)]
     lib.sv_last_device_error.restype = ci
+    lib.sv_debug_set_wait_stall.argtypes = [ctypes.c_uint32]
+    lib.sv_debug_set_wait_stall.restype = ci
     _lib = lib
     return lib
 
@@ -392,3 +394,10 @@ def last_device_error() -> int:
     out = ctypes.c_int32(0)
     _check("sv_last_device_error", load().sv_last_device_error(ctypes.byref(out)))
     return int(out.value)
+
+
+def debug_set_wait_stall(ns: int) -> None:
+    """Test hook of the bounded waits (sv_debug_set_wait_stall): with ns > 0
+    every later stream-kernel launch makes one wait run out after ns
+    nanoseconds and report SV_DEVERR_TIMEOUT; 0 turns it off."""
+    _check("sv_debug_set_wait_stall", load().sv_debug_set_wait_stall(int(ns)))

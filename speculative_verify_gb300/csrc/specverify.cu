@@ -8,6 +8,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "draft_list.cuh"
@@ -46,6 +47,10 @@ struct DeviceState {
     float *rs_logits = nullptr;           // [RS_TMAX][rs_v_cap]
     unsigned long long *rs_smax = nullptr;   // [RS_TMAX][rs_s_cap] slice maxima
     long long rs_v_cap = 0, rs_s_cap = 0;
+    // When set, every launch first clears these bytes on its stream (the
+    // allocation-free verify, whose counters are not guaranteed to be zero).
+    void *clear_ptr = nullptr;
+    size_t clear_bytes = 0;
 };
 
 // Activations of calls with more than one token tile (T > 8) are converted
@@ -54,6 +59,7 @@ constexpr int X16_MAX_GROUPS = 1024;
 
 DeviceState g_state[MAX_DEVICES];
 std::mutex g_mu;
+std::atomic<uint32_t> g_stall_ns{0};    // sv_debug_set_wait_stall
 
 template <int NT, bool HEAD, bool GATHER, bool XRES>
 cudaError_t raise_smem_limit(int bytes)
@@ -200,7 +206,7 @@ int plan_layout(Params &p, int smem_optin, int *smem_total)
     const int red_bytes = up(C::RED_FLOATS * 4, 128);
     const int bk_bytes = HEAD ? up(32 * BK_STRIDE * 8, 128) : 0;
     const int fixed = xres_bytes + 2 * p.sbuf_bytes + ids_bytes + red_bytes + 128 + ROWS * 8 * 4 + bk_bytes + 256 +
-                      7 * 8 + 8;
+                      6 * 8 + 16;
     int nst = (smem_optin - fixed - 1024) / (p.stage_bytes + 16);
     if (nst > 8) nst = 8;
     if (nst < 2) return SV_ERR_SHAPE;
@@ -223,7 +229,7 @@ int plan_layout(Params &p, int smem_optin, int *smem_total)
     p.off_xzero = off;
     off += 256;
     p.off_bars = off;
-    off += (2 * nst + 6) * 8 + 8;
+    off += (2 * nst + 6) * 8 + 16;       // barriers, the time-out flag, the test hook's barrier
     *smem_total = off;
     return off <= smem_optin ? SV_OK : SV_ERR_SHAPE;
 }
@@ -273,6 +279,7 @@ int launch(Params p, const DeviceState &st, cudaStream_t stream)
     p.keys = st.keys;
     p.done = st.done;
     p.err = st.err;
+    p.stall_ns = g_stall_ns.load(std::memory_order_relaxed);
     // Programmatic dependent launch: each kernel may begin while the previous
     // kernel of the stream drains; it waits (griddepcontrol.wait) before it
     // touches anything that kernel could have written.
@@ -283,6 +290,11 @@ int launch(Params p, const DeviceState &st, cudaStream_t stream)
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    // Every check has passed: from here on work is enqueued.
+    if (st.clear_bytes && cudaMemsetAsync(st.clear_ptr, 0, st.clear_bytes, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return SV_ERR_CUDA;
+    }
     if (!XRES && NT > 1) {
         // several token tiles: convert x into ready-made group blocks first
         p.x16 = st.x16;
@@ -570,9 +582,11 @@ int sampled_call(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, in
 // Its scratch -- split-tile partial sums, arrival counters, argmax keys --
 // lives in the file-scope device array below instead of a cudaMalloc'd
 // area, so the call never allocates.  The array is sized for at most
-// NOALLOC_MAX_CTAS thread blocks (each keeps two 32-token partial tiles);
-// the call never launches more blocks than that.  Every device that loads
-// this library holds the array (about 2.6 MB) until the process exits.
+// NOALLOC_MAX_CTAS thread blocks (each keeps two 32-token partial tiles,
+// 2.6 MB in all) plus the conversion buffer of calls with more than 7
+// drafts (1.1 MB, K <= 16384); the call never launches more blocks than
+// that.  Every device that loads this library holds the array (about
+// 3.7 MB) until the process exits.
 
 constexpr int NOALLOC_MAX_CTAS = 160;
 constexpr size_t NOALLOC_PART_BYTES = static_cast<size_t>(NOALLOC_MAX_CTAS) * 2 * PART_FLOATS * sizeof(float);
@@ -634,6 +648,10 @@ int noalloc_state(DeviceState **out)
         st.x16_max_groups = NOALLOC_X16_GROUPS;
         st.sms = sms < NOALLOC_MAX_CTAS ? sms : NOALLOC_MAX_CTAS;
         st.smem_optin = optin;
+        // the array keeps whatever the last call left: the counters, keys,
+        // completion count and error word are cleared before every launch
+        st.clear_ptr = st.ctr;
+        st.clear_bytes = NOALLOC_XINV_OFF - NOALLOC_CTR_OFF;
         st.ready = true;
     }
     *out = &st;
@@ -663,17 +681,13 @@ int lmhead_verify_noalloc(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *s
     if (n_draft > 0 && !drafts) return SV_ERR_NULL;
     if ((drafts && !aligned4(drafts)) || !aligned4(accept_len) || !aligned4(next_token))
         return SV_ERR_ALIGN;
+    // more than 7 drafts: the activations go through the fixed conversion
+    // buffer, sized for K <= 128 * NOALLOC_X16_GROUPS
+    if (T > 8 && K / 128 > NOALLOC_X16_GROUPS) return SV_ERR_SHAPE;
     DeviceState *st = nullptr;
     rc = noalloc_state(&st);
     if (rc != SV_OK) return rc;
     const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-    // The array keeps whatever the last call left: the counters, keys and
-    // completion count must start at zero, so clear them (and the error word)
-    // on the stream first.
-    if (cudaMemsetAsync(st->ctr, 0, NOALLOC_XINV_OFF - NOALLOC_CTR_OFF, cs) != cudaSuccess) {
-        cudaGetLastError();
-        return SV_ERR_CUDA;
-    }
     Params p{};
     p.x = x;
     p.Wq = Wq;
@@ -776,8 +790,23 @@ int sv_last_device_error(int32_t *out)
     int v = 0;
     if (cudaMemcpy(&v, st->err, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return SV_ERR_CUDA;
     if (cudaMemset(st->err, 0, sizeof v) != cudaSuccess) return SV_ERR_CUDA;
+    if (v & SV_DEVERR_TIMEOUT) {
+        // A run that gave up on a wait may have left the counters of the
+        // scratch area (tile arrivals, argmax keys, CTA completions) out of
+        // step; put them back to zero so that later calls start clean.
+        const size_t n = reinterpret_cast<uint8_t *>(st->err) - reinterpret_cast<uint8_t *>(st->keys);
+        if (cudaMemset(st->keys, 0, n) != cudaSuccess) return SV_ERR_CUDA;
+        if (cudaMemset(st->rdone, 0, 2 * sizeof(unsigned)) != cudaSuccess) return SV_ERR_CUDA;
+    }
     if (cudaDeviceSynchronize() != cudaSuccess) return SV_ERR_CUDA;
     *out = v;
+    return SV_OK;
+}
+
+int sv_debug_set_wait_stall(uint32_t ns)
+{
+    if (ns > 1000000000u) return SV_ERR_SHAPE;
+    sv::g_stall_ns.store(ns, std::memory_order_relaxed);
     return SV_OK;
 }
 

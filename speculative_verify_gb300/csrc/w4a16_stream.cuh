@@ -125,6 +125,11 @@ struct Params {
     unsigned long long *keys;   // [TMAX] grid argmax keys (kept at 0 between calls)
     unsigned *done;             // CTA completion counter (kept at 0 between calls)
     int *err;                   // sticky device error word
+    // Test hook of the bounded waits: when nonzero, the epilogue warp of CTA
+    // 0 first waits up to stall_ns on an mbarrier that nothing completes,
+    // so that a test can watch a wait run out (the error word gets the
+    // time-out bit; everything after it still runs).
+    uint32_t stall_ns;
 };
 
 __device__ __forceinline__ long long cta_start(long long b, long long U, int B)
@@ -154,14 +159,21 @@ __device__ __forceinline__ int row_id(const Params &p, int tile, int rloc)
     return -1;
 }
 
-__device__ __forceinline__ void wait_or_flag(const Params &p, volatile int *flag, uint32_t bar,
-                                             uint32_t parity)
+// A bounded wait: when it runs out, the CTA's flag (shorter limits from then
+// on) and the time-out bit of the error word are set, and the caller goes on.
+__device__ __forceinline__ void wait_or_flag_for(const Params &p, volatile int *flag, uint32_t bar,
+                                                 uint32_t parity, uint64_t lim)
 {
-    const uint64_t lim = *flag ? WAIT_LIMIT_AFTER_ERR_NS : WAIT_LIMIT_NS;
     if (!mbar_wait_bounded(bar, parity, lim)) {
         *flag = 1;
         atomicOr(p.err, 2);
     }
+}
+
+__device__ __forceinline__ void wait_or_flag(const Params &p, volatile int *flag, uint32_t bar,
+                                             uint32_t parity)
+{
+    wait_or_flag_for(p, flag, bar, parity, *flag ? WAIT_LIMIT_AFTER_ERR_NS : WAIT_LIMIT_NS);
 }
 
 // Largest magnitude among the 8 bf16 values of a 16-byte chunk, as bf16 bits.
@@ -379,6 +391,7 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
     uint64_t *red_full = meta_full + 4;       //        consumers -> epilogue
     uint64_t *red_empty = meta_full + 5;      //        epilogue -> consumers
     volatile int *flag = reinterpret_cast<volatile int *>(meta_full + 6);   // a wait timed out
+    uint64_t *stall_bar = meta_full + 7;      //        never completed (test hook)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int B = gridDim.x, b = blockIdx.x;
@@ -401,6 +414,7 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
         }
         mbar_init(smem_addr(red_full), NCW);
         mbar_init(smem_addr(red_empty), 1);
+        mbar_init(smem_addr(stall_bar), 1);
         *flag = 0;
         if (XRES)
             for (int t = 0; t < 8; ++t) reinterpret_cast<unsigned *>(smem + p.off_xsc)[t] = 0u;
@@ -546,6 +560,7 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
             if (tile_last != tile_first && u1 < tz + G) ncZ = cta_of(tz + G - 1, U, B) - b + 1;
         }
         pdl_wait_prior();                  // scratch area, outputs and drafts from here on
+        if (p.stall_ns != 0u && b == 0) wait_or_flag_for(p, flag, smem_addr(stall_bar), 0u, p.stall_ns);
         for (int k = 0, tile = tile_first; tile <= tile_last; ++k, ++tile) {
             const int kb = k & 1;
             // The CTA's last tile, when it is shared with exactly one later
