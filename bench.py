@@ -1,17 +1,27 @@
 #!/usr/bin/env python
 """Benchmark of the W4A16 verify hot path on GB300.
 
-One step = one speculative verify pass of a 27B-class decoder's weight read at
-T = 4 (1 + 3 drafts): the three decode GEMMs (fused QKV 5120->10240, fused
-gate+up 5120->34816, down 17408->5120) and the int4 lm_head pass with greedy
-verification over V = 248,320 (the "mtp_T4" workload).  The metric is
-algorithmic HBM bytes per second (weights + scales read once, activations
-read, outputs written).  Inputs are seeded synthetic data with the shapes of
-that model; the step streams 820 MB, more than the 129 MB L2, so every kernel
-reads its weights from HBM.
+One step is one pass over every configuration the metric spans, T = 1..32,
+with the shapes of a 27B-class decoder (fused QKV 5120->10240, fused gate+up
+5120->34816, down 17408->5120, int4 lm_head 248,320 x 5,120, a 40,960-id
+restricted draft head):
+
+  leg              calls (in order)
+  decode_T1        the three GEMMs at T = 1
+  mtp_T4           the three GEMMs at T = 4, then the lm_head verify (3 drafts)
+  dflash2_T8       the three GEMMs at T = 8, then the lm_head verify (7 drafts)
+  dflash2_4x8_T32  the three GEMMs at T = 32, then one lm_head pass verifying
+                   four streams of 1 + 7 rows
+  restricted_T1    the restricted head over 40,960 mapped rows, T = 1
+  restricted_T4    the restricted head, T = 4 (3 drafts)
+
+Every leg has its own weights, so the step streams 2.85 GB (far more than the
+129 MB L2) and every call reads its weights from HBM.  The metric is
+algorithmic HBM bytes per second (weights + scales read once, activations,
+id list and drafts read, outputs written).  Inputs are seeded synthetic data.
 
 Usage: python bench.py [--gpus N --steps K --warmup W] [--impl reference]
-                       [--ncu-case head|gemm|sampled|rescored|restricted] [--breakdown]
+                       [--breakdown] [--ncu-case ...]
 One JSON line on stdout (rank 0).
 """
 from __future__ import annotations
@@ -21,6 +31,7 @@ import ctypes
 import hashlib
 import json
 import os
+import platform
 import subprocess
 import sys
 import threading
@@ -36,9 +47,52 @@ import gen  # noqa: E402
 
 METRIC = "W4A16 skinny-GEMM + lm_head verify HBM GB/s (frac of 8 TB/s), T=1..32"
 NOMINAL_HBM_GBS = 8000.0
-WORKLOAD = "mtp_T4"
-T_STEP = 4
-N_DRAFT = 3
+WORKLOAD = "sweep_T1_T4_T8_T32_restricted"
+
+# (leg name, config index, seed, T, GEMMs?, head: (n_draft, n_streams, n_map) or None)
+LEGS = (
+    ("decode_T1", 1, 1, 1, True, None),
+    ("mtp_T4", 2, 2, 4, True, (3, 1, 0)),
+    ("dflash2_T8", 3, 3, 8, True, (7, 1, 0)),
+    ("dflash2_4x8_T32", 3, 33, 32, True, (7, 4, 0)),
+    ("restricted_T1", 4, 4, 1, False, (0, 1, gen.DRAFT_VOCAB)),
+    ("restricted_T4", 4, 44, 4, False, (3, 1, gen.DRAFT_VOCAB)),
+)
+
+
+def workload_config():
+    """The workload, as both arms print it."""
+    return {"workload": WORKLOAD,
+            "legs": [{"leg": n, "config": c, "T": T,
+                      "gemms": [list(s) for s in gen.GEMM_SHAPES] if g else [],
+                      "head": None if h is None else {"V": gen.VOCAB, "K": gen.HIDDEN, "n_draft": h[0],
+                                                      "n_streams": h[1], "n_map": h[2]}}
+                     for n, c, _, T, g, h in LEGS],
+            "bytes_per_step": step_bytes(),
+            "l2": "inputs larger than L2 (2.85 GB streamed per step, every leg with its own weights)",
+            "seeds": {n: s for n, _, s, _, _, _ in LEGS}}
+
+
+def head_bytes(T, head):
+    n_draft, S, n_map = head
+    return gen.lmhead_bytes(gen.VOCAB, gen.HIDDEN, T, n_map=n_map, n_streams=S, n_draft=n_draft)
+
+
+def leg_bytes(leg):
+    _, _, _, T, g, h = leg
+    b = sum(gen.gemm_bytes(T, K, N) for _, K, N in gen.GEMM_SHAPES) if g else 0
+    return b + (head_bytes(T, h) if h is not None else 0)
+
+
+def step_bytes():
+    return sum(leg_bytes(leg) for leg in LEGS)
+
+
+def kernels_per_call(T):
+    """Kernel launches of one library call: the stream kernel, plus the
+    activation conversion kernel when the call has more than one token tile
+    (T > 8)."""
+    return 2 if T > 8 else 1
 
 
 # ----------------------------------------------------------------------------
@@ -102,6 +156,25 @@ def recorded_traffic(kernel):
             if len(parts) >= 3 and not line.startswith("#") and parts[0] == kernel and parts[1] == digest:
                 return int(parts[2])
     return None
+
+
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":")[0].strip() in ("Model name", "Model Name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return platform.processor() or platform.machine()
 
 
 class ClockSampler:
@@ -176,178 +249,204 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------
-# workload
+# host inputs (shared by the GPU arm and the oracle timing)
+
+
+def host_leg(leg):
+    """Seeded host inputs of one leg: per GEMM (x, Wq, scales); for the head
+    (x, Wq, scales, drafts [S][n_draft], vocab_map or None)."""
+    name, _, seed, T, g, h = leg
+    rng = np.random.default_rng(seed)
+    out = {"gemms": [], "head": None}
+    if g:
+        for label, K, N in gen.GEMM_SHAPES:
+            Wq, sc = gen.weights(rng, N, K)
+            out["gemms"].append((label, K, N, gen.activations(rng, T, K), Wq, sc))
+    if h is not None:
+        n_draft, S, n_map = h
+        V, K = gen.VOCAB, gen.HIDDEN
+        Wq, sc = gen.weights(rng, V, K)
+        x = gen.activations(rng, T, K)
+        vm = gen.vocab_map(rng, V, n_map) if n_map else None
+        pool = vm if vm is not None else None
+        if pool is None:
+            drafts = rng.integers(0, V, size=(S, n_draft)).astype(np.int32)
+        else:
+            drafts = pool[rng.integers(0, pool.size, size=(S, n_draft))].astype(np.int32)
+        out["head"] = (x, Wq, sc, drafts, vm)
+    return out
+
+
+# ----------------------------------------------------------------------------
+# device workload
 
 
 class Workload:
-    """Device-resident inputs of the mtp_T4 step (seeded, synthetic).  The
-    step's per-call inputs (the four activation blocks and the drafts) are
-    views of one device arena, and its two outputs (accept_len, next_token)
-    of one int32 pair, so the end-to-end leg moves them with one copy each
-    way."""
+    """Device-resident inputs of the sweep step.  The per-call inputs of a
+    step (every call's activations and drafts) are views of one device
+    arena, and the verify results (accept_len, next_token of every verify
+    stream) of one int32 array, so the end-to-end leg moves them with one
+    copy each way."""
 
-    def __init__(self, torch, device, seed=2):
-        rng = np.random.default_rng(seed)
-        self.T = T_STEP
-        self.gemms = []
+    def __init__(self, torch, device):
         dev = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a).view(dt)).to(device)
-        self.host = {}
-        V, Kh = gen.VOCAB, gen.HIDDEN
-        # arena layout: x of each GEMM, x of the head, drafts (16-byte aligned)
-        sizes = [self.T * K * 2 for _, K, _ in gen.GEMM_SHAPES] + [self.T * Kh * 2, N_DRAFT * 4]
+        self.legs = []
+        hosts = [host_leg(leg) for leg in LEGS]
+        # arena: activations of every call, then drafts (16-byte aligned pieces)
+        pieces = []
+        for leg, hl in zip(LEGS, hosts):
+            for (_, K, N, x, _, _) in hl["gemms"]:
+                pieces.append(x.view(np.uint8).reshape(-1))
+            if hl["head"] is not None:
+                pieces.append(hl["head"][0].view(np.uint8).reshape(-1))
+                pieces.append(hl["head"][3].view(np.uint8).reshape(-1))
         offs, o = [], 0
-        for n in sizes:
+        for pc in pieces:
             offs.append(o)
-            o += (n + 15) // 16 * 16
-        self.arena = torch.zeros(o, dtype=torch.uint8, device=device)
-        view = lambda i, dt, shape: self.arena[offs[i]:offs[i] + sizes[i]].view(dt).view(shape)
-        for i, (label, K, N) in enumerate(gen.GEMM_SHAPES):
-            Wq, sc = gen.weights(rng, N, K)
-            x = gen.activations(rng, self.T, K)
-            self.host[label] = (x, Wq, sc)
-            xd = view(i, torch.int16, (self.T, K))
-            xd.copy_(dev(x, np.int16))
-            self.gemms.append(dict(label=label, K=K, N=N, x=xd, Wq=dev(Wq, np.int32),
-                                   sc=dev(sc, np.int16),
-                                   y=torch.empty((self.T, N), dtype=torch.bfloat16, device=device),
-                                   bytes=gen.gemm_bytes(self.T, K, N)))
-        K = Kh
-        Wq, sc = gen.weights(rng, V, K)
-        x = gen.activations(rng, self.T, K)
-        drafts = rng.integers(0, V, size=N_DRAFT).astype(np.int32)
-        self.host["head"] = (x, Wq, sc, drafts)
-        nh = len(gen.GEMM_SHAPES)
-        xh = view(nh, torch.int16, (self.T, K))
-        xh.copy_(dev(x, np.int16))
-        dr = view(nh + 1, torch.int32, (N_DRAFT,))
-        dr.copy_(torch.from_numpy(drafts).to(device))
-        self.out = torch.zeros(2, dtype=torch.int32, device=device)
-        self.head = dict(V=V, K=K, x=xh, Wq=dev(Wq, np.int32), sc=dev(sc, np.int16), drafts=dr,
-                         acc=self.out[0:1], nxt=self.out[1:2],
-                         bytes=gen.lmhead_bytes(V, K, self.T, n_streams=1, n_draft=N_DRAFT))
-        self.bytes_per_step = sum(g["bytes"] for g in self.gemms) + self.head["bytes"]
-        self.launches_per_step = sum(kernels_per_call(self.T, g["K"]) for g in self.gemms) + \
-            kernels_per_call(self.T, K)
+            o += (pc.size + 15) // 16 * 16
+        arena_host = np.zeros(o, np.uint8)
+        for pc, off in zip(pieces, offs):
+            arena_host[off:off + pc.size] = pc
+        self.arena = torch.from_numpy(arena_host).to(device)
+        n_out = sum(2 * h[1] for *_, h in LEGS if h is not None)
+        self.out = torch.zeros(n_out, dtype=torch.int32, device=device)
+        pi, oi = 0, 0
 
-    def gemm_part(self, sv, stream):
-        for g in self.gemms:
-            sv.w4a16_gemm(g["x"], g["Wq"], g["sc"], y=g["y"], stream=stream)
+        def view(i, dt, shape):
+            nb = pieces[i].size
+            return self.arena[offs[i]:offs[i] + nb].view(dt).view(shape)
 
-    def head_part(self, sv, stream):
-        h = self.head
-        sv.lmhead_verify(h["x"], h["Wq"], h["sc"], h["drafts"], accept_len=h["acc"],
-                         next_token=h["nxt"], stream=stream)
+        for leg, hl in zip(LEGS, hosts):
+            name, cfg, _, T, _, h = leg
+            calls = []
+            for (label, K, N, x, Wq, sc) in hl["gemms"]:
+                xd = view(pi, torch.int16, (T, K))
+                pi += 1
+                calls.append(dict(kind="gemm", label="gemm_%s_T%d" % (label, T), T=T, K=K, N=N, x=xd,
+                                  Wq=dev(Wq, np.int32), sc=dev(sc, np.int16),
+                                  y=torch.empty((T, N), dtype=torch.bfloat16, device=device),
+                                  bytes=gen.gemm_bytes(T, K, N)))
+            if h is not None:
+                n_draft, S, n_map = h
+                x, Wq, sc, drafts, vm = hl["head"]
+                xd = view(pi, torch.int16, (T, gen.HIDDEN))
+                dd = view(pi + 1, torch.int32, (S, n_draft))
+                pi += 2
+                acc = self.out[oi:oi + S]
+                nxt = self.out[oi + S:oi + 2 * S]
+                oi += 2 * S
+                label = ("lmhead_verify_restricted_T%d" % T if n_map
+                         else "lmhead_verify_T%d" % T if S == 1 else "lmhead_verify_%dx%d_T%d" % (S, n_draft + 1, T))
+                calls.append(dict(kind="head", label=label, T=T, S=S, n_draft=n_draft, x=xd,
+                                  Wq=dev(Wq, np.int32), sc=dev(sc, np.int16), drafts=dd,
+                                  vm=None if vm is None else dev(vm, np.int32), acc=acc, nxt=nxt,
+                                  bytes=head_bytes(T, h)))
+            self.legs.append(dict(name=name, config=cfg, T=T, calls=calls, bytes=leg_bytes(leg)))
+        self.bytes_per_step = sum(l["bytes"] for l in self.legs)
+        self.launches_per_step = sum(kernels_per_call(c["T"]) for l in self.legs for c in l["calls"])
+        self.host = hosts
+
+    @staticmethod
+    def call(sv, c, stream):
+        if c["kind"] == "gemm":
+            sv.w4a16_gemm(c["x"], c["Wq"], c["sc"], y=c["y"], stream=stream)
+        else:
+            sv.lmhead_verify_batched(c["x"], c["Wq"], c["sc"], c["drafts"], vocab_map=c["vm"],
+                                     accept_len=c["acc"], next_token=c["nxt"], stream=stream)
+
+    def calls(self):
+        return [c for l in self.legs for c in l["calls"]]
 
     def step(self, sv, stream):
-        self.gemm_part(sv, stream)
-        self.head_part(sv, stream)
+        for c in self.calls():
+            self.call(sv, c, stream)
 
-    def capture_e2e(self, torch, sv, in_host, out_host):
-        """One CUDA graph of a whole end-to-end step: the pinned host->device
-        copy of the step's inputs, the step's library calls, and the
-        device->host copy of accept_len and next_token."""
+    def capture(self, torch, sv, groups, prologue=None, epilogue=None):
+        """One CUDA graph per group of calls (programmatic dependent launch
+        between the kernels inside a graph); prologue/epilogue (optional)
+        are captured before the first and after the last group's calls."""
         side = torch.cuda.Stream()
         side.wait_stream(torch.cuda.current_stream())
-        g = torch.cuda.CUDAGraph()
+        graphs = []
         with torch.cuda.stream(side):
-            with torch.cuda.graph(g, stream=side):
-                self.arena.copy_(in_host, non_blocking=True)
-                self.gemm_part(sv, side)
-                self.head_part(sv, side)
-                out_host.copy_(self.out, non_blocking=True)
+            for i, grp in enumerate(groups):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=side):
+                    if prologue is not None and i == 0:
+                        prologue()
+                    for c in grp:
+                        self.call(sv, c, side)
+                    if epilogue is not None and i == len(groups) - 1:
+                        epilogue()
+                graphs.append(g)
         torch.cuda.current_stream().wait_stream(side)
         torch.cuda.synchronize()
-        return g
-
-    def capture(self, torch, sv):
-        """One CUDA graph of the whole step (the three GEMMs, then the head
-        pass, with programmatic dependent launch between them), as a decode
-        engine issues a verify cycle; and the same step as two graphs (the
-        GEMMs; the head), so that an event between them can time the head's
-        own launch inside the step."""
-        side = torch.cuda.Stream()
-        side.wait_stream(torch.cuda.current_stream())
-        g, g1, g2 = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-        with torch.cuda.stream(side):
-            with torch.cuda.graph(g, stream=side):
-                self.gemm_part(sv, side)
-                self.head_part(sv, side)
-            with torch.cuda.graph(g1, stream=side):
-                self.gemm_part(sv, side)
-            with torch.cuda.graph(g2, stream=side):
-                self.head_part(sv, side)
-        torch.cuda.current_stream().wait_stream(side)
-        torch.cuda.synchronize()
-        return g, g1, g2
+        return graphs
 
 
 # ----------------------------------------------------------------------------
 # CPU oracle timing (the cpu_baseline leg and the reference arm)
 
 
-def kernels_per_call(T, K):
-    """Kernel launches of one library call: the stream kernel, plus the
-    activation conversion kernel when the call has more than one token tile
-    (T > 8)."""
-    return 2 if T > 8 else 1
-
-
-def oracle_sample_step(oracle, host, rows_frac):
-    """Run the oracle on a bounded sample of one step: the first
-    rows_frac of every GEMM's output rows and of the lm_head rows, with the
-    same x.  Returns (algorithmic bytes of the sample, seconds)."""
+def oracle_sample_step(oracle, hosts, rows_frac):
+    """Run the oracle on a bounded sample of one sweep step: the first
+    rows_frac of every GEMM's output rows and of every head's scored rows
+    (for a restricted head, of its vocab_map), with the same x; the verify
+    itself on the sampled logits.  Returns (algorithmic bytes, seconds)."""
     t0 = time.perf_counter()
     nbytes = 0
-    for label, K, N in gen.GEMM_SHAPES:
-        x, Wq, sc = host[label]
-        n = max(1, int(N * rows_frac))
-        oracle.w4a16_gemm(x, Wq[:n], sc[:n], T_STEP, K, n)
-        nbytes += gen.gemm_bytes(T_STEP, K, n)
-    x, Wq, sc, drafts = host["head"]
-    V, K = Wq.shape[0], Wq.shape[1] * 8
-    n = max(1, int(V * rows_frac))
-    lg = oracle.lmhead_logits(x, Wq[:n], sc[:n], K, T_STEP, n)
-    a, _, _ = oracle.argmax(lg)
-    oracle.verify(a, drafts)
-    nbytes += gen.lmhead_bytes(n, K, T_STEP, n_streams=1, n_draft=N_DRAFT)
+    for leg, hl in zip(LEGS, hosts):
+        _, _, _, T, _, h = leg
+        for (label, K, N, x, Wq, sc) in hl["gemms"]:
+            n = max(1, int(N * rows_frac))
+            oracle.w4a16_gemm(x, Wq[:n], sc[:n], T, K, n)
+            nbytes += gen.gemm_bytes(T, K, n)
+        if h is not None:
+            n_draft, S, n_map = h
+            x, Wq, sc, drafts, vm = hl["head"]
+            V, K = Wq.shape[0], Wq.shape[1] * 8
+            if vm is None:
+                n = max(1, int(V * rows_frac))
+                lg = oracle.lmhead_logits(x, Wq[:n], sc[:n], K, T, n)
+                a, _, _ = oracle.argmax(lg)
+                nbytes += gen.lmhead_bytes(n, K, T, n_streams=S, n_draft=n_draft)
+            else:
+                n = max(1, int(vm.size * rows_frac))
+                lg = oracle.lmhead_logits(x, Wq, sc, K, T, V, rows=vm[:n])
+                a, _, _ = oracle.argmax(lg, ids=vm[:n])
+                nbytes += gen.lmhead_bytes(V, K, T, n_map=n, n_streams=S, n_draft=n_draft)
+            for s in range(S):
+                oracle.verify(a[s * (n_draft + 1):(s + 1) * (n_draft + 1)], drafts[s])
     return nbytes, time.perf_counter() - t0
 
 
-def host_only_workload(seed=2):
-    rng = np.random.default_rng(seed)
-    host = {}
-    for label, K, N in gen.GEMM_SHAPES:
-        Wq, sc = gen.weights(rng, N, K)
-        x = gen.activations(rng, T_STEP, K)
-        host[label] = (x, Wq, sc)
-    V, K = gen.VOCAB, gen.HIDDEN
-    Wq, sc = gen.weights(rng, V, K)
-    x = gen.activations(rng, T_STEP, K)
-    drafts = rng.integers(0, V, size=N_DRAFT).astype(np.int32)
-    host["head"] = (x, Wq, sc, drafts)
-    return host
+def timed_oracle(oracle, hosts, budget_s, calib_frac=0.002):
+    """The oracle on a row fraction of the sweep sized to fill about budget_s
+    (calibrated on calib_frac of the rows).  Returns (GB/s, fraction, s)."""
+    _, dt = oracle_sample_step(oracle, hosts, calib_frac)
+    frac = min(1.0, max(1e-4, calib_frac * budget_s / max(dt, 1e-4)))
+    b, t = oracle_sample_step(oracle, hosts, frac)
+    return b / t / 1e9, frac, t
 
 
-def cpu_baseline(host, budget_s=12.0):
-    """The oracle timed on the host cores on a bounded sample of the step:
-    calibrated on 1% of the rows, then a row fraction (and, once that reaches
-    every row, a number of whole passes) that fills about budget_s."""
+def cpu_baseline(hosts, budget_s=10.0, budget_1core_s=5.0):
+    """The oracle timed on the host cores (OpenMP over output rows, all
+    cores, then one core) on bounded samples of the sweep step."""
     import oracle
     oracle.build()
-    nb, dt = oracle_sample_step(oracle, host, 0.01)
-    frac = min(1.0, max(0.01, 0.01 * budget_s / max(dt, 1e-3)))
-    passes = 1
-    if frac >= 1.0:
-        passes = max(1, int(round(budget_s / max(dt * 100, 1e-3))))
-    tot_b, tot_t = 0, 0.0
-    for _ in range(passes):
-        b, t = oracle_sample_step(oracle, host, frac)
-        tot_b += b
-        tot_t += t
-    return {"value": tot_b / tot_t / 1e9, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": "%.1f%% of the output rows of each of the 3 GEMMs and of the 248,320 "
-                      "lm_head rows (T=4), %d pass%s, %.1f s" % (100 * frac, passes, "" if passes == 1 else "es",
-                                                             tot_t)}
+    ncpu = os.cpu_count() or 1
+    oracle.set_num_threads(ncpu)
+    cores = oracle.num_threads()
+    v_all, f_all, t_all = timed_oracle(oracle, hosts, budget_s)
+    oracle.set_num_threads(1)
+    v_one, f_one, t_one = timed_oracle(oracle, hosts, budget_1core_s)
+    oracle.set_num_threads(ncpu)
+    return {"value": v_all, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": "the first %.2f%% of the output rows of every GEMM and of every head's scored rows "
+                      "in the six legs of the sweep, one pass, %.1f s" % (100 * f_all, t_all),
+            "one_core": {"value": v_one, "unit": "GB/s", "cores": 1,
+                         "sample": "the first %.3f%% of the rows, one pass, %.1f s" % (100 * f_one, t_one)},
+            "cpu_model": cpu_model(), "nproc": ncpu}
 
 
 # ----------------------------------------------------------------------------
@@ -361,32 +460,47 @@ def run_reference(args, rank, world):
         return
     import oracle
     oracle.build()
-    host = host_only_workload()
+    ncpu = os.cpu_count() or 1
+    oracle.set_num_threads(ncpu)
+    hosts = [host_leg(leg) for leg in LEGS]
     budget_total = 150.0
-    nb, dt = oracle_sample_step(oracle, host, 0.002)
     per_step = budget_total / max(1, args.steps + args.warmup)
-    frac = min(1.0, max(0.0005, 0.002 * per_step / max(dt, 1e-4)))
+    _, dt = oracle_sample_step(oracle, hosts, 0.001)
+    frac = min(1.0, max(1e-4, 0.001 * per_step / max(dt, 1e-4)))
     for _ in range(args.warmup):
-        oracle_sample_step(oracle, host, frac)
+        oracle_sample_step(oracle, hosts, frac)
     tot_b, tot_t = 0, 0.0
     for _ in range(args.steps):
-        b, t = oracle_sample_step(oracle, host, frac)
+        b, t = oracle_sample_step(oracle, hosts, frac)
         tot_b += b
         tot_t += t
     value = tot_b / tot_t / 1e9
-    sample = ("%.2f%% of the output rows of each GEMM and of the lm_head rows per step (T=4)"
-              % (100 * frac))
+    sample = ("the first %.3f%% of the output rows of every GEMM and of every head's scored rows in the "
+              "six legs of the sweep, per step" % (100 * frac))
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * tot_t / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "T": T_STEP, "n_draft": N_DRAFT,
-                       "gemms": [list(s) for s in gen.GEMM_SHAPES], "V": gen.VOCAB,
-                       "K_head": gen.HIDDEN, "l2": "oracle on host cores"},
+            "config": workload_config(),
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.num_threads(),
-                             "kind": "oracle", "sample": sample},
+                             "kind": "oracle", "sample": sample, "cpu_model": cpu_model(), "nproc": ncpu},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def time_groups(torch, graphs, stream, reps):
+    """Mean time (ms) of each graph of `graphs`, replayed in order `reps`
+    times with an event between consecutive graphs."""
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(graphs) + 1)] for _ in range(reps)]
+    torch.cuda.synchronize()
+    for r in range(reps):
+        evs[r][0].record(stream)
+        for i, g in enumerate(graphs):
+            g.replay()
+            evs[r][i + 1].record(stream)
+    torch.cuda.synchronize()
+    return [float(np.mean([evs[r][i].elapsed_time(evs[r][i + 1]) for r in range(reps)]))
+            for i in range(len(graphs))]
 
 
 def run_ours(args, rank, world, local_rank):
@@ -420,11 +534,10 @@ def run_ours(args, rank, world, local_rank):
         wl.step(sv, stream)
         torch.cuda.synchronize()
 
-    g_step, g_gemm, g_head = wl.capture(torch, sv)
+    calls = wl.calls()
+    (g_step,) = wl.capture(torch, sv, [calls])
     for _ in range(3):
         g_step.replay()
-        g_gemm.replay()
-        g_head.replay()
     torch.cuda.synchronize()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
@@ -440,43 +553,43 @@ def run_ours(args, rank, world, local_rank):
     barrier()
     sampler.stop()
     ms = ev0.elapsed_time(ev1)
-    # the head's own launch time inside the step: the same steps as two
-    # graphs with an event between the GEMMs and the head (the event costs
-    # the programmatic overlap of the down GEMM's tail with the head's start,
-    # so this slightly understates the head's rate in the step above)
-    head_steps = max(1, min(args.steps, 200))
-    ev_mid = [torch.cuda.Event(enable_timing=True) for _ in range(head_steps)]
-    ev_end = [torch.cuda.Event(enable_timing=True) for _ in range(head_steps)]
-    barrier()
-    torch.cuda.synchronize()
-    for i in range(head_steps):
-        g_gemm.replay()
-        ev_mid[i].record(stream)
-        g_head.replay()
-        ev_end[i].record(stream)
-    torch.cuda.synchronize()
-    barrier()
-    head_ms = float(np.mean([a.elapsed_time(b) for a, b in zip(ev_mid, ev_end)]))
     ms = reduce_max(dist, ms, device)
     assert sv.last_device_error() == 0
 
-    # end to end through the public API with host buffers: per step the
-    # activations and drafts go host->device from pinned memory (one copy of
-    # the input arena), the step's captured calls run (the two graphs), the
-    # verify result comes back (one copy of accept_len and next_token) and
-    # the host waits for it, as a decode loop must before its next step.
+    # Inside the step: each leg's time (one graph per leg, an event between
+    # legs), and each call's launch time (one graph per call, an event
+    # between calls).  An event boundary costs the programmatic overlap of
+    # one kernel's tail with the next one's start, so these slightly
+    # understate the rates inside the one-graph step above.
+    reps = max(1, min(args.steps, 200))
+    leg_graphs = wl.capture(torch, sv, [l["calls"] for l in wl.legs])
+    call_graphs = wl.capture(torch, sv, [[c] for c in calls])
+    for g in leg_graphs + call_graphs:
+        g.replay()
+    leg_ms = time_groups(torch, leg_graphs, stream, reps)
+    call_ms = time_groups(torch, call_graphs, stream, reps)
+    leg_ms = [reduce_max(dist, v, device) for v in leg_ms]
+    call_ms = [reduce_max(dist, v, device) for v in call_ms]
+    assert sv.last_device_error() == 0
+
+    # End to end through the public API with host buffers: per step the
+    # activations and drafts of every call go host->device from pinned
+    # memory (one copy of the input arena), the step's library calls run and
+    # the verify results come back (one copy), and the host waits for them,
+    # as a decode loop must before its next step.  Two ways: the copies and
+    # calls captured in one CUDA graph replayed per step (a graph-capturing
+    # engine), and every call made through the C ABI per step (no graph).
     in_host = wl.arena.cpu().pin_memory()
-    out_host = torch.empty(2, dtype=torch.int32).pin_memory()
-    out_host.fill_(-7)
+    out_host = torch.empty(wl.out.numel(), dtype=torch.int32).pin_memory()
     h2d = in_host.numel() * in_host.element_size()
     d2h = out_host.numel() * out_host.element_size()
     e2e_steps = max(1, min(args.steps, 200))
-    # the copies are nodes of the step's graph: one launch per step runs the
-    # host->device copy, the kernels and the device->host copy
-    g_e2e = wl.capture_e2e(torch, sv, in_host, out_host)
+    (g_e2e,) = wl.capture(torch, sv, [calls], prologue=lambda: wl.arena.copy_(in_host, non_blocking=True),
+                          epilogue=lambda: out_host.copy_(wl.out, non_blocking=True))
+    out_host.fill_(-7)
     g_e2e.replay()
     torch.cuda.synchronize()
-    assert int(out_host[0]) >= 0, "the end-to-end graph did not return the verify result"
+    assert int(out_host.min()) >= 0, "the end-to-end graph did not return the verify results"
     barrier()
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
@@ -487,8 +600,20 @@ def run_ours(args, rank, world, local_rank):
         stream.synchronize()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    e2e_ms = reduce_max(dist, e2e_ms, device)
+    e2e_ms = reduce_max(dist, e0.elapsed_time(e1) / e2e_steps, device)
+    # uncaptured: every step calls the C ABI through the binding
+    out_host.fill_(-7)
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        wl.arena.copy_(in_host, non_blocking=True)
+        wl.step(sv, stream)
+        out_host.copy_(wl.out, non_blocking=True)
+        stream.synchronize()
+    eager_ms = reduce_max(dist, (time.perf_counter() - t0) * 1e3 / e2e_steps, device)
+    assert int(out_host.min()) >= 0
+    assert sv.last_device_error() == 0
 
     breakdown = per_kernel_breakdown(torch, sv, device, stream) if args.breakdown else None
 
@@ -497,41 +622,58 @@ def run_ours(args, rank, world, local_rank):
     peak, peak_kind = measured_peaks()
     ms_per_step = ms / args.steps
     value = job_gbs(world, wl.bytes_per_step, args.steps, ms)
-    achieved = wl.head["bytes"] / (head_ms * 1e-3) / 1e9
+    # the dominant kernel: the call with the largest share of the step
+    i_dom = int(np.argmax(call_ms))
+    dom = calls[i_dom]
+    achieved = dom["bytes"] / (call_ms[i_dom] * 1e-3) / 1e9
     clocks = sampler.summary(t_host0, t_host1)
     cpu = cpu_baseline(wl.host) if (world == 1 and not args.no_cpu_baseline) else None
+    legs_out = []
+    ci = 0
+    for l, lm in zip(wl.legs, leg_ms):
+        gbs = l["bytes"] / (lm * 1e-3) / 1e9
+        cl = []
+        for c in l["calls"]:
+            cm = call_ms[ci]
+            ci += 1
+            cg = c["bytes"] / (cm * 1e-3) / 1e9
+            cl.append({"call": c["label"], "us": round(cm * 1e3, 2), "GB/s": round(cg, 1),
+                       "frac_of_8TBps": round(cg / NOMINAL_HBM_GBS, 4), "frac_of_measured_copy": round(cg / peak, 4)})
+        legs_out.append({"leg": l["name"], "config": l["config"], "T": l["T"], "bytes": l["bytes"],
+                         "ms": round(lm, 5), "GB/s": round(gbs, 1), "frac_of_8TBps": round(gbs / NOMINAL_HBM_GBS, 4),
+                         "frac_of_measured_copy": round(gbs / peak, 4), "calls": cl})
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16 x int4 -> fp32",
         "data": "synthetic (seeded; shapes of a 27B-class decoder)",
-        "config": {"workload": WORKLOAD, "T": T_STEP, "n_draft": N_DRAFT,
-                   "gemms": [list(s) for s in gen.GEMM_SHAPES], "V": gen.VOCAB,
-                   "K_head": gen.HIDDEN, "bytes_per_step": wl.bytes_per_step,
-                   "l2": "inputs larger than L2 (820 MB streamed per step; each weight set is "
-                         "evicted by the others before it is read again)",
-                   "parallelism": "replicas" if world > 1 else "1 GPU"},
+        "config": dict(workload_config(), parallelism="replicas" if world > 1 else "1 GPU"),
         "frac_of_8TBps": value / world / NOMINAL_HBM_GBS,
         "frac_of_measured_copy": value / world / peak,
-        "roofline": {"kernel": "lmhead_verify (w4a16_stream_kernel<1,true>)", "bound": "hbm",
+        "legs": legs_out,
+        "roofline": {"kernel": "%s (w4a16_stream_kernel)" % dom["label"], "bound": "hbm",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind
                      if peak_kind == "measured" else "fallback",
-                     "algorithmic_bytes_per_launch": wl.head["bytes"],
-                     "avg_launch_ms": head_ms,
-                     "traffic": recorded_traffic("lmhead_verify_T4")},
+                     "algorithmic_bytes_per_launch": dom["bytes"],
+                     "avg_launch_ms": call_ms[i_dom],
+                     "share_of_step": call_ms[i_dom] / sum(call_ms),
+                     "traffic": recorded_traffic(dom["label"])},
         "clocks": clocks,
         "e2e": {"value": job_gbs(world, wl.bytes_per_step, 1, e2e_ms), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms, "steps": e2e_steps,
-                "per_step": "one CUDA graph per step holding a pinned host->device copy of the step's "
-                            "activations and drafts, the step's library calls and a device->host copy "
-                            "of accept_len and next_token; stream synchronize"},
+                "per_step": "one CUDA graph per step holding a pinned host->device copy of every call's "
+                            "activations and drafts, the step's library calls and a device->host copy of the "
+                            "verify results; stream synchronize",
+                "uncaptured": {"value": job_gbs(world, wl.bytes_per_step, 1, eager_ms), "unit": "GB/s",
+                               "ms_per_step": eager_ms, "steps": e2e_steps,
+                               "per_step": "the same copies and every library call made through the C ABI "
+                                           "(ctypes binding) each step, no graph; host wall clock"}},
         "gpu_launches": wl.launches_per_step * args.steps,
-        "timing": "each timed step replays one CUDA graph (3 GEMM launches, then the head launch, "
-                  "programmatic dependent launch between them); the roofline's head launch time comes "
-                  "from a second pass of up to 200 steps replaying the GEMMs and the head as two graphs "
-                  "with an event between them",
+        "timing": "each timed step replays one CUDA graph of the whole sweep (programmatic dependent launch "
+                  "between its kernels); leg and call times come from further passes of up to 200 steps "
+                  "replaying one graph per leg, then one graph per call, with events between them",
         "cpu_baseline": cpu,
     }
     if breakdown is not None:
@@ -666,15 +808,19 @@ def per_kernel_breakdown(torch, sv, device, stream, reps=50):
 
 
 def run_ncu_case(args):
-    """A small, fixed workload for ncu captures: a few launches of one kernel."""
+    """A small, fixed workload for ncu captures: three launches of one call.
+    gemm: one GEMM shape (--ncu-shape) at --ncu-T rows; head: the lm_head
+    verify of --ncu-streams streams of --ncu-T / streams rows; restricted:
+    the 40,960-id head at --ncu-T rows; sampled / rescored at T = 4."""
     import torch
     import speculative_verify_gb300 as sv
     sv.load()
     device = torch.device("cuda", 0)
     rng = np.random.default_rng(5)
     dev = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a).view(dt)).to(device)
+    T = args.ncu_T
     if args.ncu_case == "restricted":
-        V, K, T = gen.VOCAB, gen.HIDDEN, T_STEP
+        V, K = gen.VOCAB, gen.HIDDEN
         Wq, sc = gen.weights(rng, V, K)
         Wd, sd = dev(Wq, np.int32), dev(sc, np.int16)
         x = dev(gen.activations(rng, T, K), np.int16)
@@ -683,43 +829,51 @@ def run_ncu_case(args):
         for _ in range(3):
             sv.lmhead_verify(x, Wd, sd, drafts, vocab_map=vm)
     elif args.ncu_case in ("head", "sampled", "rescored"):
-        V, K, T = gen.VOCAB, gen.HIDDEN, T_STEP
+        V, K = gen.VOCAB, gen.HIDDEN
         Wq, sc = gen.weights(rng, V, K)
         Wd, sd = dev(Wq, np.int32), dev(sc, np.int16)
-        x = dev(gen.activations(rng, T, K), np.int16)
-        drafts = torch.zeros(T - 1, dtype=torch.int32, device=device)
         if args.ncu_case == "head":
+            S = args.ncu_streams
+            x = dev(gen.activations(rng, T, K), np.int16)
+            drafts = torch.zeros((S, T // S - 1), dtype=torch.int32, device=device)
             for _ in range(3):
-                sv.lmhead_verify(x, Wd, sd, drafts)
-        elif args.ncu_case == "sampled":
-            u = torch.rand(2 * T, dtype=torch.float32, device=device)
-            for _ in range(3):
-                sv.lmhead_verify_sampled(x, Wd, sd, drafts, u, temperature=0.7, top_k=20, top_p=0.95)
+                sv.lmhead_verify_batched(x, Wd, sd, drafts)
         else:
-            Wbf = (torch.randn((V, K), dtype=torch.float32, device=device) * 0.02).to(torch.bfloat16)
-            for _ in range(3):
-                sv.lmhead_verify_rescored(x, Wd, sd, Wbf, drafts, top_k=16)
+            T = 4
+            x = dev(gen.activations(rng, T, K), np.int16)
+            drafts = torch.zeros(T - 1, dtype=torch.int32, device=device)
+            if args.ncu_case == "sampled":
+                u = torch.rand(2 * T, dtype=torch.float32, device=device)
+                for _ in range(3):
+                    sv.lmhead_verify_sampled(x, Wd, sd, drafts, u, temperature=0.7, top_k=20, top_p=0.95)
+            else:
+                Wbf = (torch.randn((V, K), dtype=torch.float32, device=device) * 0.02).to(torch.bfloat16)
+                for _ in range(3):
+                    sv.lmhead_verify_rescored(x, Wd, sd, Wbf, drafts, top_k=16)
     else:
-        label, K, N = gen.GEMM_SHAPES[1]
+        label, K, N = {s[0]: s for s in gen.GEMM_SHAPES}[args.ncu_shape]
         Wq, sc = gen.weights(rng, N, K)
         Wd, sd = dev(Wq, np.int32), dev(sc, np.int16)
-        x = dev(gen.activations(rng, T_STEP, K), np.int16)
+        x = dev(gen.activations(rng, T, K), np.int16)
         for _ in range(3):
             sv.w4a16_gemm(x, Wd, sd)
     torch.cuda.synchronize()
     assert sv.last_device_error() == 0
-    print(json.dumps({"ncu_case": args.ncu_case, "ok": True}))
+    print(json.dumps({"ncu_case": args.ncu_case, "T": T, "ok": True}))
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--breakdown", action="store_true", help="also time each kernel alone at T=1..32")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ncu-case", choices=["head", "gemm", "sampled", "rescored", "restricted"], default=None)
+    ap.add_argument("--ncu-T", type=int, default=4)
+    ap.add_argument("--ncu-streams", type=int, default=1)
+    ap.add_argument("--ncu-shape", choices=[s[0] for s in gen.GEMM_SHAPES], default="gate_up")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

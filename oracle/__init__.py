@@ -77,6 +77,8 @@ def _load():
     lib.or_verify.restype = c_int
     lib.or_num_threads.restype = c_int
     lib.or_num_threads.argtypes = []
+    lib.or_set_num_threads.restype = None
+    lib.or_set_num_threads.argtypes = [c_int]
     lib.or_verify.argtypes = [_i32p, ctypes.c_void_p, c_int, ctypes.POINTER(ctypes.c_int32),
                               ctypes.POINTER(ctypes.c_int32)]
     _lib = lib
@@ -86,6 +88,11 @@ def _load():
 def num_threads() -> int:
     """Threads the oracle's OpenMP regions use."""
     return int(_load().or_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads later OpenMP regions of the oracle use (n >= 1)."""
+    _load().or_set_num_threads(int(n))
 
 
 def _ptr(a):

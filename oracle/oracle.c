@@ -313,3 +313,11 @@ int or_num_threads(void)
     }
     return n;
 }
+
+/* Set the number of threads later OpenMP regions of this library use
+   (n >= 1); used to time the oracle on one core as well as on all. */
+void or_set_num_threads(int n)
+{
+    if (n >= 1)
+        omp_set_num_threads(n);
+}
