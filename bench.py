@@ -325,7 +325,7 @@ class Workload:
                 calls.append(dict(kind="gemm", label="gemm_%s_T%d" % (label, T), T=T, K=K, N=N, x=xd,
                                   Wq=dev(Wq, np.int32), sc=dev(sc, np.int16),
                                   y=torch.empty((T, N), dtype=torch.bfloat16, device=device),
-                                  bytes=gen.gemm_bytes(T, K, N)))
+                                  bytes=gen.gemm_bytes(T, K, N), wbytes=N * K // 2 + N * K // 64))
             if h is not None:
                 n_draft, S, n_map = h
                 x, Wq, sc, drafts, vm = hl["head"]
@@ -340,7 +340,8 @@ class Workload:
                 calls.append(dict(kind="head", label=label, T=T, S=S, n_draft=n_draft, x=xd,
                                   Wq=dev(Wq, np.int32), sc=dev(sc, np.int16), drafts=dd,
                                   vm=None if vm is None else dev(vm, np.int32), acc=acc, nxt=nxt,
-                                  bytes=head_bytes(T, h)))
+                                  bytes=head_bytes(T, h),
+                                  wbytes=(n_map or gen.VOCAB) * (gen.HIDDEN // 2 + gen.HIDDEN // 64)))
             self.legs.append(dict(name=name, config=cfg, T=T, calls=calls, bytes=leg_bytes(leg)))
         self.bytes_per_step = sum(l["bytes"] for l in self.legs)
         self.launches_per_step = sum(kernels_per_call(c["T"]) for l in self.legs for c in l["calls"])
@@ -488,19 +489,87 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def time_groups(torch, graphs, stream, reps):
-    """Mean time (ms) of each graph of `graphs`, replayed in order `reps`
-    times with an event between consecutive graphs."""
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(graphs) + 1)] for _ in range(reps)]
-    torch.cuda.synchronize()
-    for r in range(reps):
-        evs[r][0].record(stream)
-        for i, g in enumerate(graphs):
+def read_ceilings(torch, sv, device, stream, sizes, reps=40):
+    """GB/s of the read-ceiling kernel (sv_hbm_read: only reads, same launch
+    structure as the GEMMs) for each byte count, timed like the calls: back
+    to back in one graph, rotating over enough buffers to exceed L2 twice."""
+    out = {}
+    sink = torch.empty(4096, dtype=torch.int32, device=device)
+    for nb in sizes:
+        copies = max(2, int(np.ceil(2 * 129 * 2 ** 20 / nb)))
+        bufs = [torch.empty((nb + 15) // 16 * 16, dtype=torch.uint8, device=device) for _ in range(copies)]
+        for b in bufs:
+            b.fill_(1)
+        fn = lambda i: sv.hbm_read(bufs[i % copies], sink, nbytes=nb // 16 * 16)
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                for i in range(reps):
+                    fn(i)
+        stream.wait_stream(side)
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        out[nb] = (nb // 16 * 16) * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9
+        del bufs, g
+        torch.cuda.empty_cache()
+    return out
+
+
+def graph_ms(torch, g, stream, reps, rounds=3):
+    """Time (ms) of one replay of graph g: the least over `rounds` runs of
+    `reps` back-to-back replays, CUDA events on `stream`."""
+    best = None
+    for _ in range(rounds):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
             g.replay()
-            evs[r][i + 1].record(stream)
-    torch.cuda.synchronize()
-    return [float(np.mean([evs[r][i].elapsed_time(evs[r][i + 1]) for r in range(reps)]))
-            for i in range(len(graphs))]
+        e1.record(stream)
+        torch.cuda.synchronize()
+        t = e0.elapsed_time(e1) / reps
+        best = t if best is None else min(best, t)
+    return best
+
+
+def time_calls_in_step(torch, sv, wl, stream, reps):
+    """Each call's and each leg's time inside the step, by ablation: the
+    step's graph time minus the time of the same graph without that call
+    (or leg).  Events between the calls would cost each boundary the
+    programmatic overlap of one kernel's tail with the next one's start
+    (several microseconds), so the step is never cut; the full step is timed
+    again after every ablated graph and the median taken."""
+    calls = wl.calls()
+    (g_full,) = wl.capture(torch, sv, [calls])
+    g_full.replay()
+    fulls = [graph_ms(torch, g_full, stream, reps)]
+    call_ms = []
+    for i in range(len(calls)):
+        (g,) = wl.capture(torch, sv, [calls[:i] + calls[i + 1:]])
+        g.replay()
+        t = graph_ms(torch, g, stream, reps)
+        fulls.append(graph_ms(torch, g_full, stream, reps))
+        call_ms.append(t)
+        del g
+    leg_ms = []
+    for l in wl.legs:
+        ids = {id(c) for c in l["calls"]}
+        (g,) = wl.capture(torch, sv, [[c for c in calls if id(c) not in ids]])
+        g.replay()
+        leg_ms.append(graph_ms(torch, g, stream, reps))
+        fulls.append(graph_ms(torch, g_full, stream, reps))
+        del g
+    full = float(np.median(fulls))
+    return ([full - t for t in call_ms], [full - t for t in leg_ms], full,
+            "ablation: the step's graph time minus that of the step without the call (or leg); "
+            "%d replays per timing, the least of 3 timings, the full step's median over %d timings"
+            % (reps, len(fulls)))
 
 
 def run_ours(args, rank, world, local_rank):
@@ -556,20 +625,11 @@ def run_ours(args, rank, world, local_rank):
     ms = reduce_max(dist, ms, device)
     assert sv.last_device_error() == 0
 
-    # Inside the step: each leg's time (one graph per leg, an event between
-    # legs), and each call's launch time (one graph per call, an event
-    # between calls).  An event boundary costs the programmatic overlap of
-    # one kernel's tail with the next one's start, so these slightly
-    # understate the rates inside the one-graph step above.
-    reps = max(1, min(args.steps, 200))
-    leg_graphs = wl.capture(torch, sv, [l["calls"] for l in wl.legs])
-    call_graphs = wl.capture(torch, sv, [[c] for c in calls])
-    for g in leg_graphs + call_graphs:
-        g.replay()
-    leg_ms = time_groups(torch, leg_graphs, stream, reps)
-    call_ms = time_groups(torch, call_graphs, stream, reps)
-    leg_ms = [reduce_max(dist, v, device) for v in leg_ms]
+    # Inside the step: each call's and each leg's time, by ablation.
+    reps = max(3, min(args.steps, 50))
+    call_ms, leg_ms, full_ms, timing_how = time_calls_in_step(torch, sv, wl, stream, reps)
     call_ms = [reduce_max(dist, v, device) for v in call_ms]
+    leg_ms = [reduce_max(dist, v, device) for v in leg_ms]
     assert sv.last_device_error() == 0
 
     # End to end through the public API with host buffers: per step the
@@ -615,6 +675,7 @@ def run_ours(args, rank, world, local_rank):
     assert int(out_host.min()) >= 0
     assert sv.last_device_error() == 0
 
+    ceilings = read_ceilings(torch, sv, device, stream, sorted({c["wbytes"] for c in calls}))
     breakdown = per_kernel_breakdown(torch, sv, device, stream) if args.breakdown else None
 
     if rank != 0:
@@ -637,8 +698,10 @@ def run_ours(args, rank, world, local_rank):
             cm = call_ms[ci]
             ci += 1
             cg = c["bytes"] / (cm * 1e-3) / 1e9
+            ceil = ceilings[c["wbytes"]]
             cl.append({"call": c["label"], "us": round(cm * 1e3, 2), "GB/s": round(cg, 1),
-                       "frac_of_8TBps": round(cg / NOMINAL_HBM_GBS, 4), "frac_of_measured_copy": round(cg / peak, 4)})
+                       "frac_of_8TBps": round(cg / NOMINAL_HBM_GBS, 4), "frac_of_measured_copy": round(cg / peak, 4),
+                       "read_ceiling": {"GB/s": round(ceil, 1), "frac": round(cg / ceil, 4)}})
         legs_out.append({"leg": l["name"], "config": l["config"], "T": l["T"], "bytes": l["bytes"],
                          "ms": round(lm, 5), "GB/s": round(gbs, 1), "frac_of_8TBps": round(gbs / NOMINAL_HBM_GBS, 4),
                          "frac_of_measured_copy": round(gbs / peak, 4), "calls": cl})
@@ -657,7 +720,7 @@ def run_ours(args, rank, world, local_rank):
                      if peak_kind == "measured" else "fallback",
                      "algorithmic_bytes_per_launch": dom["bytes"],
                      "avg_launch_ms": call_ms[i_dom],
-                     "share_of_step": call_ms[i_dom] / sum(call_ms),
+                     "share_of_step": call_ms[i_dom] / full_ms,
                      "traffic": recorded_traffic(dom["label"])},
         "clocks": clocks,
         "e2e": {"value": job_gbs(world, wl.bytes_per_step, 1, e2e_ms), "unit": "GB/s",
@@ -672,8 +735,7 @@ def run_ours(args, rank, world, local_rank):
                                            "(ctypes binding) each step, no graph; host wall clock"}},
         "gpu_launches": wl.launches_per_step * args.steps,
         "timing": "each timed step replays one CUDA graph of the whole sweep (programmatic dependent launch "
-                  "between its kernels); leg and call times come from further passes of up to 200 steps "
-                  "replaying one graph per leg, then one graph per call, with events between them",
+                  "between its kernels); call and leg times inside the step: %s" % timing_how,
         "cpu_baseline": cpu,
     }
     if breakdown is not None:

@@ -131,6 +131,51 @@ int lmhead_verify_batched(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *s
                           int32_t *accept_len, int32_t *next_token, sv_stream stream);
 
 /*
+ * sv_verify_cycle -- one verify cycle's weight reads in one call: the
+ * given W4A16 GEMMs in order, then (when verify != NULL) the lm_head pass
+ * with greedy verification of n_streams blocks, all enqueued on `stream`
+ * with programmatic dependent launch, so each kernel streams its weights
+ * while the previous one drains and the GPU does not wait for the host
+ * between them.  Capturing this call in a CUDA graph gives the graph-per-
+ * cycle form of the page "qwen-warp and llamAmpere: two RTX 3090 engines
+ * for Qwen3.8, and what each one calls the same answer" (section "What
+ * makes each one a 3090 engine": a decode cycle is one CUDA graph); the
+ * page "OpenJet Engine: CUDA LLM inference for Qwen3.8-27B" (section "How
+ * it works") runs the same cycle -- the main model over the T = 1 +
+ * n_draft rows, then lm_head and verification on the device -- as one
+ * persistent kernel.
+ *   gemms [n_gemms] (host array, 0 <= n_gemms <= SV_CYCLE_MAX_GEMMS): each
+ *   entry as the arguments of w4a16_gemm.  verify (host pointer or NULL):
+ *   the arguments of lmhead_verify_batched.  The GEMMs' inputs are the
+ *   caller's: this call does not chain one GEMM's output into the next.
+ *   Every argument of every entry is checked before anything is enqueued
+ *   (errors as w4a16_gemm and lmhead_verify_batched; SV_ERR_SHAPE when
+ *   there is nothing to do); after that only a failed launch (SV_ERR_CUDA)
+ *   can stop the call, leaving the kernels before it enqueued.
+ */
+#define SV_CYCLE_MAX_GEMMS 64
+typedef struct sv_gemm_call {
+    const sv_bf16 *x;          /* [T][K] */
+    const uint32_t *Wq;        /* [N][K/8] */
+    const sv_bf16 *scales;     /* [N][K/128] */
+    int T, K, N;
+    sv_bf16 *y;                /* [T][N], written */
+} sv_gemm_call;
+typedef struct sv_verify_call {
+    const sv_bf16 *x;          /* [n_streams * (1 + n_draft)][K] */
+    const uint32_t *Wq;        /* [V][K/8] */
+    const sv_bf16 *scales;     /* [V][K/128] */
+    int K;
+    const int32_t *drafts;     /* [n_streams][n_draft] */
+    int n_draft, n_streams;
+    const int32_t *vocab_map;  /* [n_map] or NULL */
+    int n_map, V;
+    int32_t *accept_len;       /* [n_streams], written */
+    int32_t *next_token;       /* [n_streams], written */
+} sv_verify_call;
+int sv_verify_cycle(const sv_gemm_call *gemms, int n_gemms, const sv_verify_call *verify, sv_stream stream);
+
+/*
  * lmhead_argmax -- the same pass without the draft comparison: for each of
  * the T rows of x, ids[t] = the argmax token id (lowest id on ties) and
  * vals[t] = its fp32 logit.  This is the greedy step of a restricted draft
@@ -309,6 +354,21 @@ int sv_last_device_error(int32_t *out);
  *   per-device scratch counters (split-tile arrivals, argmax keys, CTA
  *   completions) back to zero, so that a run which gave up on a wait cannot
  *   affect later calls. */
+
+/*
+ * sv_hbm_read -- a measurement aid: one launch that only reads `bytes` of
+ * device memory at src (bulk copies into shared memory, one thread block
+ * per SM, equal contiguous shares, programmatic dependent launch -- the
+ * launch structure of the GEMM kernels) and writes one checksum word per
+ * block to sink.  Timed back to back on a weight matrix's byte count, it is
+ * the read rate a kernel of that size reaches with nothing else to do, the
+ * ceiling the GEMMs are reported against.  No source page has a
+ * counterpart.
+ *   src: 16-byte aligned, bytes a multiple of 16 (>= 16); sink: one uint32
+ *   per SM of the device (written).  Errors: SV_ERR_NULL, SV_ERR_SHAPE,
+ *   SV_ERR_ALIGN, SV_ERR_CUDA, SV_ERR_NOMEM.
+ */
+int sv_hbm_read(const void *src, size_t bytes, uint32_t *sink, sv_stream stream);
 
 /*
  * sv_debug_set_wait_stall -- a test hook for the bounded waits.  With

@@ -23,6 +23,20 @@ DEVERR_TIMEOUT = 0x2
 _lib = None
 
 
+class GemmCall(ctypes.Structure):
+    """sv_gemm_call of include/specverify.h."""
+    _fields_ = [("x", ctypes.c_void_p), ("Wq", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("T", ctypes.c_int), ("K", ctypes.c_int), ("N", ctypes.c_int), ("y", ctypes.c_void_p)]
+
+
+class VerifyCall(ctypes.Structure):
+    """sv_verify_call of include/specverify.h."""
+    _fields_ = [("x", ctypes.c_void_p), ("Wq", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("K", ctypes.c_int), ("drafts", ctypes.c_void_p), ("n_draft", ctypes.c_int),
+                ("n_streams", ctypes.c_int), ("vocab_map", ctypes.c_void_p), ("n_map", ctypes.c_int),
+                ("V", ctypes.c_int), ("accept_len", ctypes.c_void_p), ("next_token", ctypes.c_void_p)]
+
+
 class SpecVerifyError(RuntimeError):
     def __init__(self, fn, status):
         self.status = status
@@ -82,6 +96,10 @@ def load(path: str | None = None):
     lib.sv_status_string.restype = ctypes.c_char_p
     lib.sv_last_device_error.argtypes = [ctypes.POINTER(ctypes.c_int32)]
     lib.sv_last_device_error.restype = ci
+    lib.sv_hbm_read.argtypes = [vp, ctypes.c_size_t, vp, vp]
+    lib.sv_hbm_read.restype = ci
+    lib.sv_verify_cycle.argtypes = [ctypes.POINTER(GemmCall), ci, ctypes.POINTER(VerifyCall), vp]
+    lib.sv_verify_cycle.restype = ci
     lib.sv_debug_set_wait_stall.argtypes = [ctypes.c_uint32]
     lib.sv_debug_set_wait_stall.restype = ci
     _lib = lib
@@ -254,6 +272,49 @@ def lmhead_verify_noalloc(x, Wq, scales, drafts, vocab_map=None, accept_len=None
         _ptr(x), _ptr(Wq), _ptr(scales), K, _ptr(drafts) if n_draft else None, n_draft,
         _ptr(vocab_map), n_map, V, _ptr(accept_len), _ptr(next_token), _stream(stream)))
     return accept_len, next_token
+
+
+def verify_cycle(gemms, verify=None, stream=None):
+    """One verify cycle's weight reads in one call (sv_verify_cycle).
+
+    gemms: a list of (x [T][K], Wq [N][K/8], scales [N][K/128], y [T][N])
+    CUDA tensors; verify: None or a dict with x, Wq, scales, drafts
+    [n_streams][n_draft], accept_len and next_token ([n_streams] int32), and
+    optionally vocab_map.  Outputs are written in place."""
+    arr = (GemmCall * max(1, len(gemms)))()
+    for i, (x, Wq, scales, y) in enumerate(gemms):
+        _bits16(x, "x"), _words(Wq, "Wq"), _bits16(scales, "scales"), _bits16(y, "y")
+        T, K = x.shape
+        N = Wq.shape[0]
+        if Wq.shape[1] * 8 != K or tuple(scales.shape) != (N, K // 128) or tuple(y.shape) != (T, N):
+            raise ValueError("shape mismatch in GEMM %d" % i)
+        arr[i] = GemmCall(x.data_ptr(), Wq.data_ptr(), scales.data_ptr(), T, K, N, y.data_ptr())
+    vptr = None
+    if verify is not None:
+        x, Wq, scales, drafts = verify["x"], verify["Wq"], verify["scales"], verify["drafts"]
+        _bits16(x, "x"), _words(Wq, "Wq"), _bits16(scales, "scales")
+        S, n_draft = drafts.shape
+        if n_draft:
+            _i32(drafts, "drafts")
+        vm = verify.get("vocab_map")
+        if vm is not None:
+            _i32(vm, "vocab_map")
+        acc, nxt = _i32(verify["accept_len"], "accept_len"), _i32(verify["next_token"], "next_token")
+        K = x.shape[1]
+        v = VerifyCall(x.data_ptr(), Wq.data_ptr(), scales.data_ptr(), K,
+                       drafts.data_ptr() if n_draft else None, n_draft, S,
+                       None if vm is None else vm.data_ptr(), 0 if vm is None else vm.numel(), Wq.shape[0],
+                       acc.data_ptr(), nxt.data_ptr())
+        vptr = ctypes.byref(v)
+    _check("sv_verify_cycle", load().sv_verify_cycle(arr, len(gemms), vptr, _stream(stream)))
+
+
+def hbm_read(src, sink, nbytes=None, stream=None):
+    """Read nbytes (default: all) of the CUDA tensor src in one launch of the
+    read-ceiling kernel (sv_hbm_read); sink: an int32/uint32 CUDA tensor with
+    one entry per SM."""
+    n = src.numel() * src.element_size() if nbytes is None else int(nbytes)
+    _check("sv_hbm_read", load().sv_hbm_read(_ptr(src), n, _ptr(sink), _stream(stream)))
 
 
 def lmhead_argmax(x, Wq, scales, vocab_map=None, ids=None, vals=None, stream=None):

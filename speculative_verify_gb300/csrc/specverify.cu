@@ -12,9 +12,11 @@
 #include <mutex>
 
 #include "draft_list.cuh"
+#include "hbm_read.cuh"
 #include "rescore.cuh"
 #include "specverify.h"
 #include "w4a16_stream.cuh"
+#include "w4a16_wide.cuh"
 
 namespace sv {
 namespace {
@@ -30,6 +32,7 @@ struct DeviceState {
     int sms = 0;
     int smem_optin = 0;
     float *part = nullptr;
+    float *wpart = nullptr;     // split-tile partials of the wide kernel, [sms][2][WIDE_PART_FLOATS]
     unsigned *ctr = nullptr;
     unsigned long long *keys = nullptr;
     unsigned *done = nullptr;
@@ -66,6 +69,13 @@ cudaError_t raise_smem_limit(int bytes)
 {
     return cudaFuncSetAttribute(w4a16_stream_kernel<NT, HEAD, GATHER, XRES>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+template <int NT, bool HEAD, int NCW>
+cudaError_t raise_smem_limit_wide(int bytes)
+{
+    return cudaFuncSetAttribute(w4a16_wide_kernel<NT, HEAD, NCW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                bytes);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -117,8 +127,9 @@ int device_state(DeviceState **out)
         const size_t ctr_bytes = static_cast<size_t>(prop.multiProcessorCount) * sizeof(unsigned);
         const size_t keys_bytes = TMAX * sizeof(unsigned long long);
         const size_t x16_bytes = static_cast<size_t>(X16_MAX_GROUPS) * TMAX * XSTR;
+        const size_t wpart_bytes = static_cast<size_t>(prop.multiProcessorCount) * 2 * WIDE_PART_FLOATS * sizeof(float);
         const size_t total = part_bytes + ctr_bytes + keys_bytes + 2 * sizeof(unsigned) + 256 + x16_bytes +
-                             TMAX * sizeof(float) + 256 + RS_SCRATCH_BYTES;
+                             TMAX * sizeof(float) + 256 + RS_SCRATCH_BYTES + 256 + wpart_bytes;
         uint8_t *base = nullptr;
         if (cudaMalloc(&base, total) != cudaSuccess) {
             cudaGetLastError();
@@ -152,6 +163,9 @@ int device_state(DeviceState **out)
         st.sdone = st.rdone + 1;
         st.row_acc = reinterpret_cast<int32_t *>(base + off + RS_TMAX * RS_KMAX * 8 + 16);
         st.row_tok = st.row_acc + RS_TMAX;
+        off += RS_SCRATCH_BYTES;
+        off = (off + 255) & ~static_cast<size_t>(255);
+        st.wpart = reinterpret_cast<float *>(base + off);
         st.x16_max_groups = X16_MAX_GROUPS;
         cudaError_t e = cudaSuccess;
         e = e != cudaSuccess ? e : raise_smem_limit<1, false, false, false>(optin);
@@ -166,6 +180,10 @@ int device_state(DeviceState **out)
         e = e != cudaSuccess ? e : raise_smem_limit<1, true, true, true>(optin);
         e = e != cudaSuccess ? e : raise_smem_limit<2, true, true, false>(optin);
         e = e != cudaSuccess ? e : raise_smem_limit<4, true, true, false>(optin);
+        e = e != cudaSuccess ? e : cudaFuncSetAttribute(hbm_read_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                        HR_NST * HR_STAGE + 2 * HR_NST * 8);
+        e = e != cudaSuccess ? e : raise_smem_limit_wide<2, false, 8>(optin);
+        e = e != cudaSuccess ? e : raise_smem_limit_wide<2, true, 8>(optin);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(rescore_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      optin - RS_STATIC_SMEM_SLACK);
@@ -318,9 +336,109 @@ int launch(Params p, const DeviceState &st, cudaStream_t stream)
     return SV_OK;
 }
 
+// Shared-memory layout of a wide launch (offsets in bytes, 128-byte
+// aligned): nst stages (one group of the tile's packed weights + the
+// group's activation block) | the two-slot scale ring | the head's per-warp
+// key table | mbarriers, the time-out flag and the split-tile decision word.
+template <int NT, bool HEAD, int NCW>
+int plan_layout_wide(Params &p, int smem_optin, int *smem_total)
+{
+    constexpr int RT = wide_rt(NCW);
+    p.xslot_bytes = 8 * NT * XSTR;
+    p.stage_bytes = RT * 64 + p.xslot_bytes;              // a multiple of 128
+    const int ring_bytes = 2 * RT * 16;
+    const int kt_bytes = HEAD ? NCW * TMAX * 8 : 0;
+    int nst = (smem_optin - ring_bytes - kt_bytes - 256) / p.stage_bytes;
+    if (nst > 8) nst = 8;           // the scale ring's reuse rule needs at most 9 stages
+    if (nst < 2) return SV_ERR_SHAPE;
+    p.nst = nst;
+    int off = nst * p.stage_bytes;
+    p.off_sbuf = off;
+    off += ring_bytes;
+    p.off_bk = off;
+    off += kt_bytes;
+    p.off_bars = off;
+    off += (2 * nst + 2) * 8;
+    *smem_total = off;
+    return off <= smem_optin ? SV_OK : SV_ERR_SHAPE;
+}
+
+template <int NT, bool HEAD, int NCW>
+int launch_wide(Params p, const DeviceState &st, cudaStream_t stream)
+{
+    constexpr int RT = wide_rt(NCW);
+    constexpr unsigned BOX_ROWS = RT < 256 ? RT : 256;
+    if (p.G > st.x16_max_groups) return SV_ERR_SHAPE;
+    int smem = 0;
+    int rc = plan_layout_wide<NT, HEAD, NCW>(p, st.smem_optin, &smem);
+    if (rc != SV_OK) return rc;
+    CUtensorMap tmW, tmS;
+    std::memset(&tmW, 0, sizeof tmW);
+    std::memset(&tmS, 0, sizeof tmS);
+    rc = encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, p.Wq, static_cast<unsigned long long>(p.K / 8),
+                   static_cast<unsigned long long>(p.n_rows), 16, BOX_ROWS);
+    if (rc != SV_OK) return rc;
+    rc = encode_2d(&tmS, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, p.scales, static_cast<unsigned long long>(p.G),
+                   static_cast<unsigned long long>(p.n_rows), 8, BOX_ROWS);
+    if (rc != SV_OK) return rc;
+    const long long tiles = (static_cast<long long>(p.n_rows) + RT - 1) / RT;
+    p.U = tiles * p.G;
+    long long B = st.sms;
+    if (B > p.U) B = p.U;
+    p.part = st.wpart;
+    p.ctr = st.ctr;
+    p.keys = st.keys;
+    p.done = st.done;
+    p.err = st.err;
+    p.stall_ns = g_stall_ns.load(std::memory_order_relaxed);
+    p.x16 = st.x16;
+    p.xinv = st.xinv;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // the activations, converted into ready-made group blocks first
+    cfg.gridDim = dim3(static_cast<unsigned>(8 * NT));
+    cfg.blockDim = dim3(XP_THREADS);
+    cfg.dynamicSmemBytes = 0;
+    if (cudaLaunchKernelEx(&cfg, xprep_kernel, p.x, p.T, p.K, 8 * NT, st.x16, st.xinv) != cudaSuccess) {
+        cudaGetLastError();
+        return SV_ERR_CUDA;
+    }
+    cfg.gridDim = dim3(static_cast<unsigned>(B));
+    cfg.blockDim = dim3(static_cast<unsigned>((NCW + 1) * 32));
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    if (cudaLaunchKernelEx(&cfg, w4a16_wide_kernel<NT, HEAD, NCW>, p, tmW, tmS) != cudaSuccess) {
+        cudaGetLastError();
+        return SV_ERR_CUDA;
+    }
+    return SV_OK;
+}
+
+// The wide kernel (512-row tiles) serves calls with two token tiles
+// (9 <= T <= 16) and at least two 512-row tiles per SM -- an lm_head-sized
+// pass -- when the scales' rows are 16-byte multiples (G % 8 == 0, a TMA
+// requirement of the scale boxes), the rows are contiguous (no vocab_map)
+// and the device state has its partial-sum area.  Measured on GB300 at
+// V = 248,320, K = 5,120: 4.05 TB/s at T = 16 against 3.47 for 64-row
+// tiles.  Smaller calls, and four token tiles (T > 16, where the 512-row
+// kernel's 168-register cap spills and runs 10 % slower), stay on the
+// 64-row kernel; the 256-row variant measured slower everywhere.
+template <bool HEAD, bool GATHER>
+bool use_wide(const Params &p, const DeviceState &st)
+{
+    if (GATHER || !st.wpart || p.T <= 8 || p.T > 16 || (p.G % 8) != 0) return false;
+    const long long tiles512 = (static_cast<long long>(p.n_rows) + 511) / 512;
+    return tiles512 >= 2LL * st.sms;
+}
+
 template <bool HEAD, bool GATHER>
 int dispatch(Params &p, const DeviceState &st, cudaStream_t stream)
 {
+    if (use_wide<HEAD, GATHER>(p, st)) return launch_wide<2, HEAD, 8>(p, st, stream);
     if (p.T <= 8) {
         if (static_cast<long long>(p.T + 1) * (2LL * p.K + 16) <= XRES_MAX_BYTES &&
             p.U >= static_cast<long long>(XRES_MIN_UNITS) * st.sms)
@@ -339,10 +457,9 @@ int check_common(const void *x, const void *Wq, const void *scales, int T, int K
     return SV_OK;
 }
 
-int head_call(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, int K, int T,
-              const int32_t *vocab_map, int n_map, int V, int mode, const int32_t *drafts,
-              int n_draft, int n_streams, int32_t *accept_len, int32_t *next_token,
-              int32_t *ids, float *vals, cudaStream_t stream)
+int check_head(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, int K, int T,
+               const int32_t *vocab_map, int n_map, int V, int mode, const int32_t *drafts,
+               int n_draft, int32_t *accept_len, int32_t *next_token, int32_t *ids, float *vals)
 {
     int rc = check_common(x, Wq, scales, T, K);
     if (rc != SV_OK) return rc;
@@ -360,6 +477,34 @@ int head_call(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, int K
         if (!ids) return SV_ERR_NULL;
         if (!aligned4(ids) || (vals && !aligned4(vals))) return SV_ERR_ALIGN;
     }
+    return SV_OK;
+}
+
+int check_batched(int n_draft, int n_streams)
+{
+    if (n_draft < 0 || n_draft > 31 || n_streams < 1) return SV_ERR_SHAPE;
+    if (static_cast<long long>(n_streams) * (n_draft + 1) > TMAX) return SV_ERR_SHAPE;
+    return SV_OK;
+}
+
+int check_gemm(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, int T, int K, int N, sv_bf16 *y)
+{
+    int rc = check_common(x, Wq, scales, T, K);
+    if (rc != SV_OK) return rc;
+    if (!y) return SV_ERR_NULL;
+    if (N < 1) return SV_ERR_SHAPE;
+    if (!aligned16(y)) return SV_ERR_ALIGN;
+    return SV_OK;
+}
+
+int head_call(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, int K, int T,
+              const int32_t *vocab_map, int n_map, int V, int mode, const int32_t *drafts,
+              int n_draft, int n_streams, int32_t *accept_len, int32_t *next_token,
+              int32_t *ids, float *vals, cudaStream_t stream)
+{
+    int rc = check_head(x, Wq, scales, K, T, vocab_map, n_map, V, mode, drafts, n_draft, accept_len, next_token,
+                        ids, vals);
+    if (rc != SV_OK) return rc;
     DeviceState *st = nullptr;
     rc = device_state(&st);
     if (rc != SV_OK) return rc;
@@ -714,11 +859,8 @@ int w4a16_gemm(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, int 
                sv_bf16 *y, sv_stream stream)
 {
     using namespace sv;
-    int rc = check_common(x, Wq, scales, T, K);
+    int rc = check_gemm(x, Wq, scales, T, K, N, y);
     if (rc != SV_OK) return rc;
-    if (!y) return SV_ERR_NULL;
-    if (N < 1) return SV_ERR_SHAPE;
-    if (!aligned16(y)) return SV_ERR_ALIGN;
     DeviceState *st = nullptr;
     rc = device_state(&st);
     if (rc != SV_OK) return rc;
@@ -742,12 +884,46 @@ int lmhead_verify_batched(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *s
                           const int32_t *vocab_map, int n_map, int V, int32_t *accept_len,
                           int32_t *next_token, sv_stream stream)
 {
-    if (n_draft < 0 || n_draft > 31 || n_streams < 1) return SV_ERR_SHAPE;
-    const long long T = static_cast<long long>(n_streams) * (n_draft + 1);
-    if (T > sv::TMAX) return SV_ERR_SHAPE;
-    return sv::head_call(x, Wq, scales, K, static_cast<int>(T), vocab_map, n_map, V, 0, drafts,
+    const int rc = sv::check_batched(n_draft, n_streams);
+    if (rc != SV_OK) return rc;
+    return sv::head_call(x, Wq, scales, K, n_streams * (n_draft + 1), vocab_map, n_map, V, 0, drafts,
                          n_draft, n_streams, accept_len, next_token, nullptr, nullptr,
                          reinterpret_cast<cudaStream_t>(stream));
+}
+
+int sv_verify_cycle(const sv_gemm_call *gemms, int n_gemms, const sv_verify_call *verify, sv_stream stream)
+{
+    using namespace sv;
+    if (n_gemms < 0 || n_gemms > SV_CYCLE_MAX_GEMMS || (n_gemms == 0 && !verify)) return SV_ERR_SHAPE;
+    if (n_gemms > 0 && !gemms) return SV_ERR_NULL;
+    // every argument first: on an error nothing is enqueued
+    for (int i = 0; i < n_gemms; ++i) {
+        const sv_gemm_call &g = gemms[i];
+        const int rc = check_gemm(g.x, g.Wq, g.scales, g.T, g.K, g.N, g.y);
+        if (rc != SV_OK) return rc;
+    }
+    if (verify) {
+        const sv_verify_call &v = *verify;
+        int rc = check_batched(v.n_draft, v.n_streams);
+        if (rc != SV_OK) return rc;
+        rc = check_head(v.x, v.Wq, v.scales, v.K, v.n_streams * (v.n_draft + 1), v.vocab_map, v.n_map, v.V, 0,
+                        v.drafts, v.n_draft, v.accept_len, v.next_token, nullptr, nullptr);
+        if (rc != SV_OK) return rc;
+    }
+    DeviceState *st = nullptr;
+    int rc = device_state(&st);
+    if (rc != SV_OK) return rc;
+    for (int i = 0; i < n_gemms; ++i) {
+        const sv_gemm_call &g = gemms[i];
+        rc = w4a16_gemm(g.x, g.Wq, g.scales, g.T, g.K, g.N, g.y, stream);
+        if (rc != SV_OK) return rc;
+    }
+    if (verify) {
+        const sv_verify_call &v = *verify;
+        rc = lmhead_verify_batched(v.x, v.Wq, v.scales, v.K, v.drafts, v.n_draft, v.n_streams, v.vocab_map,
+                                   v.n_map, v.V, v.accept_len, v.next_token, stream);
+    }
+    return rc;
 }
 
 int lmhead_verify(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, int K,
@@ -800,6 +976,33 @@ int sv_last_device_error(int32_t *out)
     }
     if (cudaDeviceSynchronize() != cudaSuccess) return SV_ERR_CUDA;
     *out = v;
+    return SV_OK;
+}
+
+int sv_hbm_read(const void *src, size_t bytes, uint32_t *sink, sv_stream stream)
+{
+    using namespace sv;
+    if (!src || !sink) return SV_ERR_NULL;
+    if (bytes < 16 || (bytes % 16) != 0) return SV_ERR_SHAPE;
+    if (!aligned16(src) || !aligned4(sink)) return SV_ERR_ALIGN;
+    DeviceState *st = nullptr;
+    int rc = device_state(&st);
+    if (rc != SV_OK) return rc;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(st->sms));
+    cfg.blockDim = dim3(64);
+    cfg.dynamicSmemBytes = HR_NST * HR_STAGE + 2 * HR_NST * 8;
+    if (cudaLaunchKernelEx(&cfg, hbm_read_kernel, static_cast<const uint8_t *>(src),
+                           static_cast<unsigned long long>(bytes), sink, st->err) != cudaSuccess) {
+        cudaGetLastError();
+        return SV_ERR_CUDA;
+    }
     return SV_OK;
 }
 

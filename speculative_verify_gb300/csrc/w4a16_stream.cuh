@@ -361,6 +361,56 @@ __device__ __forceinline__ void stage_tile_meta(const Params &p, int tile, uint8
     if (lane == 0) mbar_arrive(bar);
 }
 
+// Grid-level end of a head launch, run by one warp of every CTA: lane t
+// (< T) holds the CTA's best key of token t.  The keys go to the grid's
+// per-token maxima (atomicMax), then the CTA counts itself in; the last CTA
+// turns the maxima into ids and writes them (argmax mode) or runs the
+// greedy verify of every stream, and leaves the keys and the counter at 0.
+__device__ __forceinline__ void head_grid_tail(const Params &p, unsigned long long best, int lane, int B)
+{
+    const int T = p.T;
+    if (lane < T && best != 0ull) atomicMax(&p.keys[lane], best);
+    __threadfence();
+    __syncwarp();
+    unsigned last = 0;
+    if (lane == 0) last = (atomicAdd(p.done, 1u) == static_cast<unsigned>(B - 1));
+    if (__shfl_sync(0xFFFFFFFFu, last, 0)) {
+        __threadfence();
+        int32_t a = -1;
+        unsigned long long kk = 0ull;
+        if (lane < T) {
+            kk = __ldcg(&p.keys[lane]);
+            a = (kk == 0ull) ? -1 : key_id(kk);
+            p.keys[lane] = 0ull;
+        }
+        if (p.mode == 1) {
+            if (lane < T) {
+                p.ids[lane] = a;
+                if (p.vals) p.vals[lane] = (kk == 0ull) ? __int_as_float(0x7fc00000) : key_value(kk);
+            }
+        } else {
+            const int rows_per = p.n_draft + 1;
+            const int sidx = lane < p.n_streams ? lane : 0;
+            int acc = -1, nxt = -1;
+            for (int i = 0; i <= p.n_draft; ++i) {
+                const int ai = __shfl_sync(0xFFFFFFFFu, a, (sidx * rows_per + i) & 31);
+                if (acc < 0) {
+                    if (i == p.n_draft || p.drafts[static_cast<size_t>(sidx) * p.n_draft + i] != ai) {
+                        acc = i;
+                        nxt = ai;
+                    }
+                }
+            }
+            if (lane < p.n_streams) {
+                p.accept_len[lane] = acc;
+                p.next_token[lane] = nxt;
+            }
+        }
+        __syncwarp();
+        if (lane == 0) *p.done = 0u;
+    }
+}
+
 template <int NT, bool HEAD, bool GATHER, bool XRES>
 __global__ void __launch_bounds__((consumer_warps(NT, XRES, GATHER) + 2) * 32, 1)
 w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tmW,
@@ -753,46 +803,7 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
                     best = v > best ? v : best;
                 }
             }
-            if (lane < T && best != 0ull) atomicMax(&p.keys[lane], best);
-            __threadfence();
-            __syncwarp();
-            unsigned last = 0;
-            if (lane == 0) last = (atomicAdd(p.done, 1u) == static_cast<unsigned>(B - 1));
-            if (__shfl_sync(0xFFFFFFFFu, last, 0)) {
-                __threadfence();
-                int32_t a = -1;
-                unsigned long long kk = 0ull;
-                if (lane < T) {
-                    kk = __ldcg(&p.keys[lane]);
-                    a = (kk == 0ull) ? -1 : key_id(kk);
-                    p.keys[lane] = 0ull;
-                }
-                if (p.mode == 1) {
-                    if (lane < T) {
-                        p.ids[lane] = a;
-                        if (p.vals) p.vals[lane] = (kk == 0ull) ? __int_as_float(0x7fc00000) : key_value(kk);
-                    }
-                } else {
-                    const int rows_per = p.n_draft + 1;
-                    const int sidx = lane < p.n_streams ? lane : 0;
-                    int acc = -1, nxt = -1;
-                    for (int i = 0; i <= p.n_draft; ++i) {
-                        const int ai = __shfl_sync(0xFFFFFFFFu, a, (sidx * rows_per + i) & 31);
-                        if (acc < 0) {
-                            if (i == p.n_draft || p.drafts[static_cast<size_t>(sidx) * p.n_draft + i] != ai) {
-                                acc = i;
-                                nxt = ai;
-                            }
-                        }
-                    }
-                    if (lane < p.n_streams) {
-                        p.accept_len[lane] = acc;
-                        p.next_token[lane] = nxt;
-                    }
-                }
-                __syncwarp();
-                if (lane == 0) *p.done = 0u;
-            }
+            head_grid_tail(p, best, lane, B);
         }
         return;
     }

@@ -427,6 +427,121 @@ def test_restricted_head_full_size(sv, oracle, n_draft):
 
 
 # --------------------------------------------------------------------------
+# calls with more than one n8 token tile (9 <= T <= 32): 64-row tiles, and
+# for lm_head-sized calls at 9 <= T <= 16 (at least two 512-row tiles per
+# SM, K a multiple of 1024) 512-row tiles
+
+
+def wide_rows_512(K, ragged=29):
+    """A row count for which the library takes 512-row tiles (at least 2 x
+    the SM count of them); ragged last tile, whose second 256-row half is
+    partly filled."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return 2 * sms * 512 + 3 * 512 - ragged
+
+
+def wide_rows_512_half(K):
+    """As wide_rows_512, with the last tile's second 256-row half empty."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return 2 * sms * 512 + 3 * 512 + 100
+
+
+@pytest.mark.parametrize("T,K,N", [
+    (9, 1024, 777),      # two token tiles, one real token in the second, ragged tile
+    (12, 5120, 600),
+    (16, 2048, 1500),
+    (17, 1024, 300),     # four token tiles, one real token in the third
+    (24, 3072, 1000),
+    (32, 5120, 2000),
+    (32, 1024, 70),      # one tile shared by 16 CTAs
+    (32, 17408, 70),     # one tile shared by 136 CTAs (one unit each)
+    (16, 17408, 5120),   # the down GEMM's shape at T = 16
+])
+def test_multi_tile_gemm_matches_oracle(sv, oracle, T, K, N):
+    rng = np.random.default_rng(9000 + 31 * T + K + N)
+    Wq, sc = gen.weights(rng, N, K)
+    x = gen.activations(rng, T, K)
+    y32, _ = oracle.w4a16_gemm(x, Wq, sc, T, K, N)
+    y = sv.w4a16_gemm(dev_bits16(x), dev_words(Wq), dev_bits16(sc))
+    torch.cuda.synchronize()
+    assert_gemm_close(y.view(torch.int16).cpu().numpy().view(np.uint16), y32)
+    # same call again: identical bits (fixed reduction order of split tiles)
+    y2 = sv.w4a16_gemm(dev_bits16(x), dev_words(Wq), dev_bits16(sc))
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
+    assert sv.last_device_error() == 0
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("T,K,rows", [(9, 1024, "ragged"), (12, 2048, "ragged"), (16, 1024, "half"),
+                                      (16, 3072, "ragged")])
+def test_wide_gemm_512_row_tiles_sampled_rows(sv, oracle, T, K, rows):
+    """GEMMs with enough rows for 512-row tiles; the oracle recomputes 640
+    sampled rows and the last tile; a repeat call gives identical bits."""
+    N = wide_rows_512(K) if rows == "ragged" else wide_rows_512_half(K)
+    rng = np.random.default_rng(9500 + T + K)
+    Wq, sc = gen.weights(rng, N, K)
+    x = gen.activations(rng, T, K)
+    y = sv.w4a16_gemm(dev_bits16(x), dev_words(Wq), dev_bits16(sc))
+    torch.cuda.synchronize()
+    yg = y.view(torch.int16).cpu().numpy().view(np.uint16)
+    rows = np.unique(np.concatenate([rng.choice(N, 576, replace=False), np.arange(N - 600, N)]))
+    y32, _ = oracle.w4a16_gemm(x, Wq[rows], sc[rows], T, K, rows.size)
+    assert_gemm_close(yg[:, rows], y32)
+    y2 = sv.w4a16_gemm(dev_bits16(x), dev_words(Wq), dev_bits16(sc))
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
+    assert sv.last_device_error() == 0
+
+
+@pytest.mark.slow
+def test_wide_gemm_activation_dynamic_range(sv, oracle):
+    """The wide-range rows (2^100, 2^-100, spread over 2^+-40, outliers),
+    repeated to 16 token rows, on 512-row tiles (sampled rows)."""
+    K, T = 1024, 16
+    N = wide_rows_512(K)
+    rng = np.random.default_rng(4300 + K)
+    Wq, sc = gen.weights(rng, N, K)
+    x = np.concatenate([wide_range_activations(rng, K)] * (T // 4))
+    y = sv.w4a16_gemm(dev_bits16(x), dev_words(Wq), dev_bits16(sc))
+    torch.cuda.synchronize()
+    yg = y.view(torch.int16).cpu().numpy().view(np.uint16)
+    rows = np.unique(np.concatenate([rng.choice(N, 400, replace=False), np.arange(N - 100, N)]))
+    y32, _ = oracle.w4a16_gemm(x, Wq[rows], sc[rows], T, K, rows.size)
+    assert_gemm_close(yg[:, rows], y32)
+
+
+@pytest.mark.parametrize("V,K,n_draft,n_streams", [
+    (4000, 1024, 12, 1),     # 13 rows, two token tiles
+    (3000, 2048, 7, 2),      # two streams of 8 rows
+    (2500, 1024, 15, 2),     # 32 rows
+    (5000, 3072, 10, 2),     # 22 rows, ragged third token tile
+    (6000, 1024, 31, 1),     # 32 rows, one stream
+])
+def test_multi_tile_verify_matches_oracle(sv, oracle, V, K, n_draft, n_streams):
+    run_head_case(sv, oracle, 9700 + V + K + n_draft, V, K, n_draft, n_streams, 0)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("K,n_draft,n_streams,rows", [
+    (1024, 7, 2, "ragged"),      # two streams of 8 rows
+    (1024, 8, 1, "half"),        # 9 rows, one real token in the second token tile
+    (2048, 12, 1, "ragged"),     # 13 rows
+    (1024, 3, 4, "ragged"),      # four streams of 4 rows
+    (1024, 15, 1, "half"),       # 16 rows
+])
+def test_wide_verify_512_row_tiles(sv, oracle, K, n_draft, n_streams, rows):
+    """Heads with enough rows for 512-row tiles at 9 <= T <= 16."""
+    V = wide_rows_512(K) if rows == "ragged" else wide_rows_512_half(K)
+    run_head_case(sv, oracle, 9801 + K + n_draft, V, K, n_draft, n_streams, 0)
+
+
+@pytest.mark.slow
+def test_verify_two_streams_T16_full_size(sv, oracle):
+    run_head_case(sv, oracle, 316, gen.VOCAB, gen.HIDDEN, 7, 2, 0)
+
+
+# --------------------------------------------------------------------------
 # bounded waits: a wait that runs out is reported, and later calls are clean
 
 
