@@ -351,9 +351,13 @@ class Workload:
     def call(sv, c, stream):
         if c["kind"] == "gemm":
             sv.w4a16_gemm(c["x"], c["Wq"], c["sc"], y=c["y"], stream=stream)
-        else:
-            sv.lmhead_verify_batched(c["x"], c["Wq"], c["sc"], c["drafts"], vocab_map=c["vm"],
+        elif c["vm"] is None:
+            sv.lmhead_verify_batched(c["x"], c["Wq"], c["sc"], c["drafts"],
                                      accept_len=c["acc"], next_token=c["nxt"], stream=stream)
+        else:
+            # the draft vocabulary is model data: no kernel of the step writes it
+            sv.lmhead_verify_ex(c["x"], c["Wq"], c["sc"], c["drafts"], vocab_map=c["vm"], flags=sv.MAP_STATIC,
+                                accept_len=c["acc"], next_token=c["nxt"], stream=stream)
 
     def calls(self):
         return [c for l in self.legs for c in l["calls"]]
@@ -881,6 +885,18 @@ def run_ncu_case(args):
     rng = np.random.default_rng(5)
     dev = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a).view(dt)).to(device)
     T = args.ncu_T
+    if args.ncu_fma:
+        sv.debug_set_fma_consumers(True)
+    if args.ncu_case == "step":
+        # one warm-up step, then the profiled step: 21 launches each
+        wl = Workload(torch, device)
+        stream = torch.cuda.current_stream(device)
+        for _ in range(2):
+            wl.step(sv, stream)
+        torch.cuda.synchronize()
+        assert sv.last_device_error() == 0
+        print(json.dumps({"ncu_case": "step", "launches_per_step": wl.launches_per_step, "ok": True}))
+        return
     if args.ncu_case == "restricted":
         V, K = gen.VOCAB, gen.HIDDEN
         Wq, sc = gen.weights(rng, V, K)
@@ -889,7 +905,7 @@ def run_ncu_case(args):
         vm = dev(gen.vocab_map(rng, V, gen.DRAFT_VOCAB), np.int32)
         drafts = torch.zeros(T - 1, dtype=torch.int32, device=device)
         for _ in range(3):
-            sv.lmhead_verify(x, Wd, sd, drafts, vocab_map=vm)
+            sv.lmhead_verify_ex(x, Wd, sd, drafts.view(1, T - 1), vocab_map=vm, flags=sv.MAP_STATIC)
     elif args.ncu_case in ("head", "sampled", "rescored"):
         V, K = gen.VOCAB, gen.HIDDEN
         Wq, sc = gen.weights(rng, V, K)
@@ -932,7 +948,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--breakdown", action="store_true", help="also time each kernel alone at T=1..32")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--ncu-case", choices=["head", "gemm", "sampled", "rescored", "restricted"], default=None)
+    ap.add_argument("--ncu-case", choices=["head", "gemm", "sampled", "rescored", "restricted", "step"], default=None)
+    ap.add_argument("--ncu-fma", action="store_true", help="CUDA-core consumers (sv_debug_set_fma_consumers)")
     ap.add_argument("--ncu-T", type=int, default=4)
     ap.add_argument("--ncu-streams", type=int, default=1)
     ap.add_argument("--ncu-shape", choices=[s[0] for s in gen.GEMM_SHAPES], default="gate_up")

@@ -131,6 +131,27 @@ int lmhead_verify_batched(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *s
                           int32_t *accept_len, int32_t *next_token, sv_stream stream);
 
 /*
+ * lmhead_verify_ex -- lmhead_verify_batched with flags.
+ *   SV_MAP_STATIC: the caller promises that vocab_map is model data that no
+ *   kernel enqueued before this call on `stream` writes (a draft
+ *   vocabulary loaded once, as on page "Tesla P100 (sm_60) llama.cpp
+ *   patches for Qwen3.5/3.6-35B-A3B: ~2x decode and prompt processing over
+ *   the shinbunbun baseline", section "MTP draft vocabulary (patch 17)": a
+ *   token list shipped with the model).  The kernel then reads the ids,
+ *   gathers their scales and starts streaming their weight rows while the
+ *   previous kernel of the stream is still finishing, instead of after it
+ *   (programmatic dependent launch).  Not for a list that a preceding
+ *   kernel maintains, such as the dynamic draft list of draft_list_add.
+ *   Ignored without a vocab_map.  Other flag bits: SV_ERR_SHAPE.
+ *   Everything else as lmhead_verify_batched.
+ */
+#define SV_MAP_STATIC 0x1
+int lmhead_verify_ex(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, int K,
+                     const int32_t *drafts, int n_draft, int n_streams,
+                     const int32_t *vocab_map, int n_map, int V, int flags,
+                     int32_t *accept_len, int32_t *next_token, sv_stream stream);
+
+/*
  * sv_verify_cycle -- one verify cycle's weight reads in one call: the
  * given W4A16 GEMMs in order, then (when verify != NULL) the lm_head pass
  * with greedy verification of n_streams blocks, all enqueued on `stream`
@@ -369,6 +390,19 @@ int sv_last_device_error(int32_t *out);
  *   SV_ERR_ALIGN, SV_ERR_CUDA, SV_ERR_NOMEM.
  */
 int sv_hbm_read(const void *src, size_t bytes, uint32_t *sink, sv_stream stream);
+
+/*
+ * sv_debug_set_fma_consumers -- a measurement switch: with on != 0, later
+ * calls whose launch keeps the activations resident (T <= 8, contiguous
+ * rows, at least 80 units of 64 rows x 128 columns per SM) compute their
+ * dot products on CUDA cores -- one mixed-precision fp16 x fp16 -> fp32 fma
+ * per weight and token -- instead of with tensor-core mma; same weight
+ * stream, same results within fp32 rounding order.  It exists to measure
+ * the two formulations against each other at equal HBM traffic (the
+ * tensor-core path is the default because it measured faster); 0 restores
+ * the default.  Process-wide.  No source page has a counterpart.
+ */
+int sv_debug_set_fma_consumers(int on);
 
 /*
  * sv_debug_set_wait_stall -- a test hook for the bounded waits.  With

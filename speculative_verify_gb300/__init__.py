@@ -69,6 +69,8 @@ def load(path: str | None = None):
     lib.lmhead_verify.restype = ci
     lib.lmhead_verify_batched.argtypes = [vp, vp, vp, ci, vp, ci, ci, vp, ci, ci, vp, vp, vp]
     lib.lmhead_verify_batched.restype = ci
+    lib.lmhead_verify_ex.argtypes = [vp, vp, vp, ci, vp, ci, ci, vp, ci, ci, ci, vp, vp, vp]
+    lib.lmhead_verify_ex.restype = ci
     lib.lmhead_verify_noalloc.argtypes = [vp, vp, vp, ci, vp, ci, vp, ci, ci, vp, vp, vp]
     lib.lmhead_verify_noalloc.restype = ci
     lib.lmhead_argmax.argtypes = [vp, vp, vp, ci, ci, vp, ci, ci, vp, vp, vp]
@@ -100,6 +102,8 @@ def load(path: str | None = None):
     lib.sv_hbm_read.restype = ci
     lib.sv_verify_cycle.argtypes = [ctypes.POINTER(GemmCall), ci, ctypes.POINTER(VerifyCall), vp]
     lib.sv_verify_cycle.restype = ci
+    lib.sv_debug_set_fma_consumers.argtypes = [ci]
+    lib.sv_debug_set_fma_consumers.restype = ci
     lib.sv_debug_set_wait_stall.argtypes = [ctypes.c_uint32]
     lib.sv_debug_set_wait_stall.restype = ci
     _lib = lib
@@ -213,6 +217,39 @@ def lmhead_verify_batched(x, Wq, scales, drafts, vocab_map=None, accept_len=None
     _check("lmhead_verify_batched", load().lmhead_verify_batched(
         _ptr(x), _ptr(Wq), _ptr(scales), K, _ptr(drafts) if n_draft else None, n_draft, S,
         _ptr(vocab_map), n_map, V, _ptr(accept_len), _ptr(next_token), _stream(stream)))
+    return accept_len, next_token
+
+
+MAP_STATIC = 0x1
+
+
+def lmhead_verify_ex(x, Wq, scales, drafts, vocab_map=None, flags=0, accept_len=None, next_token=None,
+                     stream=None):
+    """lmhead_verify_batched with flags (lmhead_verify_ex): MAP_STATIC for a
+    vocab_map that no preceding kernel writes.  drafts: [n_streams][n_draft]."""
+    torch = _torch()
+    _bits16(x, "x"), _words(Wq, "Wq"), _bits16(scales, "scales")
+    T, K = x.shape
+    V = Wq.shape[0]
+    if drafts.dim() != 2:
+        raise ValueError("drafts must be [n_streams][n_draft]")
+    S, n_draft = drafts.shape
+    if S * (n_draft + 1) != T:
+        raise ValueError("x must have n_streams * (1 + n_draft) rows")
+    if Wq.shape[1] * 8 != K or tuple(scales.shape) != (V, K // 128):
+        raise ValueError("shape mismatch between x, Wq and scales")
+    if n_draft:
+        _i32(drafts, "drafts")
+    if vocab_map is not None:
+        _i32(vocab_map, "vocab_map")
+    if accept_len is None:
+        accept_len = torch.empty(S, dtype=torch.int32, device=x.device)
+    if next_token is None:
+        next_token = torch.empty(S, dtype=torch.int32, device=x.device)
+    n_map = 0 if vocab_map is None else vocab_map.numel()
+    _check("lmhead_verify_ex", load().lmhead_verify_ex(
+        _ptr(x), _ptr(Wq), _ptr(scales), K, _ptr(drafts) if n_draft else None, n_draft, S,
+        _ptr(vocab_map), n_map, V, int(flags), _ptr(accept_len), _ptr(next_token), _stream(stream)))
     return accept_len, next_token
 
 
@@ -462,3 +499,9 @@ def debug_set_wait_stall(ns: int) -> None:
     every later stream-kernel launch makes one wait run out after ns
     nanoseconds and report SV_DEVERR_TIMEOUT; 0 turns it off."""
     _check("sv_debug_set_wait_stall", load().sv_debug_set_wait_stall(int(ns)))
+
+
+def debug_set_fma_consumers(on: bool) -> None:
+    """Measurement switch (sv_debug_set_fma_consumers): CUDA-core fma
+    consumers instead of tensor-core mma for resident-activation launches."""
+    _check("sv_debug_set_fma_consumers", load().sv_debug_set_fma_consumers(1 if on else 0))

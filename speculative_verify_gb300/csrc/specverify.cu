@@ -63,11 +63,12 @@ constexpr int X16_MAX_GROUPS = 1024;
 DeviceState g_state[MAX_DEVICES];
 std::mutex g_mu;
 std::atomic<uint32_t> g_stall_ns{0};    // sv_debug_set_wait_stall
+std::atomic<int> g_fma_consumers{0};     // sv_debug_set_fma_consumers
 
-template <int NT, bool HEAD, bool GATHER, bool XRES>
+template <int NT, bool HEAD, bool GATHER, bool XRES, bool FMA = false>
 cudaError_t raise_smem_limit(int bytes)
 {
-    return cudaFuncSetAttribute(w4a16_stream_kernel<NT, HEAD, GATHER, XRES>,
+    return cudaFuncSetAttribute(w4a16_stream_kernel<NT, HEAD, GATHER, XRES, FMA>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
@@ -180,6 +181,8 @@ int device_state(DeviceState **out)
         e = e != cudaSuccess ? e : raise_smem_limit<1, true, true, true>(optin);
         e = e != cudaSuccess ? e : raise_smem_limit<2, true, true, false>(optin);
         e = e != cudaSuccess ? e : raise_smem_limit<4, true, true, false>(optin);
+        e = e != cudaSuccess ? e : raise_smem_limit<1, false, false, true, true>(optin);
+        e = e != cudaSuccess ? e : raise_smem_limit<1, true, false, true, true>(optin);
         e = e != cudaSuccess ? e : cudaFuncSetAttribute(hbm_read_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                         HR_NST * HR_STAGE + 2 * HR_NST * 8);
         e = e != cudaSuccess ? e : raise_smem_limit_wide<2, false, 8>(optin);
@@ -260,7 +263,7 @@ int plan_layout(Params &p, int smem_optin, int *smem_total)
 constexpr int XRES_MAX_BYTES = 100 * 1024;
 constexpr int XRES_MIN_UNITS = 80;
 
-template <int NT, bool HEAD, bool GATHER, bool XRES>
+template <int NT, bool HEAD, bool GATHER, bool XRES, bool FMA = false>
 int launch(Params p, const DeviceState &st, cudaStream_t stream)
 {
     // several token tiles: the activations go through the conversion buffer
@@ -329,7 +332,7 @@ int launch(Params p, const DeviceState &st, cudaStream_t stream)
     cfg.gridDim = dim3(static_cast<unsigned>(B));
     cfg.blockDim = dim3(static_cast<unsigned>((consumer_warps(NT, XRES, GATHER) + 2) * 32));
     cfg.dynamicSmemBytes = static_cast<size_t>(smem);
-    if (cudaLaunchKernelEx(&cfg, w4a16_stream_kernel<NT, HEAD, GATHER, XRES>, p, tmW, tmX) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, w4a16_stream_kernel<NT, HEAD, GATHER, XRES, FMA>, p, tmW, tmX) != cudaSuccess) {
         cudaGetLastError();
         return SV_ERR_CUDA;
     }
@@ -441,8 +444,11 @@ int dispatch(Params &p, const DeviceState &st, cudaStream_t stream)
     if (use_wide<HEAD, GATHER>(p, st)) return launch_wide<2, HEAD, 8>(p, st, stream);
     if (p.T <= 8) {
         if (static_cast<long long>(p.T + 1) * (2LL * p.K + 16) <= XRES_MAX_BYTES &&
-            p.U >= static_cast<long long>(XRES_MIN_UNITS) * st.sms)
+            p.U >= static_cast<long long>(XRES_MIN_UNITS) * st.sms) {
+            if constexpr (!GATHER)
+                if (g_fma_consumers.load(std::memory_order_relaxed)) return launch<1, HEAD, false, true, true>(p, st, stream);
             return launch<1, HEAD, GATHER, true>(p, st, stream);
+        }
         return launch<1, HEAD, GATHER, false>(p, st, stream);
     }
     if (p.T <= 16) return launch<2, HEAD, GATHER, false>(p, st, stream);
@@ -500,7 +506,7 @@ int check_gemm(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, int 
 int head_call(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, int K, int T,
               const int32_t *vocab_map, int n_map, int V, int mode, const int32_t *drafts,
               int n_draft, int n_streams, int32_t *accept_len, int32_t *next_token,
-              int32_t *ids, float *vals, cudaStream_t stream)
+              int32_t *ids, float *vals, cudaStream_t stream, int flags = 0)
 {
     int rc = check_head(x, Wq, scales, K, T, vocab_map, n_map, V, mode, drafts, n_draft, accept_len, next_token,
                         ids, vals);
@@ -528,6 +534,7 @@ int head_call(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, int K
     p.next_token = next_token;
     p.ids = ids;
     p.vals = vals;
+    p.map_static = (vocab_map && (flags & SV_MAP_STATIC)) ? 1 : 0;
     return vocab_map ? dispatch<true, true>(p, *st, stream) : dispatch<true, false>(p, *st, stream);
 }
 
@@ -891,6 +898,19 @@ int lmhead_verify_batched(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *s
                          reinterpret_cast<cudaStream_t>(stream));
 }
 
+int lmhead_verify_ex(const sv_bf16 *x, const uint32_t *Wq, const sv_bf16 *scales, int K,
+                     const int32_t *drafts, int n_draft, int n_streams,
+                     const int32_t *vocab_map, int n_map, int V, int flags, int32_t *accept_len,
+                     int32_t *next_token, sv_stream stream)
+{
+    if (flags & ~SV_MAP_STATIC) return SV_ERR_SHAPE;
+    const int rc = sv::check_batched(n_draft, n_streams);
+    if (rc != SV_OK) return rc;
+    return sv::head_call(x, Wq, scales, K, n_streams * (n_draft + 1), vocab_map, n_map, V, 0, drafts,
+                         n_draft, n_streams, accept_len, next_token, nullptr, nullptr,
+                         reinterpret_cast<cudaStream_t>(stream), flags);
+}
+
 int sv_verify_cycle(const sv_gemm_call *gemms, int n_gemms, const sv_verify_call *verify, sv_stream stream)
 {
     using namespace sv;
@@ -1003,6 +1023,12 @@ int sv_hbm_read(const void *src, size_t bytes, uint32_t *sink, sv_stream stream)
         cudaGetLastError();
         return SV_ERR_CUDA;
     }
+    return SV_OK;
+}
+
+int sv_debug_set_fma_consumers(int on)
+{
+    sv::g_fma_consumers.store(on ? 1 : 0, std::memory_order_relaxed);
     return SV_OK;
 }
 

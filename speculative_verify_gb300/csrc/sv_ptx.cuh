@@ -294,6 +294,19 @@ __device__ __forceinline__ uint32_t dequant2_f16_hi(uint32_t v)
     return r;
 }
 
+// c + a.lo * b.lo + a.hi * b.hi: two fp16 x fp16 products added to an fp32
+// accumulator by the mixed-precision fma (products exact in fp32, each add
+// rounded to fp32).
+__device__ __forceinline__ float fma2_f16_f32(uint32_t a, uint32_t b, float c)
+{
+    float d;
+    asm("{\n\t.reg .f16 al, ah, bl, bh;\n\t.reg .f32 t;\n\t"
+        "mov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+        "fma.rn.f32.f16 t, al, bl, %3;\n\tfma.rn.f32.f16 %0, ah, bh, t;\n\t}"
+        : "=f"(d) : "r"(a), "r"(b), "f"(c));
+    return d;
+}
+
 // ---------------------------------------------------------------- tensor core
 
 // D (16x8 fp32) += A (16x16 fp16, row) * B (16x8 fp16, col).

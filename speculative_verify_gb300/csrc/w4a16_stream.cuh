@@ -114,6 +114,8 @@ struct Params {
     float *y32;                 // [T][N] fp32 when not null (the lm_head's logits for rescoring)
     // HEAD outputs
     int mode;                   // 0: verify, 1: argmax
+    int map_static;             // the vocab_map is model data no preceding kernel writes:
+                                // it may be read before griddepcontrol.wait
     const int32_t *drafts;      // [n_streams][n_draft]
     int n_draft, n_streams;
     int32_t *accept_len, *next_token;   // [n_streams]
@@ -411,7 +413,11 @@ __device__ __forceinline__ void head_grid_tail(const Params &p, unsigned long lo
     }
 }
 
-template <int NT, bool HEAD, bool GATHER, bool XRES>
+// FMA: the consumers compute on CUDA cores instead of tensor cores (one
+// mixed-precision fp16 x fp16 -> fp32 fma per weight and token); only for
+// one token tile of contiguous rows with resident activations.  It exists
+// for the measured comparison of the two formulations at equal HBM traffic.
+template <int NT, bool HEAD, bool GATHER, bool XRES, bool FMA = false>
 __global__ void __launch_bounds__((consumer_warps(NT, XRES, GATHER) + 2) * 32, 1)
 w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tmW,
                     const __grid_constant__ CUtensorMap tmX)
@@ -421,6 +427,7 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
     constexpr int EPILOGUE_WARP = NCW + 1;
     using C = Cfg<NT, GATHER, NCW>;
     static_assert(!XRES || NT == 1, "resident activations are laid out for one n8 token tile");
+    static_assert(!FMA || (NT == 1 && XRES && !GATHER), "the CUDA-core consumers read resident rows");
     // How activations reach the B loads: resident fp16 rows (XRES); raw bf16
     // rows copied into every stage by tensor copies (XBF: one token tile
     // whose rows are too long to keep resident; permuted in registers, bf16
@@ -488,7 +495,7 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
         int s = 0, issued = 0, tile = tile_first, grp = grp_first, rem = n_units;
         uint32_t ph = 0;
         bool waited = false;
-        if (GATHER) {
+        if (GATHER && !p.map_static) {
             pdl_wait_prior();       // the id list may come from the previous kernel
             waited = true;
         }
@@ -582,7 +589,7 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
 
     if (warp == EPILOGUE_WARP) {
         // ============================================================ epilogue
-        if (GATHER) pdl_wait_prior();   // the id list may come from the previous kernel
+        if (GATHER && !p.map_static) pdl_wait_prior();   // the id list may come from the previous kernel
         stage_tile_meta<HEAD, GATHER>(p, tile_first, sbuf, idbuf, smem_addr(&meta_full[0]), lane);
         if (tile_first + 1 <= tile_last)
             stage_tile_meta<HEAD, GATHER>(p, tile_first + 1, sbuf + p.sbuf_bytes, idbuf + ROWS,
@@ -926,6 +933,18 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[r][nt][e] = 0.f;
+    // FMA: this lane's partial sums over its 32 columns of each group, for
+    // rows g (h = 0) and g + 8 (h = 1) of each m16 tile and all 8 tokens
+    float accf[FMA ? C::R : 1][2][8];
+    if constexpr (FMA) {
+#pragma unroll
+        for (int r = 0; r < C::R; ++r)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int t = 0; t < 8; ++t) accf[r][h][t] = 0.f;
+    }
+    const uint32_t xr0 = XRES ? smem_addr(smem + p.off_xres) + static_cast<uint32_t>(c * 64) : 0u;
 
     int s = 0, grp = grp_first, rem = n_units, k = 0;
     uint32_t ph = 0;
@@ -942,6 +961,59 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
             const int gs = grp + slot;     // group within the row
             const uint32_t stage = smem0 + static_cast<uint32_t>(s * p.stage_bytes);
             const uint32_t wbase = stage + w_lane;
+          if constexpr (FMA) {
+            // Each lane dots its 32 columns (chunk c of the group) of rows g
+            // and g + 8 of its m16 tiles with every token's resident row:
+            // the levels (fp16, pairs (j, j+4) as the dequant yields them)
+            // times the activations (fp16, stored in the same pairing), one
+            // fp32-accumulating fma per weight and token.
+            const uint32_t sbf = sbuf0 + kb * p.sbuf_bytes + s_lane + gs * 2;
+#pragma unroll
+            for (int r = 0; r < C::R; ++r) {
+                const uint4 wa = lds128(wbase + r * RSTEP);
+                const uint4 wb = lds128(wbase + r * RSTEP + HSTEP);
+                float fs[2][8];
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) fs[h][t] = 0.f;
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    uint32_t lv[2][4];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint4 &w4 = h ? wb : wa;
+                        const uint32_t w = (m == 0) ? w4.x : (m == 1) ? w4.y : (m == 2) ? w4.z : w4.w;
+                        lv[h][0] = dequant2_f16_lo(w);         // nibbles (0, 4)
+                        lv[h][1] = dequant2_f16_hi(w);         // (1, 5)
+                        lv[h][2] = dequant2_f16_lo(w >> 8);    // (2, 6)
+                        lv[h][3] = dequant2_f16_hi(w >> 8);    // (3, 7)
+                    }
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) {
+                        if (t >= T) break;
+                        const uint4 v = lds128(xr0 + static_cast<uint32_t>(t * p.xres_stride + gs * 256) +
+                                               ((16u * m) ^ xsw));
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            float a = fs[h][t];
+                            a = fma2_f16_f32(lv[h][0], v.x, a);
+                            a = fma2_f16_f32(lv[h][1], v.y, a);
+                            a = fma2_f16_f32(lv[h][2], v.z, a);
+                            a = fma2_f16_f32(lv[h][3], v.w, a);
+                            fs[h][t] = a;
+                        }
+                    }
+                }
+                const float s0 = bf16_bits_to_float(lds_u16(sbf + r * 16 * G * 2));
+                const float s1 = bf16_bits_to_float(lds_u16(sbf + (r * 16 + 8) * G * 2));
+#pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                    accf[r][0][t] += s0 * fs[0][t];
+                    accf[r][1][t] += s1 * fs[1][t];
+                }
+            }
+          } else {
             uint4 wa[C::R], wb[C::R];
 #pragma unroll
             for (int r = 0; r < C::R; ++r) {
@@ -1029,6 +1101,7 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
                     acc[r][nt][3] += s1 * gacc[r][nt][3];
                 }
             }
+          }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_addr(&empty[s]));
@@ -1039,6 +1112,39 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
         if (grp == G || rem == 0) {
             // End of this CTA's share of a tile: hand the partial sums over.
             if (lane == 0) mbar_arrive(smem_addr(&meta_empty[kb]));   // scales no longer read
+            if constexpr (FMA) {
+                // the four lanes of a row hold its four 32-column parts:
+                // add them (xor 1, 2), then keep tokens 2c, 2c+1 in the
+                // fragment layout the hand-off below expects
+#pragma unroll
+                for (int r = 0; r < C::R; ++r)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int t = 0; t < 8; ++t) {
+                            float v = accf[r][h][t];
+                            v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
+                            v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
+                            accf[r][h][t] = v;
+                        }
+#pragma unroll
+                for (int r = 0; r < C::R; ++r) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            float v = 0.f;
+#pragma unroll
+                            for (int cc = 0; cc < 4; ++cc)
+                                if (c == cc) v = accf[r][h][2 * cc + e];
+                            acc[r][0][2 * h + e] = v;
+                        }
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int t = 0; t < 8; ++t) accf[r][h][t] = 0.f;
+                }
+            }
             wait_or_flag(p, flag, smem_addr(red_empty), static_cast<uint32_t>((k & 1) ^ 1));
 #pragma unroll
             for (int r = 0; r < C::R; ++r)

@@ -579,3 +579,89 @@ def test_timed_out_wait_is_reported_and_later_calls_are_clean(sv, oracle):
         assert sv.last_device_error() == 0
     # the stalled GEMM still computed its outputs
     assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
+
+
+# --------------------------------------------------------------------------
+# the CUDA-core formulation of the consumers (measurement switch) and the
+# static-map head
+
+
+@pytest.mark.parametrize("T,K", [(1, 1152), (4, 5120), (8, 1664)])
+def test_fma_consumers_gemm_match_oracle(sv, oracle, T, K):
+    """With the CUDA-core consumers switched on, a resident-activation GEMM
+    still matches the oracle within the tolerance."""
+    N = resident_rows(K)
+    rng = np.random.default_rng(7600 + T + K)
+    Wq, sc = gen.weights(rng, N, K)
+    x = gen.activations(rng, T, K)
+    y32, _ = oracle.w4a16_gemm(x, Wq, sc, T, K, N)
+    sv.debug_set_fma_consumers(True)
+    try:
+        y = sv.w4a16_gemm(dev_bits16(x), dev_words(Wq), dev_bits16(sc))
+        torch.cuda.synchronize()
+    finally:
+        sv.debug_set_fma_consumers(False)
+    assert_gemm_close(y.view(torch.int16).cpu().numpy().view(np.uint16), y32)
+    assert sv.last_device_error() == 0
+
+
+@pytest.mark.parametrize("n_draft", [0, 3, 7])
+def test_fma_consumers_verify_matches_oracle(sv, oracle, n_draft):
+    K = 1024
+    V = resident_rows(K, ragged=11)
+    sv.debug_set_fma_consumers(True)
+    try:
+        run_head_case(sv, oracle, 7700 + n_draft, V, K, n_draft, 1, 0)
+    finally:
+        sv.debug_set_fma_consumers(False)
+
+
+@pytest.mark.parametrize("V,K,n_draft,n_streams,n_map", [
+    (5000, 768, 3, 1, 1234),
+    (5000, 768, 0, 1, 1),
+    (6000, 512, 3, 2, 4000),
+    (5000, 768, 7, 1, 2000),
+])
+def test_static_map_verify_matches_oracle(sv, oracle, V, K, n_draft, n_streams, n_map):
+    """lmhead_verify_ex with SV_MAP_STATIC gives the regular call's results."""
+    rng = np.random.default_rng(7800 + V + n_map)
+    Wq, sc = gen.weights(rng, V, K)
+    T = n_streams * (n_draft + 1)
+    x = gen.activations(rng, T, K)
+    vm = gen.vocab_map(rng, V, n_map)
+    a, _, _ = oracle.argmax(oracle.lmhead_logits(x, Wq, sc, K, T, V, rows=vm), ids=vm)
+    drafts = np.stack([gen.drafts_with_mismatch(rng, a[s * (n_draft + 1):(s + 1) * (n_draft + 1)],
+                                                int(rng.integers(0, n_draft + 1)), V, pool=vm)
+                       for s in range(n_streams)]).astype(np.int32).reshape(n_streams, n_draft)
+    res = oracle.lmhead_verify(x, Wq, sc, K, V, drafts, n_streams=n_streams, vocab_map=vm)
+    dx, dW, ds, dvm = dev_bits16(x), dev_words(Wq), dev_bits16(sc), dev_i32(vm)
+    dd = torch.from_numpy(drafts).cuda()
+    acc_s, nxt_s = sv.lmhead_verify_ex(dx, dW, ds, dd, vocab_map=dvm, flags=sv.MAP_STATIC)
+    acc_r, nxt_r = sv.lmhead_verify_batched(dx, dW, ds, dd, vocab_map=dvm)
+    ids, _ = sv.lmhead_argmax(dx, dW, ds, vocab_map=dvm)
+    torch.cuda.synchronize()
+    assert torch.equal(acc_s, acc_r) and torch.equal(nxt_s, nxt_r)
+    check_verify(res, drafts, acc_s.cpu().numpy(), nxt_s.cpu().numpy(), ids.cpu().numpy(), n_draft, n_streams, vm)
+    assert sv.last_device_error() == 0
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("n_draft", [0, 3])
+def test_static_map_restricted_head_full_size(sv, oracle, n_draft):
+    """The 40,960-id restricted head of a 248,320 x 5,120 lm_head with the
+    static-map flag, as the benchmark runs it."""
+    rng = np.random.default_rng(7900 + n_draft)
+    V, K, n_map = gen.VOCAB, gen.HIDDEN, gen.DRAFT_VOCAB
+    Wq, sc = gen.weights(rng, V, K)
+    x = gen.activations(rng, n_draft + 1, K)
+    vm = gen.vocab_map(rng, V, n_map)
+    a, _, _ = oracle.argmax(oracle.lmhead_logits(x, Wq, sc, K, n_draft + 1, V, rows=vm), ids=vm)
+    drafts = gen.drafts_with_mismatch(rng, a, min(2, n_draft), V, pool=vm).reshape(1, n_draft)
+    res = oracle.lmhead_verify(x, Wq, sc, K, V, drafts, vocab_map=vm)
+    dx, dW, ds, dvm = dev_bits16(x), dev_words(Wq), dev_bits16(sc), dev_i32(vm)
+    acc, nxt = sv.lmhead_verify_ex(dx, dW, ds, torch.from_numpy(drafts).cuda(), vocab_map=dvm,
+                                   flags=sv.MAP_STATIC)
+    ids, _ = sv.lmhead_argmax(dx, dW, ds, vocab_map=dvm)
+    torch.cuda.synchronize()
+    check_verify(res, drafts, acc.cpu().numpy(), nxt.cpu().numpy(), ids.cpu().numpy(), n_draft, 1, vm)
+    assert sv.last_device_error() == 0
