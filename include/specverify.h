@@ -60,6 +60,7 @@ enum sv_status {
 /* Bits of the sticky device error word. */
 #define SV_DEVERR_BAD_MAP_ID  0x1   /* a vocab_map entry outside [0, V) was skipped */
 #define SV_DEVERR_TIMEOUT     0x2   /* a pipeline wait gave up; outputs are invalid */
+#define SV_DEVERR_SMEM_ALIGN  0x4   /* shared memory not 1024-byte aligned; nothing was computed */
 
 /*
  * w4a16_gemm -- y[t][n] = bf16_rne( sum_g float(scales[n][g]) *
@@ -403,6 +404,19 @@ int sv_hbm_read(const void *src, size_t bytes, uint32_t *sink, sv_stream stream)
  * the default.  Process-wide.  No source page has a counterpart.
  */
 int sv_debug_set_fma_consumers(int on);
+
+/*
+ * sv_debug_set_tcgen05 -- a measurement switch: with on != 0, later calls
+ * with 17 <= T <= 32 (four n8 token tiles), contiguous rows and K a
+ * multiple of 1024 run on the 5th-generation tensor cores (tcgen05.mma,
+ * M = 128 weight rows x N = 32 tokens x K = 16, the dequantised levels
+ * stored to tensor memory as the A operand, fp32 group sums accumulated in
+ * tensor memory and scaled in registers) instead of mma.sync; same results
+ * within fp32 rounding order.  It exists to measure that formulation (it
+ * measured slower, so mma.sync is the default); 0 restores the default.
+ * Process-wide.  No source page has a counterpart.
+ */
+int sv_debug_set_tcgen05(int on);
 
 /*
  * sv_debug_set_wait_stall -- a test hook for the bounded waits.  With

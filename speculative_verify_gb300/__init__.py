@@ -104,6 +104,8 @@ def load(path: str | None = None):
     lib.sv_verify_cycle.restype = ci
     lib.sv_debug_set_fma_consumers.argtypes = [ci]
     lib.sv_debug_set_fma_consumers.restype = ci
+    lib.sv_debug_set_tcgen05.argtypes = [ci]
+    lib.sv_debug_set_tcgen05.restype = ci
     lib.sv_debug_set_wait_stall.argtypes = [ctypes.c_uint32]
     lib.sv_debug_set_wait_stall.restype = ci
     _lib = lib
@@ -505,3 +507,9 @@ def debug_set_fma_consumers(on: bool) -> None:
     """Measurement switch (sv_debug_set_fma_consumers): CUDA-core fma
     consumers instead of tensor-core mma for resident-activation launches."""
     _check("sv_debug_set_fma_consumers", load().sv_debug_set_fma_consumers(1 if on else 0))
+
+
+def debug_set_tcgen05(on: bool) -> None:
+    """Measurement switch (sv_debug_set_tcgen05): the tcgen05 kernel for
+    calls with 17 <= T <= 32 instead of the mma.sync kernel."""
+    _check("sv_debug_set_tcgen05", load().sv_debug_set_tcgen05(1 if on else 0))

@@ -17,6 +17,7 @@
 #include "specverify.h"
 #include "w4a16_stream.cuh"
 #include "w4a16_wide.cuh"
+#include "w4a16_tc.cuh"
 
 namespace sv {
 namespace {
@@ -64,6 +65,7 @@ DeviceState g_state[MAX_DEVICES];
 std::mutex g_mu;
 std::atomic<uint32_t> g_stall_ns{0};    // sv_debug_set_wait_stall
 std::atomic<int> g_fma_consumers{0};     // sv_debug_set_fma_consumers
+std::atomic<int> g_tcgen05{0};           // sv_debug_set_tcgen05
 
 template <int NT, bool HEAD, bool GATHER, bool XRES, bool FMA = false>
 cudaError_t raise_smem_limit(int bytes)
@@ -96,14 +98,15 @@ int tensor_map_fn()
 
 // 2-D row-major tensor [rows][cols] of `esize`-byte elements; box = bc x br.
 int encode_2d(CUtensorMap *m, CUtensorMapDataType dt, int esize, const void *base,
-              unsigned long long cols, unsigned long long rows, unsigned bc, unsigned br)
+              unsigned long long cols, unsigned long long rows, unsigned bc, unsigned br,
+              CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_NONE)
 {
     const cuuint64_t dims[2] = {cols, rows};
     const cuuint64_t strides[1] = {cols * static_cast<unsigned long long>(esize)};
     const cuuint32_t box[2] = {bc, br};
     const cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? SV_OK : SV_ERR_CUDA;
 }
@@ -185,6 +188,10 @@ int device_state(DeviceState **out)
         e = e != cudaSuccess ? e : raise_smem_limit<1, true, false, true, true>(optin);
         e = e != cudaSuccess ? e : cudaFuncSetAttribute(hbm_read_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                         HR_NST * HR_STAGE + 2 * HR_NST * 8);
+        e = e != cudaSuccess ? e : cudaFuncSetAttribute(w4a16_tc_kernel<false>,
+                                                        cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+        e = e != cudaSuccess ? e : cudaFuncSetAttribute(w4a16_tc_kernel<true>,
+                                                        cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
         e = e != cudaSuccess ? e : raise_smem_limit_wide<2, false, 8>(optin);
         e = e != cudaSuccess ? e : raise_smem_limit_wide<2, true, 8>(optin);
         if (e == cudaSuccess)
@@ -323,7 +330,7 @@ int launch(Params p, const DeviceState &st, cudaStream_t stream)
         cfg.gridDim = dim3(static_cast<unsigned>(Cfg<NT, GATHER, consumer_warps(NT, XRES, GATHER)>::TP));
         cfg.blockDim = dim3(XP_THREADS);
         cfg.dynamicSmemBytes = 0;
-        if (cudaLaunchKernelEx(&cfg, xprep_kernel, p.x, p.T, p.K, Cfg<NT, GATHER, consumer_warps(NT, XRES, GATHER)>::TP, st.x16, st.xinv) !=
+        if (cudaLaunchKernelEx(&cfg, xprep_kernel<false>, p.x, p.T, p.K, Cfg<NT, GATHER, consumer_warps(NT, XRES, GATHER)>::TP, st.x16, st.xinv) !=
             cudaSuccess) {
             cudaGetLastError();
             return SV_ERR_CUDA;
@@ -407,7 +414,7 @@ int launch_wide(Params p, const DeviceState &st, cudaStream_t stream)
     cfg.gridDim = dim3(static_cast<unsigned>(8 * NT));
     cfg.blockDim = dim3(XP_THREADS);
     cfg.dynamicSmemBytes = 0;
-    if (cudaLaunchKernelEx(&cfg, xprep_kernel, p.x, p.T, p.K, 8 * NT, st.x16, st.xinv) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, xprep_kernel<false>, p.x, p.T, p.K, 8 * NT, st.x16, st.xinv) != cudaSuccess) {
         cudaGetLastError();
         return SV_ERR_CUDA;
     }
@@ -430,6 +437,97 @@ int launch_wide(Params p, const DeviceState &st, cudaStream_t stream)
 // tiles.  Smaller calls, and four token tiles (T > 16, where the 512-row
 // kernel's 168-register cap spills and runs 10 % slower), stay on the
 // 64-row kernel; the 256-row variant measured slower everywhere.
+// Shared-memory layout of a tcgen05 launch (offsets in bytes): nst stages
+// of 16 KB (8 KB of packed weights, 8 KB of activations) from 0 -- 1024-byte
+// aligned, as the swizzled weight boxes need | the four-slot scale ring | the
+// head's key table | mbarriers, flag, decision word, tensor-memory address.
+template <bool HEAD>
+int plan_layout_tc(Params &p, int smem_optin, int *smem_total)
+{
+    const int ring_bytes = TC_RING * TC_RING_SLOT;
+    const int kt_bytes = HEAD ? 4 * TMAX * 8 : 0;
+    int nst = (smem_optin - ring_bytes - kt_bytes - 512) / TC_STAGE;
+    if (nst > TC_MAX_STAGES) nst = TC_MAX_STAGES;
+    if (nst < 2) return SV_ERR_SHAPE;
+    p.nst = nst;
+    p.stage_bytes = TC_STAGE;
+    p.xslot_bytes = TC_X_BYTES;
+    int off = nst * TC_STAGE;
+    p.off_sbuf = off;
+    off += ring_bytes;
+    p.off_bk = off;
+    off += kt_bytes;
+    p.off_bars = off;
+    off += (2 * nst + 2 * TC_NA + 2 * TC_NACC + 2) * 8 + 16;
+    *smem_total = off;
+    return off <= smem_optin ? SV_OK : SV_ERR_SHAPE;
+}
+
+template <bool HEAD>
+int launch_tc(Params p, const DeviceState &st, cudaStream_t stream)
+{
+    if (p.G > st.x16_max_groups) return SV_ERR_SHAPE;
+    int smem = 0;
+    int rc = plan_layout_tc<HEAD>(p, st.smem_optin, &smem);
+    if (rc != SV_OK) return rc;
+    CUtensorMap tmW, tmS;
+    std::memset(&tmW, 0, sizeof tmW);
+    std::memset(&tmS, 0, sizeof tmS);
+    rc = encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, p.Wq, static_cast<unsigned long long>(p.K / 8),
+                   static_cast<unsigned long long>(p.n_rows), 16, TC_RT, CU_TENSOR_MAP_SWIZZLE_64B);
+    if (rc != SV_OK) return rc;
+    rc = encode_2d(&tmS, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, p.scales, static_cast<unsigned long long>(p.G),
+                   static_cast<unsigned long long>(p.n_rows), 8, TC_RT);
+    if (rc != SV_OK) return rc;
+    const long long tiles = (static_cast<long long>(p.n_rows) + TC_RT - 1) / TC_RT;
+    p.U = tiles * p.G;
+    long long B = st.sms;
+    if (B > p.U) B = p.U;
+    p.part = st.wpart;
+    p.ctr = st.ctr;
+    p.keys = st.keys;
+    p.done = st.done;
+    p.err = st.err;
+    p.stall_ns = g_stall_ns.load(std::memory_order_relaxed);
+    p.x16 = st.x16;
+    p.xinv = st.xinv;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // the activations, converted into the tensor cores' K-major layout first
+    cfg.gridDim = dim3(32);
+    cfg.blockDim = dim3(XP_THREADS);
+    cfg.dynamicSmemBytes = 0;
+    if (cudaLaunchKernelEx(&cfg, xprep_kernel<true>, p.x, p.T, p.K, 32, st.x16, st.xinv) != cudaSuccess) {
+        cudaGetLastError();
+        return SV_ERR_CUDA;
+    }
+    cfg.gridDim = dim3(static_cast<unsigned>(B));
+    cfg.blockDim = dim3(TC_WARPS * 32);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    if (cudaLaunchKernelEx(&cfg, w4a16_tc_kernel<HEAD>, p, tmW, tmS) != cudaSuccess) {
+        cudaGetLastError();
+        return SV_ERR_CUDA;
+    }
+    return SV_OK;
+}
+
+// The tcgen05 kernel can serve four token tiles (17 <= T <= 32) of
+// contiguous rows whose scale rows are 16-byte multiples (G % 8 == 0), when
+// the device state has its partial-sum area.  It is correct but measured
+// slower than the mma.sync kernel (lm_head, four streams x 8 rows: 305 us
+// against 271 us), so it runs only when sv_debug_set_tcgen05 asks for it.
+template <bool HEAD, bool GATHER>
+bool use_tc(const Params &p, const DeviceState &st)
+{
+    return g_tcgen05.load(std::memory_order_relaxed) && !GATHER && st.wpart && p.T > 16 && (p.G % 8) == 0 &&
+           !p.y32;
+}
+
 template <bool HEAD, bool GATHER>
 bool use_wide(const Params &p, const DeviceState &st)
 {
@@ -441,6 +539,7 @@ bool use_wide(const Params &p, const DeviceState &st)
 template <bool HEAD, bool GATHER>
 int dispatch(Params &p, const DeviceState &st, cudaStream_t stream)
 {
+    if (use_tc<HEAD, GATHER>(p, st)) return launch_tc<HEAD>(p, st, stream);
     if (use_wide<HEAD, GATHER>(p, st)) return launch_wide<2, HEAD, 8>(p, st, stream);
     if (p.T <= 8) {
         if (static_cast<long long>(p.T + 1) * (2LL * p.K + 16) <= XRES_MAX_BYTES &&
@@ -1029,6 +1128,12 @@ int sv_hbm_read(const void *src, size_t bytes, uint32_t *sink, sv_stream stream)
 int sv_debug_set_fma_consumers(int on)
 {
     sv::g_fma_consumers.store(on ? 1 : 0, std::memory_order_relaxed);
+    return SV_OK;
+}
+
+int sv_debug_set_tcgen05(int on)
+{
+    sv::g_tcgen05.store(on ? 1 : 0, std::memory_order_relaxed);
     return SV_OK;
 }
 

@@ -215,6 +215,21 @@ __device__ __forceinline__ int chunk_slot(int i)
 // 2^-s_t.  One CTA per token row.  The main kernel then copies ready-made
 // group blocks into its stages (one bulk copy per group) and its B loads
 // need neither byte permutes nor conversion.
+//
+// TC = true writes the layout of w4a16_tc_kernel instead: per group a block
+// of 8 KB holding, for 16-byte chunk k (0..15, eight columns) and token t
+// (0..31), the chunk at ((k * 4 + t / 8) * 8 + t % 8) * 16 -- "core
+// matrices" of 8 tokens x 16 bytes, 128 bytes apart along the tokens and
+// 512 bytes apart along K, the canonical K-major layout a tcgen05 B operand
+// is described by; no chunk swizzle.
+template <bool TC>
+__device__ __forceinline__ size_t xprep_offset(int i, int t, int TP)
+{
+    if (TC) return static_cast<size_t>(i >> 4) * 8192 + static_cast<size_t>(((i & 15) * 4 + (t >> 3)) * 128 + (t & 7) * 16);
+    return (static_cast<size_t>(i >> 4) * TP + t) * XSTR + chunk_slot(i & 15) * 16;
+}
+
+template <bool TC>
 __global__ void __launch_bounds__(XP_THREADS) xprep_kernel(const uint16_t *x, int T, int K, int TP, uint8_t *x16,
                                                            float *xinv)
 {
@@ -224,8 +239,7 @@ __global__ void __launch_bounds__(XP_THREADS) xprep_kernel(const uint16_t *x, in
     const int cpr = K / 8;              // 16-byte chunks per row
     if (t >= T) {
         for (int i = tid; i < cpr; i += XP_THREADS)
-            *reinterpret_cast<uint4 *>(x16 + (static_cast<size_t>(i >> 4) * TP + t) * XSTR + (i & 15) * 16) =
-                make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4 *>(x16 + xprep_offset<TC>(i, t, TP)) = make_uint4(0u, 0u, 0u, 0u);
         if (tid == 0) xinv[t] = 1.f;
         return;
     }
@@ -265,9 +279,7 @@ __global__ void __launch_bounds__(XP_THREADS) xprep_kernel(const uint16_t *x, in
 #pragma unroll
         for (int u = 0; u < XB; ++u) {
             const int i = i0 + u * XP_THREADS;
-            if (i < cpr)
-                *reinterpret_cast<uint4 *>(x16 + (static_cast<size_t>(i >> 4) * TP + t) * XSTR +
-                                           chunk_slot(i & 15) * 16) = chunk_to_f16(r[u], sc);
+            if (i < cpr) *reinterpret_cast<uint4 *>(x16 + xprep_offset<TC>(i, t, TP)) = chunk_to_f16(r[u], sc);
         }
     }
     if (tid == 0) xinv[t] = __uint_as_float(static_cast<uint32_t>(127 - sh) << 23);
