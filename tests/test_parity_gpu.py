@@ -92,6 +92,57 @@ def test_gpu_one_hot_pins_nibble_order_and_page_constant(sv, oracle):
         assert np.array_equal(got, expect)
 
 
+@pytest.mark.parametrize("path", ["bf16_stages", "resident"])
+def test_gpu_one_hot_at_one_token(sv, oracle, path):
+    """The one-hot pin at T = 1 on the two one-token-tile paths: activations
+    copied into every stage as bf16 with the bf16 dequantisation (0x4300
+    OR, then -136; the QKV and down GEMMs of the step), and resident fp16
+    rows with the fp16 dequantisation (enough rows for the resident rule).
+    Each call has one nonzero activation, so y[n] = (nibble - 8) * s
+    exactly, for every k of two groups and every nibble value."""
+    K = 256
+    N = 64 if path == "bf16_stages" else resident_rows(K)
+    W = K // 8
+    rng = np.random.default_rng(62)
+    Wq = rng.integers(0, 2**32, size=(N, W), dtype=np.uint32)
+    Wq[:16, :] = np.array([int(("%x" % n) * 8, 16) for n in range(16)], np.uint32)[:, None]
+    s = gen.f32_to_bf16_bits((2.0 ** rng.integers(-4, 3, size=(N, K // 128))).astype(np.float32))
+    sval = gen.bf16_bits_to_f32(s).astype(np.float64)
+    one = gen.f32_to_bf16_bits(np.float32(1.0))
+    dW, ds = dev_words(Wq), dev_bits16(s)
+    for k in range(K):
+        x = np.zeros((1, K), np.uint16)
+        x[0, k] = one
+        y = sv.w4a16_gemm(dev_bits16(x), dW, ds)
+        torch.cuda.synchronize()
+        got = to_f32(y).astype(np.float64)[0]
+        level = ((Wq[:, k // 8] >> np.uint32(4 * (k % 8))) & 0xF).astype(np.int64) - 8
+        assert np.array_equal(got, level * sval[:, k // 128]), k
+    assert sv.last_device_error() == 0
+
+
+@pytest.mark.parametrize("T,V,K", [(1, 3000, 1024), (4, "resident", 1024), (8, 5000, 2048)])
+def test_gemm_rows_match_the_heads_argmax_values(sv, oracle, T, V, K):
+    """Cross-export consistency: w4a16_gemm over the head's rows (N = V)
+    computes the same fp32 sums as lmhead_argmax, so at each row's argmax id
+    the GEMM's bf16 output is exactly the bf16 rounding of the fp32 logit
+    lmhead_argmax returns, and no GEMM output exceeds it after rounding."""
+    if V == "resident":
+        V = resident_rows(K)
+    rng = np.random.default_rng(7100 + T + K)
+    Wq, sc = gen.weights(rng, V, K)
+    x = gen.activations(rng, T, K)
+    dx, dW, ds = dev_bits16(x), dev_words(Wq), dev_bits16(sc)
+    ids, vals = sv.lmhead_argmax(dx, dW, ds)
+    y = sv.w4a16_gemm(dx, dW, ds)
+    torch.cuda.synchronize()
+    yb = y.view(torch.int16).cpu().numpy().view(np.uint16)
+    ids, vals = ids.cpu().numpy(), vals.cpu().numpy()
+    for t in range(T):
+        assert yb[t, ids[t]] == gen.f32_to_bf16_bits(np.float32(vals[t])), t
+        assert gen.bf16_bits_to_f32(yb[t]).max() == gen.bf16_bits_to_f32(yb[t, ids[t]]), t
+
+
 # --------------------------------------------------------------------------
 # GEMM parity
 
