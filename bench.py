@@ -128,7 +128,7 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
-KERNEL_SOURCES = ("w4a16_stream.cuh", "sv_ptx.cuh")
+KERNEL_SOURCES = ("w4a16_stream.cuh", "w4a16_wide.cuh", "w4a16_tc.cuh", "sv_ptx.cuh")
 
 
 def kernel_source_digest():

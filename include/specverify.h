@@ -406,15 +406,15 @@ int sv_hbm_read(const void *src, size_t bytes, uint32_t *sink, sv_stream stream)
 int sv_debug_set_fma_consumers(int on);
 
 /*
- * sv_debug_set_tcgen05 -- a measurement switch: with on != 0, later calls
- * with 17 <= T <= 32 (four n8 token tiles), contiguous rows and K a
- * multiple of 1024 run on the 5th-generation tensor cores (tcgen05.mma,
- * M = 128 weight rows x N = 32 tokens x K = 16, the dequantised levels
- * stored to tensor memory as the A operand, fp32 group sums accumulated in
- * tensor memory and scaled in registers) instead of mma.sync; same results
- * within fp32 rounding order.  It exists to measure that formulation (it
- * measured slower, so mma.sync is the default); 0 restores the default.
- * Process-wide.  No source page has a counterpart.
+ * sv_debug_set_tcgen05 -- a measurement switch.  Calls with 17 <= T <= 32
+ * (four n8 token tiles), contiguous rows and K a multiple of 1024 run by
+ * default on the 5th-generation tensor cores (tcgen05.mma, M = 128 weight
+ * rows x N = 32 tokens x K = 16, the dequantised levels stored to tensor
+ * memory as the A operand, each group's fp32 sum accumulated in tensor
+ * memory and scaled in registers); on = 0 makes them run on mma.sync
+ * instead (same results within fp32 rounding order), 1 restores the
+ * default.  It exists to measure the two against each other.  Process-wide.
+ * No source page has a counterpart.
  */
 int sv_debug_set_tcgen05(int on);
 

@@ -510,6 +510,6 @@ def debug_set_fma_consumers(on: bool) -> None:
 
 
 def debug_set_tcgen05(on: bool) -> None:
-    """Measurement switch (sv_debug_set_tcgen05): the tcgen05 kernel for
-    calls with 17 <= T <= 32 instead of the mma.sync kernel."""
+    """Measurement switch (sv_debug_set_tcgen05): calls with 17 <= T <= 32
+    run on the tcgen05 kernel (the default, True) or on mma.sync (False)."""
     _check("sv_debug_set_tcgen05", load().sv_debug_set_tcgen05(1 if on else 0))

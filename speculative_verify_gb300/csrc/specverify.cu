@@ -65,7 +65,7 @@ DeviceState g_state[MAX_DEVICES];
 std::mutex g_mu;
 std::atomic<uint32_t> g_stall_ns{0};    // sv_debug_set_wait_stall
 std::atomic<int> g_fma_consumers{0};     // sv_debug_set_fma_consumers
-std::atomic<int> g_tcgen05{0};           // sv_debug_set_tcgen05
+std::atomic<int> g_tcgen05{1};           // sv_debug_set_tcgen05
 
 template <int NT, bool HEAD, bool GATHER, bool XRES, bool FMA = false>
 cudaError_t raise_smem_limit(int bytes)
@@ -438,8 +438,8 @@ int launch_wide(Params p, const DeviceState &st, cudaStream_t stream)
 // kernel's 168-register cap spills and runs 10 % slower), stay on the
 // 64-row kernel; the 256-row variant measured slower everywhere.
 // Shared-memory layout of a tcgen05 launch (offsets in bytes): nst stages
-// of 16 KB (8 KB of packed weights, 8 KB of activations) from 0 -- 1024-byte
-// aligned, as the swizzled weight boxes need | the four-slot scale ring | the
+// of TC_GU x 16 KB (8 KB of packed weights and 8 KB of activations per
+// group) from 0 -- 1024-byte aligned, as the swizzled weight boxes need | the four-slot scale ring | the
 // head's key table | mbarriers, flag, decision word, tensor-memory address.
 template <bool HEAD>
 int plan_layout_tc(Params &p, int smem_optin, int *smem_total)
@@ -480,7 +480,7 @@ int launch_tc(Params p, const DeviceState &st, cudaStream_t stream)
                    static_cast<unsigned long long>(p.n_rows), 8, TC_RT);
     if (rc != SV_OK) return rc;
     const long long tiles = (static_cast<long long>(p.n_rows) + TC_RT - 1) / TC_RT;
-    p.U = tiles * p.G;
+    p.U = tiles * (p.G / TC_GU);             // a unit is TC_GU groups of one tile
     long long B = st.sms;
     if (B > p.U) B = p.U;
     p.part = st.wpart;
@@ -516,11 +516,12 @@ int launch_tc(Params p, const DeviceState &st, cudaStream_t stream)
     return SV_OK;
 }
 
-// The tcgen05 kernel can serve four token tiles (17 <= T <= 32) of
-// contiguous rows whose scale rows are 16-byte multiples (G % 8 == 0), when
-// the device state has its partial-sum area.  It is correct but measured
-// slower than the mma.sync kernel (lm_head, four streams x 8 rows: 305 us
-// against 271 us), so it runs only when sv_debug_set_tcgen05 asks for it.
+// The tcgen05 kernel serves four token tiles (17 <= T <= 32) of contiguous
+// rows whose scale rows are 16-byte multiples (G % 8 == 0), when the device
+// state has its partial-sum area.  Measured against the mma.sync kernel at
+// T = 32 (back to back): lm_head 250 us against 267, gate+up GEMM 38.6
+// against 51.7, down 32.6 against 39.2, QKV 25.2 against 25.9.
+// sv_debug_set_tcgen05(0) selects the mma.sync kernel for comparison.
 template <bool HEAD, bool GATHER>
 bool use_tc(const Params &p, const DeviceState &st)
 {

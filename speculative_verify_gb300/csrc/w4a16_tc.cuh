@@ -47,21 +47,23 @@
 namespace sv {
 
 constexpr int TC_RT = 128;                       // rows per tile (the MMA's M)
+constexpr int TC_GU = 2;                         // 128-column groups per unit (one hand-off per TC_GU groups)
 constexpr int TC_W_BYTES = TC_RT * 64;           // one group of a tile's packed weights
 constexpr int TC_X_BYTES = 32 * 128 * 2;         // one group of 32 tokens, fp16
-constexpr int TC_STAGE = TC_W_BYTES + TC_X_BYTES;
+constexpr int TC_STAGE = TC_GU * (TC_W_BYTES + TC_X_BYTES);   // weights of the unit's groups, then their activations
 constexpr int TC_RING = 4;                       // scale-ring slots
 constexpr int TC_RING_SLOT = TC_RT * 16;         // 8 groups of bf16 scales per row
-constexpr int TC_NDQ = 3;                        // dequant warpgroups, taking units in turn
-constexpr int TC_NA = 2 * TC_NDQ;                // A buffers: two per dequant warpgroup
+constexpr int TC_NDQ = 2;                        // dequant warpgroups, taking units in turn
+constexpr int TC_NA = 3;                         // A buffers of TC_GU x 64 columns
+constexpr int TC_NACC = 2;                       // accumulators of TC_GU x 32 columns
 constexpr uint32_t TC_TMEM_COLS = 512;
-constexpr uint32_t TC_ACC_COL = TC_NA * 64;      // the 32-column accumulators after the A buffers
-constexpr int TC_NACC = 4;                       // accumulators (units in flight between MMA and epilogue)
+constexpr uint32_t TC_ACC_COL = TC_NA * 64 * TC_GU;   // the accumulators after the A buffers
 constexpr int TC_DQ0 = 2;                        // first dequant warp
 constexpr int TC_EP0 = TC_DQ0 + 4 * TC_NDQ;      // first epilogue warp
 constexpr int TC_MMA2 = TC_EP0 + 4;              // second MMA-issuing warp
 constexpr int TC_WARPS = TC_MMA2 + 1;
-constexpr int TC_MAX_STAGES = 12;                // the ring's reuse rule holds up to 25
+constexpr int TC_MAX_STAGES = 12;                // the ring's reuse rule holds up to 13
+static_assert(TC_ACC_COL + TC_NACC * 32 * TC_GU <= TC_TMEM_COLS, "tensor memory budget");
 // Instruction descriptor of kind::f16: D fp32 (bits 4-5 = 1), A and B fp16
 // (bits 7-9, 10-12 = 0), both K-major (bits 15, 16 = 0), N >> 3 at bits
 // 17-22, M >> 4 at bits 24-28.
@@ -102,7 +104,8 @@ w4a16_tc_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int B = gridDim.x, b = blockIdx.x;
     const long long U = p.U;
-    const int G = p.G, T = p.T;
+    const int T = p.T;
+    const int G = p.G / TC_GU;               // units per tile (each TC_GU groups)
     const long long u0 = cta_start(b, U, B), u1 = cta_start(b + 1, U, B);
     const int tile_first = static_cast<int>(u0 / G);
     const int grp_first = static_cast<int>(u0 - static_cast<long long>(tile_first) * G);
@@ -159,21 +162,26 @@ w4a16_tc_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
                 if (i >= nst) wait_or_flag(p, flag, smem_addr(&empty[s]), static_cast<uint32_t>(((i / nst) & 1) ^ 1));
                 const uint32_t fb = smem_addr(&full[s]);
                 const uint32_t stage = s0 + static_cast<uint32_t>(s * TC_STAGE);
-                const bool nb = wide_new_box(i == 0, grp);
+                const int g0 = grp * TC_GU;              // the unit's first group
+                const bool nb = wide_new_box(i == 0, g0);
                 if (nb) ++box;
                 mbar_arrive_expect_tx(fb, static_cast<uint32_t>(TC_STAGE + (nb ? TC_RING_SLOT : 0)));
-                tma_load_2d(stage, &tmW, grp * 16, tile * TC_RT, fb, pol_w);
+#pragma unroll
+                for (int g = 0; g < TC_GU; ++g)
+                    tma_load_2d(stage + g * TC_W_BYTES, &tmW, (g0 + g) * 16, tile * TC_RT, fb, pol_w);
                 if (nb)
-                    tma_load_2d(smem_addr(ring) + static_cast<uint32_t>((box % TC_RING) * TC_RING_SLOT), &tmS, grp & ~7,
+                    tma_load_2d(smem_addr(ring) + static_cast<uint32_t>((box % TC_RING) * TC_RING_SLOT), &tmS, g0 & ~7,
                                 tile * TC_RT, fb, pol_w);
                 if (i >= n_pre)
-                    bulk_g2s(stage + TC_W_BYTES, p.x16 + static_cast<size_t>(grp) * TC_X_BYTES, TC_X_BYTES, fb, pol_x);
+                    bulk_g2s(stage + TC_GU * TC_W_BYTES, p.x16 + static_cast<size_t>(g0) * TC_X_BYTES,
+                             TC_GU * TC_X_BYTES, fb, pol_x);
                 if (i == n_pre - 1) {
                     pdl_wait_prior();       // the activation blocks come from the conversion kernel
                     int g2 = grp_first;
                     for (int j = 0; j < n_pre; ++j) {
-                        bulk_g2s(s0 + static_cast<uint32_t>(j * TC_STAGE + TC_W_BYTES),
-                                 p.x16 + static_cast<size_t>(g2) * TC_X_BYTES, TC_X_BYTES, smem_addr(&full[j]), pol_x);
+                        bulk_g2s(s0 + static_cast<uint32_t>(j * TC_STAGE + TC_GU * TC_W_BYTES),
+                                 p.x16 + static_cast<size_t>(g2 * TC_GU) * TC_X_BYTES, TC_GU * TC_X_BYTES,
+                                 smem_addr(&full[j]), pol_x);
                         if (++g2 == G) g2 = 0;
                     }
                 }
@@ -200,11 +208,15 @@ w4a16_tc_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
                 if (i >= TC_NACC)
                     wait_or_flag(p, flag, smem_addr(&d_empty[db]), static_cast<uint32_t>(((i / TC_NACC) & 1) ^ 1));
                 tc_fence_after_sync();
-                const uint32_t d = tmem + TC_ACC_COL + 32u * db;
-                const uint32_t a = tmem + 64u * ab;
-                const uint32_t xs = s0 + static_cast<uint32_t>(s * TC_STAGE + TC_W_BYTES);
 #pragma unroll
-                for (int k = 0; k < 8; ++k) tc_mma_f16_ts(d, a + 8u * k, tc_bdesc(xs + 1024u * k), TC_IDESC, k > 0);
+                for (int g = 0; g < TC_GU; ++g) {
+                    // group g of the unit: its own accumulator (each group's sum is scaled on its own)
+                    const uint32_t d = tmem + TC_ACC_COL + 32u * (TC_GU * db + g);
+                    const uint32_t a = tmem + 64u * (TC_GU * ab + g);
+                    const uint32_t xs = s0 + static_cast<uint32_t>(s * TC_STAGE + TC_GU * TC_W_BYTES + g * TC_X_BYTES);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) tc_mma_f16_ts(d, a + 8u * k, tc_bdesc(xs + 1024u * k), TC_IDESC, k > 0);
+                }
                 tc_commit(smem_addr(&a_empty[ab]));
                 tc_commit(smem_addr(&empty[s]));
                 tc_commit(smem_addr(&d_full[db]));
@@ -224,14 +236,16 @@ w4a16_tc_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
             const int s = i % nst, ab = i % TC_NA;
             wait_or_flag(p, flag, smem_addr(&full[s]), static_cast<uint32_t>((i / nst) & 1));
             if (i >= TC_NA) wait_or_flag(p, flag, smem_addr(&a_empty[ab]), static_cast<uint32_t>(((i / TC_NA) & 1) ^ 1));
-            const uint32_t wrow = s0 + static_cast<uint32_t>(s * TC_STAGE + row * 64);
-            const uint32_t tlane = tmem + (static_cast<uint32_t>(32 * q) << 16) + 64u * ab;
+            const uint32_t wrow0 = s0 + static_cast<uint32_t>(s * TC_STAGE + row * 64);
+            const uint32_t tlane0 = tmem + (static_cast<uint32_t>(32 * q) << 16) + 64u * TC_GU * ab;
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {          // words 0..7, then 8..15: 32 columns each
+            for (int hf = 0; hf < 2 * TC_GU; ++hf) {  // per group: words 0..7, then 8..15, 32 columns each
+                const uint32_t wrow = wrow0 + static_cast<uint32_t>((hf >> 1) * TC_W_BYTES);
+                const uint32_t tlane = tlane0 + 64u * (hf >> 1);
                 uint32_t v[32];
 #pragma unroll
                 for (int jj = 0; jj < 2; ++jj) {
-                    const int j = 2 * hf + jj;
+                    const int j = 2 * (hf & 1) + jj;
                     const uint4 w4 = lds128(wrow + ((static_cast<uint32_t>(j) ^ sw) << 4));
                     const uint32_t ws[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
@@ -244,7 +258,7 @@ w4a16_tc_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
                         v[c0 + 3] = dequant2_f16_hi(w >> 8);      // (3, 7)
                     }
                 }
-                tmem_st32(tlane + 32u * hf, v);
+                tmem_st32(tlane + 32u * (hf & 1), v);
             }
             tmem_wait_st();
             tc_fence_before_sync();
@@ -283,23 +297,27 @@ w4a16_tc_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
         int tile = tile_first, grp = grp_first, box = -1;
         for (int i = 0; i < n_units; ++i) {
             const int s = i % nst, db = i % TC_NACC;
-            if (wide_new_box(i == 0, grp)) ++box;
+            if (wide_new_box(i == 0, grp * TC_GU)) ++box;
             wait_or_flag(p, flag, smem_addr(&full[s]), static_cast<uint32_t>((i / nst) & 1));
             wait_or_flag(p, flag, smem_addr(&d_full[db]), static_cast<uint32_t>((i / TC_NACC) & 1));
             tc_fence_after_sync();
-            uint32_t v[32];
-            tmem_ld32(taddr + 32u * db, v);
-            tmem_wait_ld();
-            const float sc = bf16_bits_to_float(
-                lds_u16(smem_addr(ring) + static_cast<uint32_t>((box % TC_RING) * TC_RING_SLOT + row * 16 + (grp & 7) * 2)));
+#pragma unroll
+            for (int g = 0; g < TC_GU; ++g) {
+                uint32_t v[32];
+                tmem_ld32(taddr + 32u * (TC_GU * db + g), v);
+                tmem_wait_ld();
+                const float sc = bf16_bits_to_float(lds_u16(
+                    smem_addr(ring) +
+                    static_cast<uint32_t>((box % TC_RING) * TC_RING_SLOT + row * 16 + ((grp * TC_GU + g) & 7) * 2)));
+#pragma unroll
+                for (int t = 0; t < 32; ++t) acc[t] += sc * __uint_as_float(v[t]);
+            }
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(smem_addr(&d_empty[db]));
                 mbar_arrive(smem_addr(&empty[s]));
             }
-#pragma unroll
-            for (int t = 0; t < 32; ++t) acc[t] += sc * __uint_as_float(v[t]);
 
             const bool tile_end = (grp == G - 1) || (i == n_units - 1);
             if (++grp == G) grp = 0;

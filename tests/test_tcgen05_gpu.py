@@ -1,6 +1,7 @@
-"""The tcgen05 kernel (5th-generation tensor cores, accumulators in tensor
-memory), selected by the sv_debug_set_tcgen05 measurement switch for calls
-with 17 <= T <= 32 and K a multiple of 1024, against the CPU oracle: the
+"""Calls with 17 <= T <= 32 and K a multiple of 1024 on both of their
+kernels -- the tcgen05 kernel (5th-generation tensor cores, accumulators in
+tensor memory; the default) and the mma.sync kernel (sv_debug_set_tcgen05(0))
+-- against the CPU oracle: the
 one-hot pin of the levels' order in tensor memory against the activations'
 K-major layout, wide-range activations, GEMM shapes with split tiles, and the
 greedy verify up to the full four-stream lm_head."""
@@ -15,8 +16,10 @@ torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module")
-def sv():
+@pytest.fixture(scope="module", params=["tcgen05", "mma_sync"])
+def sv(request):
+    """The library with calls of 17 <= T <= 32 on the tcgen05 kernel (the
+    default) and, for the second pass, on the mma.sync kernel."""
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     import speculative_verify_gb300 as m
@@ -24,9 +27,9 @@ def sv():
     build.build()
     m.load()
     assert m.last_device_error() == 0
-    m.debug_set_tcgen05(True)
+    m.debug_set_tcgen05(request.param == "tcgen05")
     yield m
-    m.debug_set_tcgen05(False)
+    m.debug_set_tcgen05(True)
 
 
 def test_one_hot_pins_tensor_memory_layout(sv, oracle):
