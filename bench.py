@@ -32,6 +32,7 @@ import hashlib
 import json
 import os
 import platform
+import re
 import subprocess
 import sys
 import threading
@@ -95,6 +96,17 @@ def kernels_per_call(T):
     return 2 if T > 8 else 1
 
 
+def kernel_of(c):
+    """The kernel the library dispatches a bench call to (its rule, for the
+    shapes here): tcgen05 for 17..32 tokens, the 512-row kernel for a full-
+    vocabulary head of 9..16 tokens, the stream kernel otherwise."""
+    if c["T"] > 16:
+        return "w4a16_tc_kernel"
+    if c["T"] > 8 and c["kind"] == "head" and c.get("vm") is None:
+        return "w4a16_wide_kernel"
+    return "w4a16_stream_kernel"
+
+
 # ----------------------------------------------------------------------------
 # helpers
 
@@ -128,32 +140,50 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
-KERNEL_SOURCES = ("w4a16_stream.cuh", "w4a16_wide.cuh", "w4a16_tc.cuh", "sv_ptx.cuh")
+KERNEL_SOURCES = {
+    "w4a16_stream_kernel": ("w4a16_stream.cuh", "sv_ptx.cuh"),
+    "w4a16_wide_kernel": ("w4a16_stream.cuh", "w4a16_wide.cuh", "sv_ptx.cuh"),
+    "w4a16_tc_kernel": ("w4a16_stream.cuh", "w4a16_wide.cuh", "w4a16_tc.cuh", "sv_ptx.cuh"),
+}
 
 
-def kernel_source_digest():
-    """Digest of the device-code sources; ncu counters recorded for another
-    digest describe a different kernel and are not reported."""
-    h = hashlib.sha256()
+def code_only(src):
+    """C++ source without its comments and with runs of whitespace made one
+    space: what the compiler sees of it."""
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return " ".join(src.split())
+
+
+def kernel_source_digest(kernel="w4a16_stream_kernel", read=None):
+    """Digest of the device code a kernel is compiled from (its sources
+    without comments); ncu counters recorded for another digest describe a
+    different kernel and are not reported.  `read(name)` gives a source's
+    text (default: the working tree's file)."""
     csrc = os.path.join(ROOT, "speculative_verify_gb300", "csrc")
-    for name in KERNEL_SOURCES:
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode())
-            h.update(f.read())
+    if read is None:
+        def read(name):
+            with open(os.path.join(csrc, name)) as f:
+                return f.read()
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kernel]:
+        h.update(name.encode())
+        h.update(code_only(read(name)).encode())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it
-    was taken on the current kernel sources; else None."""
+def recorded_traffic(call, kernel):
+    """DRAM bytes per launch of the bench call `call` (run by `kernel`) from
+    the committed ncu summary, if it was taken on the kernel's current
+    sources; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
-    digest = kernel_source_digest()
+    digest = kernel_source_digest(kernel)
     with open(path) as f:
         for line in f:
             parts = line.split()
-            if len(parts) >= 3 and not line.startswith("#") and parts[0] == kernel and parts[1] == digest:
+            if len(parts) >= 3 and not line.startswith("#") and parts[0] == call and parts[1] == digest:
                 return int(parts[2])
     return None
 
@@ -703,7 +733,7 @@ def run_ours(args, rank, world, local_rank):
             ci += 1
             cg = c["bytes"] / (cm * 1e-3) / 1e9
             ceil = ceilings[c["wbytes"]]
-            cl.append({"call": c["label"], "us": round(cm * 1e3, 2), "GB/s": round(cg, 1),
+            cl.append({"call": c["label"], "kernel": kernel_of(c), "us": round(cm * 1e3, 2), "GB/s": round(cg, 1),
                        "frac_of_8TBps": round(cg / NOMINAL_HBM_GBS, 4), "frac_of_measured_copy": round(cg / peak, 4),
                        "read_ceiling": {"GB/s": round(ceil, 1), "frac": round(cg / ceil, 4)}})
         legs_out.append({"leg": l["name"], "config": l["config"], "T": l["T"], "bytes": l["bytes"],
@@ -718,14 +748,14 @@ def run_ours(args, rank, world, local_rank):
         "frac_of_8TBps": value / world / NOMINAL_HBM_GBS,
         "frac_of_measured_copy": value / world / peak,
         "legs": legs_out,
-        "roofline": {"kernel": "%s (w4a16_stream_kernel)" % dom["label"], "bound": "hbm",
+        "roofline": {"kernel": "%s (%s)" % (dom["label"], kernel_of(dom)), "bound": "hbm",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind
                      if peak_kind == "measured" else "fallback",
                      "algorithmic_bytes_per_launch": dom["bytes"],
                      "avg_launch_ms": call_ms[i_dom],
                      "share_of_step": call_ms[i_dom] / full_ms,
-                     "traffic": recorded_traffic(dom["label"])},
+                     "traffic": recorded_traffic(dom["label"], kernel_of(dom))},
         "clocks": clocks,
         "e2e": {"value": job_gbs(world, wl.bytes_per_step, 1, e2e_ms), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -887,6 +917,8 @@ def run_ncu_case(args):
     T = args.ncu_T
     if args.ncu_fma:
         sv.debug_set_fma_consumers(True)
+    if args.ncu_mma_sync:
+        sv.debug_set_tcgen05(False)
     if args.ncu_case == "step":
         # one warm-up step, then the profiled step: 21 launches each
         wl = Workload(torch, device)
@@ -950,6 +982,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ncu-case", choices=["head", "gemm", "sampled", "rescored", "restricted", "step"], default=None)
     ap.add_argument("--ncu-fma", action="store_true", help="CUDA-core consumers (sv_debug_set_fma_consumers)")
+    ap.add_argument("--ncu-mma-sync", action="store_true",
+                    help="the mma.sync stream kernel for 17..32 tokens (sv_debug_set_tcgen05(0))")
     ap.add_argument("--ncu-T", type=int, default=4)
     ap.add_argument("--ncu-streams", type=int, default=1)
     ap.add_argument("--ncu-shape", choices=[s[0] for s in gen.GEMM_SHAPES], default="gate_up")

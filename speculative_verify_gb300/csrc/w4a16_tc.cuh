@@ -8,37 +8,37 @@
 // tcgen05.mma of M = 128 weight rows x N = 32 tokens x K = 16 does the work
 // of 32 of them.
 //
-// Work: a unit is one 128-row tile x one 128-column group; units are
-// numbered tile-major and split evenly over the grid (stream-K), split tiles
-// finished in CTA order as in the other kernels.
+// Work: a unit is one 128-row tile x two 128-column groups (TC_GU); units
+// are numbered tile-major and split evenly over the grid (stream-K), split
+// tiles finished in CTA order as in the other kernels.
 //
-// Warp roles (19 warps):
-//  * warp 0, producer (lane 0): per unit, the group's packed weights of the
-//    tile's 128 rows (a TMA box, 64-byte swizzle), the group's activations
-//    in the canonical K-major layout written by xprep_kernel<true> (one bulk
-//    copy, 8 KB) and, every eight groups, the rows' scales for those groups
-//    (a TMA box of 8 x 128 bf16) into a four-slot ring; completion on the
-//    stage's mbarrier.  Weights and scales of the first stages go out before
-//    griddepcontrol.wait.
-//  * warp 1 allocates the CTA's tensor memory (all 512 columns: six 64-column
-//    A buffers and four 32-column accumulators) and frees it at the end.
-//    Lane 0 of warps 1 and 18 issue the MMAs of the even and the odd units:
-//    per unit eight tcgen05.mma (A from tensor memory, B = the stage's
-//    activation block, D = accumulator unit % 4, cleared by the first), then
-//    commits to the A buffer's, the stage's and the accumulator's mbarriers.  (One issuing thread measured 1,470 cycles
-//    per unit: about 500 to issue the eight MMAs and as many again in its
-//    barrier waits; two overlap them.)
-//  * warps 2..13, dequant (three warpgroups taking units in turn, each with
-//    two A buffers):
-//    thread = weight row; it reads its row's 16 words, turns the 128
-//    nibbles into fp16 levels (pairs (j, j+4), the order the activation
+// Warp roles (15 warps):
+//  * warp 0, producer (lane 0): per unit, the two groups' packed weights of
+//    the tile's 128 rows (TMA boxes, 64-byte swizzle), the groups'
+//    activations in the canonical K-major layout written by
+//    xprep_kernel<true> (one bulk copy, 16 KB) and, every eight groups, the
+//    rows' scales for those groups (a TMA box of 8 x 128 bf16) into a
+//    four-slot ring; completion on the stage's mbarrier.  Weights and scales
+//    of the first stages go out before griddepcontrol.wait.
+//  * warp 1 allocates the CTA's tensor memory (all 512 columns: three
+//    128-column A buffers and two 64-column accumulator pairs) and frees it
+//    at the end.  Lane 0 of warps 1 and 14 issue the MMAs of the even and the
+//    odd units: per group eight tcgen05.mma (A from tensor memory, B = the
+//    stage's activation block, D = the group's own accumulator, cleared by
+//    the first), then one set of commits per unit to the A buffer's, the
+//    stage's and the accumulator pair's mbarriers.  (One hand-off costs about
+//    as much as the eight MMAs of a group; two groups per unit and two
+//    issuers that alternate hide part of it.)
+//  * warps 2..9, dequant (two warpgroups taking units in turn):
+//    thread = weight row; per group it reads its row's 16 words, turns the
+//    128 nibbles into fp16 levels (pairs (j, j+4), the order the activation
 //    chunks use) and stores them to its tensor-memory lane as the A operand.
-//  * warps 14..17, epilogue: thread = row; per unit it reads the row's 32
-//    fp32 group sums back from tensor memory, multiplies them by the row's
-//    group scale and adds them to its fp32 accumulators (the scale applied
-//    after each group's sum, as in the other kernels); at the end of its
-//    share of a tile it writes y or folds the logits into per-token argmax
-//    keys.
+//  * warps 10..13, epilogue: thread = row; per unit it reads the row's 32
+//    fp32 sums of each group back from tensor memory, multiplies them by the
+//    row's group scale and adds them to its fp32 accumulators (the scale
+//    applied after each group's sum, as in the other kernels); at the end of
+//    its share of a tile it writes y or folds the logits into per-token
+//    argmax keys.
 #pragma once
 
 #include "w4a16_stream.cuh"
