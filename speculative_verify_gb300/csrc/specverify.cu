@@ -439,26 +439,31 @@ int launch_wide(Params p, const DeviceState &st, cudaStream_t stream)
 // 64-row kernel; the 256-row variant measured slower everywhere.
 // Shared-memory layout of a tcgen05 launch (offsets in bytes): nst stages
 // of TC_GU x 16 KB (8 KB of packed weights and 8 KB of activations per
-// group) from 0 -- 1024-byte aligned, as the swizzled weight boxes need | the four-slot scale ring | the
-// head's key table | mbarriers, flag, decision word, tensor-memory address.
+// group) from 0 -- 1024-byte aligned, as the swizzled weight boxes need |
+// the head's two finished-tile buffers | mbarriers, flag, decision word,
+// tensor-memory address, the buffers' tile numbers.  (The scales go from global memory to the dequant and epilogue
+// threads' registers, one 16-byte load per row and box.)
 template <bool HEAD>
 int plan_layout_tc(Params &p, int smem_optin, int *smem_total)
 {
-    const int ring_bytes = TC_RING * TC_RING_SLOT;
-    const int kt_bytes = HEAD ? 4 * TMAX * 8 : 0;
-    int nst = (smem_optin - ring_bytes - kt_bytes - 512) / TC_STAGE;
+    const int tb_bytes = HEAD ? 2 * TC_TB_BYTES : 0;   // the head's two finished-tile buffers
+    const int bar_bytes = 1024;              // mbarriers and flags, rounded up
+    int nst = (smem_optin - tb_bytes - bar_bytes) / TC_STAGE;
     if (nst > TC_MAX_STAGES) nst = TC_MAX_STAGES;
+    // a dequant warpgroup waits only for its own units' stages: with nst a
+    // multiple of the warpgroups the previous load of a stage it waits on
+    // was its own, so its parity wait cannot alias a phase
+    nst -= nst % TC_NDQ;
     if (nst < 2) return SV_ERR_SHAPE;
     p.nst = nst;
     p.stage_bytes = TC_STAGE;
     p.xslot_bytes = TC_X_BYTES;
     int off = nst * TC_STAGE;
     p.off_sbuf = off;
-    off += ring_bytes;
-    p.off_bk = off;
-    off += kt_bytes;
+    p.off_bk = off;                          // finished-tile buffers
+    off += tb_bytes;
     p.off_bars = off;
-    off += (2 * nst + 2 * TC_NA + 2 * TC_NACC + 2) * 8 + 16;
+    off += (2 * nst + 2 * TC_NDQ * TC_NSLOT + 2 * TC_NB + 4 + 2) * 8 + 32;
     *smem_total = off;
     return off <= smem_optin ? SV_OK : SV_ERR_SHAPE;
 }
@@ -470,14 +475,10 @@ int launch_tc(Params p, const DeviceState &st, cudaStream_t stream)
     int smem = 0;
     int rc = plan_layout_tc<HEAD>(p, st.smem_optin, &smem);
     if (rc != SV_OK) return rc;
-    CUtensorMap tmW, tmS;
+    CUtensorMap tmW;
     std::memset(&tmW, 0, sizeof tmW);
-    std::memset(&tmS, 0, sizeof tmS);
     rc = encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, p.Wq, static_cast<unsigned long long>(p.K / 8),
                    static_cast<unsigned long long>(p.n_rows), 16, TC_RT, CU_TENSOR_MAP_SWIZZLE_64B);
-    if (rc != SV_OK) return rc;
-    rc = encode_2d(&tmS, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, p.scales, static_cast<unsigned long long>(p.G),
-                   static_cast<unsigned long long>(p.n_rows), 8, TC_RT);
     if (rc != SV_OK) return rc;
     const long long tiles = (static_cast<long long>(p.n_rows) + TC_RT - 1) / TC_RT;
     p.U = tiles * (p.G / TC_GU);             // a unit is TC_GU groups of one tile
@@ -509,7 +510,7 @@ int launch_tc(Params p, const DeviceState &st, cudaStream_t stream)
     cfg.gridDim = dim3(static_cast<unsigned>(B));
     cfg.blockDim = dim3(TC_WARPS * 32);
     cfg.dynamicSmemBytes = static_cast<size_t>(smem);
-    if (cudaLaunchKernelEx(&cfg, w4a16_tc_kernel<HEAD>, p, tmW, tmS) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, w4a16_tc_kernel<HEAD>, p, tmW) != cudaSuccess) {
         cudaGetLastError();
         return SV_ERR_CUDA;
     }
@@ -517,10 +518,8 @@ int launch_tc(Params p, const DeviceState &st, cudaStream_t stream)
 }
 
 // The tcgen05 kernel serves four token tiles (17 <= T <= 32) of contiguous
-// rows whose scale rows are 16-byte multiples (G % 8 == 0), when the device
-// state has its partial-sum area.  Measured against the mma.sync kernel at
-// T = 32 (back to back): lm_head 250 us against 267, gate+up GEMM 38.6
-// against 51.7, down 32.6 against 39.2, QKV 25.2 against 25.9.
+// rows whose scale rows are 16-byte multiples and split into boxes of eight
+// groups (G % 8 == 0), when the device state has its partial-sum area.
 // sv_debug_set_tcgen05(0) selects the mma.sync kernel for comparison.
 template <bool HEAD, bool GATHER>
 bool use_tc(const Params &p, const DeviceState &st)

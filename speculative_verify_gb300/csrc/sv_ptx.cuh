@@ -227,6 +227,13 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr)
     return v;
 }
 
+__device__ __forceinline__ float lds_f32(uint32_t addr)
+{
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+    return v;
+}
+
 __device__ __forceinline__ uint32_t lds_u16(uint32_t addr)
 {
     uint16_t v;
@@ -488,6 +495,68 @@ __device__ __forceinline__ void tc_commit(uint32_t bar)
                  : "memory");
 }
 
+// Whole-warp forms: every lane of the warp calls them with the same
+// (warp-uniform) operands and one elected lane issues.  Issued this way an
+// M128 x N32 x K16 MMA costs the warp about 20 cycles against about 47 when
+// one lane issues inside a lane branch.
+__device__ __forceinline__ void tc_mma_f16_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                   uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "elect.sync _|e, 0xffffffff;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+                 ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
+// Eight MMAs of one 128-column group (K = 8 x 16) from one elected lane of
+// the calling warp: A at a + 8k (tensor-memory columns), B at descriptor
+// b + 64k (1024 bytes further along K each); the first adds to D only when
+// `accumulate` is set, the others always add.
+__device__ __forceinline__ void tc_mma8_f16_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                                    uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred e, p, t;\n\t"
+                 "elect.sync _|e, 0xffffffff;\n\t"
+                 "setp.ne.b32 p, %18, 0;\n\t"
+                 "setp.eq.b32 t, %18, %18;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %9, %17, p;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %10, %17, t;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %11, %17, t;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %12, %17, t;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %13, %17, t;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%6], %14, %17, t;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %15, %17, t;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%8], %16, %17, t;\n\t}"
+                 ::"r"(d_tmem), "r"(a_tmem), "r"(a_tmem + 8u), "r"(a_tmem + 16u), "r"(a_tmem + 24u),
+                   "r"(a_tmem + 32u), "r"(a_tmem + 40u), "r"(a_tmem + 48u), "r"(a_tmem + 56u),
+                   "l"(b_desc), "l"(b_desc + 64u), "l"(b_desc + 128u), "l"(b_desc + 192u),
+                   "l"(b_desc + 256u), "l"(b_desc + 320u), "l"(b_desc + 384u), "l"(b_desc + 448u),
+                   "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
+// Two commits (and optionally a third when bar3 != 0) from one elected lane.
+__device__ __forceinline__ void tc_commit23_warp(uint32_t bar1, uint32_t bar2, uint32_t bar3)
+{
+    asm volatile("{\n\t.reg .pred e, c;\n\t"
+                 "elect.sync _|e, 0xffffffff;\n\t"
+                 "setp.ne.and.b32 c, %2, 0, e;\n\t"
+                 "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t"
+                 "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%1];\n\t"
+                 "@c tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%2];\n\t}"
+                 ::"r"(bar1), "r"(bar2), "r"(bar3)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_commit_warp(uint32_t bar)
+{
+    asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+                 "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
+                 ::"r"(bar)
+                 : "memory");
+}
+
 // ---------------------------------------------------------------- argmax keys
 
 // 64-bit key that orders (value, token id) by value, then by LOWER id:
@@ -501,6 +570,17 @@ __device__ __forceinline__ unsigned long long make_key(float v, uint32_t id)
     if (v != v) o = 0u;
     return (static_cast<unsigned long long>(o) << 32) |
            static_cast<unsigned long long>(0xFFFFFFFFu - id);
+}
+
+// The largest key among the warp's 32 lanes (all lanes get it): the largest
+// high word, then the largest low word among the lanes holding it -- the
+// 64-bit maximum, in two single-instruction warp reductions.
+__device__ __forceinline__ unsigned long long warp_max_key(unsigned long long k)
+{
+    const uint32_t hi = static_cast<uint32_t>(k >> 32), lo = static_cast<uint32_t>(k);
+    const uint32_t bh = __reduce_max_sync(0xFFFFFFFFu, hi);
+    const uint32_t bl = __reduce_max_sync(0xFFFFFFFFu, hi == bh ? lo : 0u);
+    return (static_cast<unsigned long long>(bh) << 32) | bl;
 }
 
 __device__ __forceinline__ float key_value(unsigned long long k)

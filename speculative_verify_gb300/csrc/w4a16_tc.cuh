@@ -8,37 +8,52 @@
 // tcgen05.mma of M = 128 weight rows x N = 32 tokens x K = 16 does the work
 // of 32 of them.
 //
+// Scales in the A operand.  Each weight row's group scales are taken eight
+// groups (a "box") at a time.  With E the largest exponent among the row's
+// eight scales, the dequant warps write level * s * 2^(137 - E) to the A
+// operand in fp16: the box's largest scale lands in [2^10, 2^11), the level
+// (an integer in -8..7) times the 8-bit significand of a bf16 scale has at
+// most 11 significant bits, so the product is exact in fp16 for every scale
+// within 2^28 of the box's largest (smaller ones round at 2^-24 of it, below
+// the fp32 rounding of the sum).  The tensor cores then add the products of
+// all eight groups in fp32, and the epilogue multiplies the box's sums by
+// 2^(E - 137): exactly the sum of the products level * s * x, which the
+// per-group form adds in another order.  The product is formed in one fp16
+// fma on the nibble placed in the top four mantissa bits of 16.0
+// ((16 + n) * s' - 24 s' = (n - 8) * s', with 24 s' exact in fp16).
+//
 // Work: a unit is one 128-row tile x two 128-column groups (TC_GU); units
 // are numbered tile-major and split evenly over the grid (stream-K), split
-// tiles finished in CTA order as in the other kernels.
+// tiles finished in CTA order as in the other kernels.  A box is four units
+// (fewer at the start of a CTA's share); boxes never straddle tiles (the
+// kernel needs K a multiple of 1024).
 //
 // Warp roles (15 warps):
 //  * warp 0, producer (lane 0): per unit, the two groups' packed weights of
-//    the tile's 128 rows (TMA boxes, 64-byte swizzle), the groups'
-//    activations in the canonical K-major layout written by
-//    xprep_kernel<true> (one bulk copy, 16 KB) and, every eight groups, the
-//    rows' scales for those groups (a TMA box of 8 x 128 bf16) into a
-//    four-slot ring; completion on the stage's mbarrier.  Weights and scales
-//    of the first stages go out before griddepcontrol.wait.
-//  * warp 1 allocates the CTA's tensor memory (all 512 columns: three
-//    128-column A buffers and two 64-column accumulator pairs) and frees it
-//    at the end.  Lane 0 of warps 1 and 14 issue the MMAs of the even and the
-//    odd units: per group eight tcgen05.mma (A from tensor memory, B = the
-//    stage's activation block, D = the group's own accumulator, cleared by
-//    the first), then one set of commits per unit to the A buffer's, the
-//    stage's and the accumulator pair's mbarriers.  (One hand-off costs about
-//    as much as the eight MMAs of a group; two groups per unit and two
-//    issuers that alternate hide part of it.)
-//  * warps 2..9, dequant (two warpgroups taking units in turn):
-//    thread = weight row; per group it reads its row's 16 words, turns the
-//    128 nibbles into fp16 levels (pairs (j, j+4), the order the activation
-//    chunks use) and stores them to its tensor-memory lane as the A operand.
-//  * warps 10..13, epilogue: thread = row; per unit it reads the row's 32
-//    fp32 sums of each group back from tensor memory, multiplies them by the
-//    row's group scale and adds them to its fp32 accumulators (the scale
-//    applied after each group's sum, as in the other kernels); at the end of
-//    its share of a tile it writes y or folds the logits into per-token
-//    argmax keys.
+//    the tile's 128 rows (TMA boxes, 64-byte swizzle) and their activations
+//    in the canonical K-major layout written by xprep_kernel<true> (one bulk
+//    copy, 16 KB), completion on the stage's mbarrier.  Weights of the first
+//    stages go out before griddepcontrol.wait.
+//  * warp 1 allocates the CTA's tensor memory (512 columns: three 128-column
+//    A buffers, two pairs of 32-column box accumulators) and frees it at
+//    the end.  Warps 1 and 14 issue the MMAs of the unit's first and second
+//    group, every unit in order, each into its own accumulator of the box's
+//    pair: the whole warp runs the loop and an elected lane issues eight
+//    tcgen05.mma (A from tensor memory, B = the stage's activation block;
+//    the box's first clears the accumulator), then commits per unit to the
+//    A buffer's and the stage's mbarriers and per box to the pair's.  (Every
+//    waiter walks its barriers' phases in order, so no parity wait can
+//    alias a phase two ahead.)
+//  * warps 2..9, dequant (two warpgroups taking units in turn): thread =
+//    weight row; per box it loads the row's eight scales (16 bytes, read
+//    ahead) and forms the fp16 factors, per group it reads its row's 16
+//    words and stores the 128 scaled levels (pairs (j, j+4), the order the
+//    activation chunks use) to its tensor-memory lane as the A operand.
+//  * warps 10..13, epilogue: thread = row; per box it reads the row's two
+//    accumulators of 32 fp32 sums back from tensor memory, adds them,
+//    multiplies by 2^(E - 137) and
+//    adds them to its fp32 accumulators; at the end of its share of a tile
+//    it writes y or folds the logits into per-token argmax keys.
 #pragma once
 
 #include "w4a16_stream.cuh"
@@ -48,22 +63,25 @@ namespace sv {
 
 constexpr int TC_RT = 128;                       // rows per tile (the MMA's M)
 constexpr int TC_GU = 2;                         // 128-column groups per unit (one hand-off per TC_GU groups)
+constexpr int TC_BOX_UNITS = 8 / TC_GU;          // units per box of eight groups
 constexpr int TC_W_BYTES = TC_RT * 64;           // one group of a tile's packed weights
 constexpr int TC_X_BYTES = 32 * 128 * 2;         // one group of 32 tokens, fp16
 constexpr int TC_STAGE = TC_GU * (TC_W_BYTES + TC_X_BYTES);   // weights of the unit's groups, then their activations
-constexpr int TC_RING = 4;                       // scale-ring slots
-constexpr int TC_RING_SLOT = TC_RT * 16;         // 8 groups of bf16 scales per row
 constexpr int TC_NDQ = 2;                        // dequant warpgroups, taking units in turn
-constexpr int TC_NA = 3;                         // A buffers of TC_GU x 64 columns
-constexpr int TC_NACC = 2;                       // accumulators of TC_GU x 32 columns
+constexpr int TC_NSLOT = 3;                      // A slots of one group (64 columns) per pipeline
+constexpr int TC_NB = 2;                         // box accumulator sets (one 32-column accumulator per pipeline)
 constexpr uint32_t TC_TMEM_COLS = 512;
-constexpr uint32_t TC_ACC_COL = TC_NA * 64 * TC_GU;   // the accumulators after the A buffers
+constexpr uint32_t TC_ACC_COL = TC_NDQ * TC_NSLOT * 64;   // the accumulators after the A slots
 constexpr int TC_DQ0 = 2;                        // first dequant warp
 constexpr int TC_EP0 = TC_DQ0 + 4 * TC_NDQ;      // first epilogue warp
 constexpr int TC_MMA2 = TC_EP0 + 4;              // second MMA-issuing warp
-constexpr int TC_WARPS = TC_MMA2 + 1;
-constexpr int TC_MAX_STAGES = 12;                // the ring's reuse rule holds up to 13
-static_assert(TC_ACC_COL + TC_NACC * 32 * TC_GU <= TC_TMEM_COLS, "tensor memory budget");
+constexpr int TC_RED = TC_MMA2 + 1;              // head: the warp that reduces finished tiles to per-token maxima
+constexpr int TC_WARPS = TC_RED + 1;
+constexpr int TC_TB_BYTES = TC_RT * 32 * 4;      // head: one finished tile's logits, [row][32 tokens] fp32
+constexpr int TC_MAX_STAGES = 8;
+constexpr int TC_SHIFT = 137;                    // a box's largest scale x 2^(TC_SHIFT - E) is in [2^10, 2^11)
+static_assert(TC_ACC_COL + TC_NB * TC_NDQ * 32 <= TC_TMEM_COLS, "tensor memory budget");
+static_assert(TC_NDQ == 2, "two pipelines: dequant warpgroup w with MMA warp w");
 // Instruction descriptor of kind::f16: D fp32 (bits 4-5 = 1), A and B fp16
 // (bits 7-9, 10-12 = 0), both K-major (bits 15, 16 = 0), N >> 3 at bits
 // 17-22, M >> 4 at bits 24-28.
@@ -79,27 +97,84 @@ __device__ __forceinline__ uint64_t tc_bdesc(uint32_t saddr)
            (static_cast<uint64_t>(128 >> 4) << 32) | (1ull << 46);
 }
 
+// Largest biased exponent among eight bf16 scales (two per word).
+__device__ __forceinline__ int tc_box_exp(const uint4 &s)
+{
+    const uint32_t w[4] = {s.x, s.y, s.z, s.w};
+    uint32_t e = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) e = max(e, max((w[k] >> 7) & 0xFFu, (w[k] >> 23) & 0xFFu));
+    return static_cast<int>(e);
+}
+
+// 2^k for -252 <= k <= 254 as a pair of normal fp32 factors.
+__device__ __forceinline__ void tc_pow2_pair(int k, float &f1, float &f2)
+{
+    const int a = k / 2, c = k - a;
+    f1 = __uint_as_float(static_cast<uint32_t>(a + 127) << 23);
+    f2 = __uint_as_float(static_cast<uint32_t>(c + 127) << 23);
+}
+
+// The fp16x2 factor {s', s'} and addend {-24 s', -24 s'} of one bf16 scale,
+// s' = s * f1 * f2 rounded to fp16 (exact when within the fp16 range).
+__device__ __forceinline__ void tc_factor(uint32_t s_bits, float f1, float f2, uint32_t &s2, uint32_t &c2)
+{
+    const float sp = (__uint_as_float(s_bits << 16) * f1) * f2;
+    const __half h = __float2half_rn(sp);
+    const __half c = __float2half_rn(-24.0f * __half2float(h));
+    const uint32_t hb = __half_as_ushort(h), cb = __half_as_ushort(c);
+    s2 = hb | (hb << 16);
+    c2 = cb | (cb << 16);
+}
+
+// Levels of nibbles (j, j+4) times the row's factor: `ws` is the word shifted
+// so that the two nibbles sit at bits 6..9 and 22..25 (the top mantissa bits
+// of fp16 16.0), then (16 + n) * s' - 24 s' = (n - 8) * s' in one fp16 fma.
+__device__ __forceinline__ uint32_t tc_scaled_pair(uint32_t ws, uint32_t s2, uint32_t c2)
+{
+    uint32_t q, r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(q) : "r"(ws), "r"(0x03C003C0u), "r"(0x4C004C00u));
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(q), "r"(s2), "r"(c2));
+    return r;
+}
+
+// The row's eight scales of box `bx` (groups 8 bx .. 8 bx + 7) of tile `tile`.
+__device__ __forceinline__ uint4 tc_load_scales(const Params &p, int tile, int bx, int row)
+{
+    const long long rg = static_cast<long long>(tile) * TC_RT + row;
+    if (rg >= p.n_rows) return make_uint4(0u, 0u, 0u, 0u);
+    return __ldg(reinterpret_cast<const uint4 *>(p.scales + rg * p.G + 8 * bx));
+}
+
+// A bounded wait that first polls once without reading the CTA's flag (the
+// MMA warps' common case: the barrier has completed already).
+__device__ __forceinline__ void tc_wait(const Params &p, volatile int *flag, uint32_t bar, uint32_t parity)
+{
+    if (!mbar_try_wait(bar, parity)) wait_or_flag(p, flag, bar, parity);
+}
+
 template <bool HEAD>
 __global__ void __launch_bounds__(TC_WARPS * 32, 1)
-w4a16_tc_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tmW,
-                const __grid_constant__ CUtensorMap tmS)
+w4a16_tc_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tmW)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int nst = p.nst;
-    uint8_t *ring = smem + p.off_sbuf;                                       // [TC_RING][128][8] bf16
-    unsigned long long *kt = reinterpret_cast<unsigned long long *>(smem + p.off_bk);   // [4][TMAX]
+    uint8_t *tbuf = smem + p.off_bk;        // head: [2] finished tiles, TC_TB_BYTES each
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + p.off_bars);
-    uint64_t *full = bars;                   // [nst]   producer -> dequant, MMA, epilogue
-    uint64_t *empty = bars + nst;            // [nst]   dequant (4) + MMA commit (1) + epilogue (4) -> producer
-    uint64_t *a_full = bars + 2 * nst;       // [NA]    dequant warpgroup (4) -> MMA
-    uint64_t *a_empty = a_full + TC_NA;      // [NA]    MMA commit -> dequant
-    uint64_t *d_full = a_empty + TC_NA;      // [NACC]  MMA commit -> epilogue
-    uint64_t *d_empty = d_full + TC_NACC;    // [NACC]  epilogue (4) -> MMA
-    uint64_t *mma_done = d_empty + TC_NACC;  //         MMA commit after the last unit
+    uint64_t *full = bars;                   // [nst]   producer -> the unit's dequant warpgroup and MMA warp
+    uint64_t *empty = full + nst;            // [nst]   the unit's MMA commit -> producer
+    uint64_t *a_full = empty + nst;          // [NDQ][NSLOT] dequant warpgroup w (4) -> MMA warp w
+    uint64_t *a_empty = a_full + TC_NDQ * TC_NSLOT;   // [NDQ][NSLOT] MMA warp w's commit -> warpgroup w
+    uint64_t *d_full = a_empty + TC_NDQ * TC_NSLOT;   // [NB]    MMA commits (2) at the end of a box -> epilogue
+    uint64_t *d_empty = d_full + TC_NB;      // [NB]    epilogue (4) -> MMA
+    uint64_t *tb_full = d_empty + TC_NB;     // [2]     head: epilogue (4) -> reducer
+    uint64_t *tb_empty = tb_full + 2;        // [2]     head: reducer -> epilogue
+    uint64_t *mma_done = tb_empty + 2;       //         MMA commits after the last unit
     uint64_t *stall_bar = mma_done + 1;      //         never completed (test hook)
     volatile int *flag = reinterpret_cast<volatile int *>(stall_bar + 1);   // a wait timed out
     volatile int *decision = flag + 1;       // split-tile protocol
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(flag + 2);
+    volatile int *tb_tile = flag + 3;        // [2] head: the tile in each buffer, -1 = no more
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int B = gridDim.x, b = blockIdx.x;
@@ -120,23 +195,25 @@ w4a16_tc_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
     if (threadIdx.x == 0) {
         for (int s = 0; s < nst; ++s) {
             mbar_init(smem_addr(&full[s]), 1);
-            mbar_init(smem_addr(&empty[s]), 9);
+            mbar_init(smem_addr(&empty[s]), 1);
         }
-        for (int i = 0; i < TC_NA; ++i) {
+        for (int i = 0; i < TC_NDQ * TC_NSLOT; ++i) {
             mbar_init(smem_addr(&a_full[i]), 4);
             mbar_init(smem_addr(&a_empty[i]), 1);
         }
-        for (int i = 0; i < TC_NACC; ++i) {
-            mbar_init(smem_addr(&d_full[i]), 1);
+        for (int i = 0; i < TC_NB; ++i) {
+            mbar_init(smem_addr(&d_full[i]), 2);
             mbar_init(smem_addr(&d_empty[i]), 4);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_addr(&tb_full[i]), 4);
+            mbar_init(smem_addr(&tb_empty[i]), 1);
         }
         mbar_init(smem_addr(mma_done), 2);
         mbar_init(smem_addr(stall_bar), 1);
         *flag = 0;
         fence_barrier_init();
     }
-    if (HEAD)
-        for (int i = threadIdx.x; i < 4 * TMAX; i += blockDim.x) kt[i] = 0ull;
     if (warp == 1) {
         tmem_alloc(smem_addr(const_cast<uint32_t *>(tmem_slot)), TC_TMEM_COLS);
         tmem_relinquish();
@@ -153,25 +230,19 @@ w4a16_tc_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
             const uint64_t pol_w = policy_evict_first();
             const uint64_t pol_x = policy_evict_last();
             prefetch_tmap(&tmW);
-            prefetch_tmap(&tmS);
             const uint32_t s0 = smem_addr(smem);
             const int n_pre = min(nst, n_units);
-            int tile = tile_first, grp = grp_first, box = -1;
+            int tile = tile_first, grp = grp_first;
             for (int i = 0; i < n_units; ++i) {
                 const int s = i % nst;
                 if (i >= nst) wait_or_flag(p, flag, smem_addr(&empty[s]), static_cast<uint32_t>(((i / nst) & 1) ^ 1));
                 const uint32_t fb = smem_addr(&full[s]);
                 const uint32_t stage = s0 + static_cast<uint32_t>(s * TC_STAGE);
                 const int g0 = grp * TC_GU;              // the unit's first group
-                const bool nb = wide_new_box(i == 0, g0);
-                if (nb) ++box;
-                mbar_arrive_expect_tx(fb, static_cast<uint32_t>(TC_STAGE + (nb ? TC_RING_SLOT : 0)));
+                mbar_arrive_expect_tx(fb, static_cast<uint32_t>(TC_STAGE));
 #pragma unroll
                 for (int g = 0; g < TC_GU; ++g)
                     tma_load_2d(stage + g * TC_W_BYTES, &tmW, (g0 + g) * 16, tile * TC_RT, fb, pol_w);
-                if (nb)
-                    tma_load_2d(smem_addr(ring) + static_cast<uint32_t>((box % TC_RING) * TC_RING_SLOT), &tmS, g0 & ~7,
-                                tile * TC_RT, fb, pol_w);
                 if (i >= n_pre)
                     bulk_g2s(stage + TC_GU * TC_W_BYTES, p.x16 + static_cast<size_t>(g0) * TC_X_BYTES,
                              TC_GU * TC_X_BYTES, fb, pol_x);
@@ -197,78 +268,129 @@ w4a16_tc_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
         }
     } else if (warp == 1 || warp == TC_MMA2) {
         // ============================================================ MMA issue
-        // two issuing warps take alternate units (and the accumulator of
-        // that parity), so that one's barrier waits overlap the other's issue
-        if (lane == 0) {
-            const uint32_t s0 = smem_addr(smem);
-            for (int i = (warp == 1 ? 0 : 1); i < n_units; i += 2) {
-                const int s = i % nst, ab = i % TC_NA, db = i % TC_NACC;
-                wait_or_flag(p, flag, smem_addr(&full[s]), static_cast<uint32_t>((i / nst) & 1));
-                wait_or_flag(p, flag, smem_addr(&a_full[ab]), static_cast<uint32_t>((i / TC_NA) & 1));
-                if (i >= TC_NACC)
-                    wait_or_flag(p, flag, smem_addr(&d_empty[db]), static_cast<uint32_t>(((i / TC_NACC) & 1) ^ 1));
-                tc_fence_after_sync();
+        // Two pipelines: units i with i % 2 == w go to dequant warpgroup w
+        // and MMA warp w, through the pipeline's own ring of TC_NSLOT group
+        // slots, into the pipeline's accumulator of the box's set (its first
+        // MMA of a box clears it).  Every waiter walks its barriers' phases
+        // in order.  The whole warp runs the loop with warp-uniform operands
+        // and one elected lane issues.
+        const int w = warp == 1 ? 0 : 1;
+        const uint32_t s0 = smem_addr(smem);
+        const uint32_t slot_col = static_cast<uint32_t>(w * TC_NSLOT) * 64u;
+        uint64_t *my_full = a_full + w * TC_NSLOT, *my_empty = a_empty + w * TC_NSLOT;
+        int grp4 = grp_first % TC_BOX_UNITS, left = G - grp_first, nb = -1;
+        int s = 0, slot = 0;
+        uint32_t sph = 0u, slph = 0u;                 // phase parities of stage s, of the slot ring's lap
+        bool first_in_box = true;
+        for (int i = 0; i < n_units; ++i) {
+            const bool box_start = i == 0 || grp4 == 0;
+            const bool box_end = i == n_units - 1 || grp4 == TC_BOX_UNITS - 1;
+            if (box_start) {
+                ++nb;
+                first_in_box = true;
+                if (nb >= TC_NB)            // the set's previous box has been read out
+                    tc_wait(p, flag, smem_addr(&d_empty[nb & 1]), static_cast<uint32_t>(((nb >> 1) - 1) & 1));
+            }
+            if (--left == 0) { left = G; grp4 = 0; } else grp4 = (grp4 + 1) & (TC_BOX_UNITS - 1);
+            if ((i & 1) == w) {
+                tc_wait(p, flag, smem_addr(&full[s]), sph);
+                const uint32_t d = tmem + TC_ACC_COL + 32u * static_cast<uint32_t>(TC_NDQ * (nb & 1) + w);
+                const uint32_t xs0 = s0 + static_cast<uint32_t>(s * TC_STAGE + TC_GU * TC_W_BYTES);
 #pragma unroll
                 for (int g = 0; g < TC_GU; ++g) {
-                    // group g of the unit: its own accumulator (each group's sum is scaled on its own)
-                    const uint32_t d = tmem + TC_ACC_COL + 32u * (TC_GU * db + g);
-                    const uint32_t a = tmem + 64u * (TC_GU * ab + g);
-                    const uint32_t xs = s0 + static_cast<uint32_t>(s * TC_STAGE + TC_GU * TC_W_BYTES + g * TC_X_BYTES);
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) tc_mma_f16_ts(d, a + 8u * k, tc_bdesc(xs + 1024u * k), TC_IDESC, k > 0);
+                    tc_wait(p, flag, smem_addr(&my_full[slot]), slph);
+                    __syncwarp();               // converged for elect.sync
+                    tc_fence_after_sync();
+                    tc_mma8_f16_ts_warp(d, tmem + slot_col + 64u * static_cast<uint32_t>(slot),
+                                        tc_bdesc(xs0 + static_cast<uint32_t>(g * TC_X_BYTES)), TC_IDESC,
+                                        (first_in_box && g == 0) ? 0u : 1u);
+                    tc_commit_warp(smem_addr(&my_empty[slot]));
+                    if (++slot == TC_NSLOT) { slot = 0; slph ^= 1u; }
                 }
-                tc_commit(smem_addr(&a_empty[ab]));
-                tc_commit(smem_addr(&empty[s]));
-                tc_commit(smem_addr(&d_full[db]));
+                tc_commit_warp(smem_addr(&empty[s]));
+                first_in_box = false;
             }
-            tc_commit(smem_addr(mma_done));
+            if (box_end) tc_commit_warp(smem_addr(&d_full[nb & 1]));
+            if (++s == nst) { s = 0; sph ^= 1u; }
         }
         __syncwarp();
+        tc_commit_warp(smem_addr(mma_done));
     } else if (warp < TC_EP0) {
         // ============================================================ dequant
-        // warpgroup wg takes units i with i % TC_NDQ == wg; thread = tile row
-        const int wg = (warp - TC_DQ0) >> 2;
+        // warpgroup w takes units i with i % 2 == w; thread = tile row; each
+        // group goes to the next slot of the pipeline's ring
+        const int w = (warp - TC_DQ0) >> 2;
         const int q = warp & 3;                       // tensor-memory lane quarter
         const int row = 32 * q + lane;
         const uint32_t s0 = smem_addr(smem);
         const uint32_t sw = static_cast<uint32_t>((row >> 1) & 3);   // the box's 64-byte swizzle
-        for (int i = wg; i < n_units; i += TC_NDQ) {
-            const int s = i % nst, ab = i % TC_NA;
-            wait_or_flag(p, flag, smem_addr(&full[s]), static_cast<uint32_t>((i / nst) & 1));
-            if (i >= TC_NA) wait_or_flag(p, flag, smem_addr(&a_empty[ab]), static_cast<uint32_t>(((i / TC_NA) & 1) ^ 1));
-            const uint32_t wrow0 = s0 + static_cast<uint32_t>(s * TC_STAGE + row * 64);
-            const uint32_t tlane0 = tmem + (static_cast<uint32_t>(32 * q) << 16) + 64u * TC_GU * ab;
-#pragma unroll
-            for (int hf = 0; hf < 2 * TC_GU; ++hf) {  // per group: words 0..7, then 8..15, 32 columns each
-                const uint32_t wrow = wrow0 + static_cast<uint32_t>((hf >> 1) * TC_W_BYTES);
-                const uint32_t tlane = tlane0 + 64u * (hf >> 1);
-                uint32_t v[32];
-#pragma unroll
-                for (int jj = 0; jj < 2; ++jj) {
-                    const int j = 2 * (hf & 1) + jj;
-                    const uint4 w4 = lds128(wrow + ((static_cast<uint32_t>(j) ^ sw) << 4));
-                    const uint32_t ws[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const uint32_t w = ws[e];
-                        const int c0 = 4 * (4 * jj + e);
-                        v[c0 + 0] = dequant2_f16_lo(w);           // nibbles (0, 4)
-                        v[c0 + 1] = dequant2_f16_hi(w);           // (1, 5)
-                        v[c0 + 2] = dequant2_f16_lo(w >> 8);      // (2, 6)
-                        v[c0 + 3] = dequant2_f16_hi(w >> 8);      // (3, 7)
-                    }
+        const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(w * TC_NSLOT) * 64u;
+        uint64_t *my_full = a_full + w * TC_NSLOT, *my_empty = a_empty + w * TC_NSLOT;
+        int tile = tile_first, grp = grp_first;
+        int key = -1, key_next = -1;                  // box (tile * boxes + bx) of `cur`, of `nxt`
+        uint4 cur = make_uint4(0u, 0u, 0u, 0u), nxt = cur;
+        float f1 = 0.f, f2 = 0.f;
+        const int nbox = G / TC_BOX_UNITS;            // boxes per tile
+        int s = 0, slot = 0;
+        uint32_t sph = 0u, slph = 0u;
+        bool lap0 = true;                             // the ring's first lap: no slot has been used
+        for (int i = 0; i < n_units; ++i) {
+            const int t_i = tile, j = grp;
+            if (++grp == G) { grp = 0; ++tile; }
+            if ((i & 1) == w) {
+                const int bx = j / TC_BOX_UNITS, k = t_i * nbox + bx;
+                if (k != key) {
+                    // this box's scales (read ahead when possible), then the next box's
+                    cur = (k == key_next) ? nxt : tc_load_scales(p, t_i, bx, row);
+                    key = k;
+                    const int nbx = bx + 1 < nbox ? bx + 1 : 0, ntile = bx + 1 < nbox ? t_i : t_i + 1;
+                    key_next = ntile * nbox + nbx;
+                    if (static_cast<long long>(ntile) * TC_RT < p.n_rows) nxt = tc_load_scales(p, ntile, nbx, row);
+                    tc_pow2_pair(TC_SHIFT - tc_box_exp(cur), f1, f2);
                 }
-                tmem_st32(tlane + 32u * (hf & 1), v);
+                // the unit's two groups are word j % 4 of the box's scales
+                const uint32_t jw = static_cast<uint32_t>(j % TC_BOX_UNITS);
+                const uint32_t sp = jw == 0 ? cur.x : jw == 1 ? cur.y : jw == 2 ? cur.z : cur.w;
+                wait_or_flag(p, flag, smem_addr(&full[s]), sph);
+                const uint32_t wrow0 = s0 + static_cast<uint32_t>(s * TC_STAGE + row * 64);
+#pragma unroll
+                for (int g = 0; g < TC_GU; ++g) {
+                    uint32_t s2, c2;
+                    tc_factor(g == 0 ? (sp & 0xFFFFu) : (sp >> 16), f1, f2, s2, c2);
+                    if (!lap0)                          // the slot's previous group has been multiplied
+                        wait_or_flag(p, flag, smem_addr(&my_empty[slot]), slph ^ 1u);
+                    const uint32_t wrow = wrow0 + static_cast<uint32_t>(g * TC_W_BYTES);
+                    const uint32_t tlane = tl + 64u * static_cast<uint32_t>(slot);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {         // words 0..7, then 8..15: 32 columns each
+                        uint32_t v[32];
+#pragma unroll
+                        for (int jj = 0; jj < 2; ++jj) {
+                            const int jc = 2 * h + jj;
+                            const uint4 w4 = lds128(wrow + ((static_cast<uint32_t>(jc) ^ sw) << 4));
+                            const uint32_t ws[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const uint32_t wd = ws[e];
+                                const int c0 = 4 * (4 * jj + e);
+                                v[c0 + 0] = tc_scaled_pair(wd << 6, s2, c2);   // nibbles (0, 4)
+                                v[c0 + 1] = tc_scaled_pair(wd << 2, s2, c2);   // (1, 5)
+                                v[c0 + 2] = tc_scaled_pair(wd >> 2, s2, c2);   // (2, 6)
+                                v[c0 + 3] = tc_scaled_pair(wd >> 6, s2, c2);   // (3, 7)
+                            }
+                        }
+                        tmem_st32(tlane + 32u * h, v);
+                    }
+                    tmem_wait_st();
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_addr(&my_full[slot]));
+                    if (++slot == TC_NSLOT) { slot = 0; slph ^= 1u; lap0 = false; }
+                }
             }
-            tmem_wait_st();
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(smem_addr(&a_full[ab]));
-                mbar_arrive(smem_addr(&empty[s]));
-            }
+            if (++s == nst) { s = 0; sph ^= 1u; }
         }
-    } else {
+    } else if (warp < TC_RED) {
         // ============================================================ epilogue
         const int q = warp & 3;
         const int ew = warp - TC_EP0;                 // epilogue warp 0..3
@@ -291,38 +413,49 @@ w4a16_tc_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
             if (tile_last != tile_first && u1 < tz + G) ncZ = cta_of(tz + G - 1, U, B) - b + 1;
         }
         const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + TC_ACC_COL;
+        const int nbox = G / TC_BOX_UNITS;
+        int ntb = 0;                                  // head: tiles handed to the reducer
         float acc[32];
 #pragma unroll
         for (int t = 0; t < 32; ++t) acc[t] = 0.f;
-        int tile = tile_first, grp = grp_first, box = -1;
+        int tile = tile_first, grp = grp_first, nb = -1, i_start = 0;
+        uint4 nxt = tc_load_scales(p, tile_first, grp_first / TC_BOX_UNITS, row);
         for (int i = 0; i < n_units; ++i) {
-            const int s = i % nst, db = i % TC_NACC;
-            if (wide_new_box(i == 0, grp * TC_GU)) ++box;
-            wait_or_flag(p, flag, smem_addr(&full[s]), static_cast<uint32_t>((i / nst) & 1));
-            wait_or_flag(p, flag, smem_addr(&d_full[db]), static_cast<uint32_t>((i / TC_NACC) & 1));
-            tc_fence_after_sync();
-#pragma unroll
-            for (int g = 0; g < TC_GU; ++g) {
-                uint32_t v[32];
-                tmem_ld32(taddr + 32u * (TC_GU * db + g), v);
-                tmem_wait_ld();
-                const float sc = bf16_bits_to_float(lds_u16(
-                    smem_addr(ring) +
-                    static_cast<uint32_t>((box % TC_RING) * TC_RING_SLOT + row * 16 + ((grp * TC_GU + g) & 7) * 2)));
-#pragma unroll
-                for (int t = 0; t < 32; ++t) acc[t] += sc * __uint_as_float(v[t]);
+            const bool box_start = i == 0 || (grp % TC_BOX_UNITS) == 0;
+            const bool box_end = i == n_units - 1 || (grp % TC_BOX_UNITS) == TC_BOX_UNITS - 1;
+            const bool tile_end = (grp == G - 1) || (i == n_units - 1);
+            const int bx = grp / TC_BOX_UNITS;
+            if (box_start) { ++nb; i_start = i; }
+            if (++grp == G) grp = 0;
+            if (!box_end) continue;
+
+            // ------------------------------------------- end of box nb
+            const uint4 cur = nxt;
+            {   // read the next box's scales ahead
+                const int nbx = bx + 1 < nbox ? bx + 1 : 0, ntile = bx + 1 < nbox ? tile : tile + 1;
+                if (i + 1 < n_units) nxt = tc_load_scales(p, ntile, nbx, row);
             }
+            float m1, m2;
+            tc_pow2_pair(tc_box_exp(cur) - TC_SHIFT, m1, m2);
+            const int par = nb & 1;
+            // a pipeline's accumulator holds this box only if the box has one of its units
+            const bool has0 = i > i_start || (i_start & 1) == 0, has1 = i > i_start || (i_start & 1) == 1;
+            wait_or_flag(p, flag, smem_addr(&d_full[par]), static_cast<uint32_t>((nb >> 1) & 1));
+            tc_fence_after_sync();
+            uint32_t v0[32], v1[32];        // the two pipelines' sums
+            tmem_ld32(taddr + 64u * static_cast<uint32_t>(par), v0);
+            tmem_ld32(taddr + 64u * static_cast<uint32_t>(par) + 32u, v1);
+            tmem_wait_ld();
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(smem_addr(&d_empty[db]));
-                mbar_arrive(smem_addr(&empty[s]));
+            if (lane == 0) mbar_arrive(smem_addr(&d_empty[par]));
+#pragma unroll
+            for (int t = 0; t < 32; ++t) {
+                const float e0 = has0 ? __uint_as_float(v0[t]) : 0.f, e1 = has1 ? __uint_as_float(v1[t]) : 0.f;
+                acc[t] += ((e0 + e1) * m1) * m2;
             }
 
-            const bool tile_end = (grp == G - 1) || (i == n_units - 1);
-            if (++grp == G) grp = 0;
             if (!tile_end) continue;
-
             // ------------------------------------------- end of this CTA's share of `tile`
 #pragma unroll
             for (int t = 0; t < 32; ++t) acc[t] *= __ldg(p.xinv + t);
@@ -353,15 +486,15 @@ w4a16_tc_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
                 named_bar_sync(1, NTHR_E);         // the decision word is read before it is reused
                 if (finish) {
                     __threadfence();
-                    for (int j = 0; j < nc; ++j) {
-                        const float *src = p.part + (static_cast<size_t>(bf + j) * 2 + (j == 0 ? slot_bf : 0)) *
+                    for (int jc = 0; jc < nc; ++jc) {
+                        const float *src = p.part + (static_cast<size_t>(bf + jc) * 2 + (jc == 0 ? slot_bf : 0)) *
                                                         WIDE_PART_FLOATS + row * TMAX;
                         float4 e4[8];
 #pragma unroll
                         for (int t = 0; t < 8; ++t) e4[t] = __ldcg(reinterpret_cast<const float4 *>(src) + t);
 #pragma unroll
                         for (int t = 0; t < 8; ++t) {
-                            if (j == 0) {
+                            if (jc == 0) {
                                 acc[4 * t] = e4[t].x; acc[4 * t + 1] = e4[t].y;
                                 acc[4 * t + 2] = e4[t].z; acc[4 * t + 3] = e4[t].w;
                             } else {
@@ -380,16 +513,20 @@ w4a16_tc_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
                         for (int t = 0; t < 32; ++t)
                             if (t < T) p.y[static_cast<size_t>(t) * p.n_rows + rg] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[t]));
                 } else {
+                    // hand the finished tile to the reducer warp (rows in
+                    // 16-byte chunks, chunk j of row r at j ^ (r & 7))
+                    const int tb = ntb & 1;
+                    if (ntb >= 2) wait_or_flag(p, flag, smem_addr(&tb_empty[tb]), static_cast<uint32_t>(((ntb >> 1) - 1) & 1));
+                    const uint32_t rb = smem_addr(tbuf + tb * TC_TB_BYTES + row * 128);
 #pragma unroll
-                    for (int t = 0; t < 32; ++t) {
-                        unsigned long long best = rg < p.n_rows ? make_key(acc[t], static_cast<uint32_t>(rg)) : 0ull;
-#pragma unroll
-                        for (int o = 16; o > 0; o >>= 1) {
-                            const unsigned long long k = shfl_xor_u64(best, o);
-                            best = k > best ? k : best;
-                        }
-                        if (lane == 0 && t < T && best > kt[ew * TMAX + t]) kt[ew * TMAX + t] = best;
-                    }
+                    for (int jc = 0; jc < 8; ++jc)
+                        sts128(rb + static_cast<uint32_t>((jc ^ (row & 7)) << 4),
+                               make_uint4(__float_as_uint(acc[4 * jc]), __float_as_uint(acc[4 * jc + 1]),
+                                          __float_as_uint(acc[4 * jc + 2]), __float_as_uint(acc[4 * jc + 3])));
+                    if (ew == 0 && lane == 0) tb_tile[tb] = tile;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_addr(&tb_full[tb]));
+                    ++ntb;
                 }
             }
 #pragma unroll
@@ -397,24 +534,43 @@ w4a16_tc_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
             ++tile;
         }
         if constexpr (HEAD) {
-            // ================================================ grid argmax + verify
-            named_bar_sync(1, NTHR_E);
-            if (ew == 0) {
-                unsigned long long best = 0ull;     // lane t: best key of token t in this CTA
-                if (lane < T)
-                    for (int w = 0; w < 4; ++w) {
-                        const unsigned long long k = kt[w * TMAX + lane];
-                        best = k > best ? k : best;
-                    }
-                head_grid_tail(p, best, lane, B);
-            }
+            // no more tiles: the sentinel
+            const int tb = ntb & 1;
+            if (ntb >= 2) wait_or_flag(p, flag, smem_addr(&tb_empty[tb]), static_cast<uint32_t>(((ntb >> 1) - 1) & 1));
+            if (ew == 0 && lane == 0) tb_tile[tb] = -1;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&tb_full[tb]));
         }
+    } else if (HEAD) {
+        // ============================================================ reducer (head)
+        // lane t keeps the largest key (logit, lowest id) of token t over
+        // every tile this CTA finishes; then the grid argmax and the verify
+        unsigned long long best = 0ull;
+        for (int k = 0;; ++k) {
+            const int tb = k & 1;
+            wait_or_flag(p, flag, smem_addr(&tb_full[tb]), static_cast<uint32_t>((k >> 1) & 1));
+            const int tile = tb_tile[tb];
+            if (tile < 0) break;
+            const long long r0 = static_cast<long long>(tile) * TC_RT;
+            const int nr = p.n_rows - r0 < TC_RT ? static_cast<int>(p.n_rows - r0) : TC_RT;
+            const uint32_t base = smem_addr(tbuf + tb * TC_TB_BYTES) + static_cast<uint32_t>((lane & 3) * 4);
+            const uint32_t jl = static_cast<uint32_t>(lane >> 2);
+            for (int r = 0; r < nr; ++r) {
+                const float v = lds_f32(base + static_cast<uint32_t>(r * 128) + ((jl ^ static_cast<uint32_t>(r & 7)) << 4));
+                const unsigned long long key = make_key(v, static_cast<uint32_t>(r0 + r));
+                best = key > best ? key : best;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&tb_empty[tb]));
+        }
+        pdl_wait_prior();                   // scratch keys, drafts and outputs from here on
+        head_grid_tail(p, lane < T ? best : 0ull, lane, B);
     }
 
     // ================================================================ teardown
     // Every warp gets here (no early exit after the allocation).  The MMAs
-    // are complete once the last commit has arrived; then the tensor memory
-    // is freed by the warp that allocated it.
+    // are complete once the last commits have arrived; then the tensor
+    // memory is freed by the warp that allocated it.
     __syncthreads();
     if (warp == 1) {
         if (!mbar_wait_bounded(smem_addr(mma_done), 0u, WAIT_LIMIT_AFTER_ERR_NS)) atomicOr(p.err, 2);

@@ -96,7 +96,7 @@ def test_gemm_matches_oracle(sv, oracle, T, K, N):
 
 @pytest.mark.parametrize("V,K,n_draft,n_streams", [
     (2500, 1024, 15, 2),     # 32 rows
-    (5000, 3072, 10, 2),     # 22 rows, ragged third token tile
+    (5000, 3072, 10, 2),     # 22 rows, ragged third token tile, shares of 3-4 units
     (6000, 1024, 31, 1),
     (3000, 1024, 7, 4),      # four streams of 8 rows
 ])
