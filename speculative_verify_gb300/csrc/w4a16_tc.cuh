@@ -14,8 +14,8 @@
 // operand in fp16: the box's largest scale lands in [2^10, 2^11), the level
 // (an integer in -8..7) times the 8-bit significand of a bf16 scale has at
 // most 11 significant bits, so the product is exact in fp16 for every scale
-// within 2^28 of the box's largest (smaller ones round at 2^-24 of it, below
-// the fp32 rounding of the sum).  The tensor cores then add the products of
+// of at least 2^-27 times the box's largest (a smaller one is rounded, by
+// less than 2^-34 of the largest, below the fp32 rounding of the sum).  The tensor cores then add the products of
 // all eight groups in fp32, and the epilogue multiplies the box's sums by
 // 2^(E - 137): exactly the sum of the products level * s * x, which the
 // per-group form adds in another order.  The product is formed in one fp16
@@ -25,35 +25,41 @@
 // Work: a unit is one 128-row tile x two 128-column groups (TC_GU); units
 // are numbered tile-major and split evenly over the grid (stream-K), split
 // tiles finished in CTA order as in the other kernels.  A box is four units
-// (fewer at the start of a CTA's share); boxes never straddle tiles (the
-// kernel needs K a multiple of 1024).
+// (fewer at the ends of a CTA's share); boxes never straddle tiles (the
+// kernel needs K a multiple of 1024).  Units alternate between two
+// pipelines, each a dequant warpgroup and an MMA warp with a private ring of
+// three one-group A slots (64 tensor-memory columns each) and a private
+// accumulator per box: no barrier is shared between the pipelines, and every
+// waiter walks its barriers' phases in order, so no parity wait can alias a
+// phase two ahead.
 //
-// Warp roles (15 warps):
+// Warp roles (16 warps):
 //  * warp 0, producer (lane 0): per unit, the two groups' packed weights of
 //    the tile's 128 rows (TMA boxes, 64-byte swizzle) and their activations
 //    in the canonical K-major layout written by xprep_kernel<true> (one bulk
 //    copy, 16 KB), completion on the stage's mbarrier.  Weights of the first
 //    stages go out before griddepcontrol.wait.
-//  * warp 1 allocates the CTA's tensor memory (512 columns: three 128-column
-//    A buffers, two pairs of 32-column box accumulators) and frees it at
-//    the end.  Warps 1 and 14 issue the MMAs of the unit's first and second
-//    group, every unit in order, each into its own accumulator of the box's
-//    pair: the whole warp runs the loop and an elected lane issues eight
-//    tcgen05.mma (A from tensor memory, B = the stage's activation block;
-//    the box's first clears the accumulator), then commits per unit to the
-//    A buffer's and the stage's mbarriers and per box to the pair's.  (Every
-//    waiter walks its barriers' phases in order, so no parity wait can
-//    alias a phase two ahead.)
-//  * warps 2..9, dequant (two warpgroups taking units in turn): thread =
+//  * warps 1 and 14, MMA issue for pipelines 0 and 1 (warp 1 also allocates
+//    the 512 tensor-memory columns and frees them at the end): per unit of
+//    the pipeline, per group eight tcgen05.mma (A from the group's slot, B =
+//    the stage's activation block; the pipeline's first MMA of a box clears
+//    its accumulator) issued by one elected lane of the whole warp, a commit
+//    that frees the slot, one that frees the stage, and at every box end one
+//    to the box's accumulator set.
+//  * warps 2..5 and 6..9, dequant warpgroups of pipelines 0 and 1: thread =
 //    weight row; per box it loads the row's eight scales (16 bytes, read
 //    ahead) and forms the fp16 factors, per group it reads its row's 16
 //    words and stores the 128 scaled levels (pairs (j, j+4), the order the
-//    activation chunks use) to its tensor-memory lane as the A operand.
+//    activation chunks use) to its tensor-memory lane of the next slot.
 //  * warps 10..13, epilogue: thread = row; per box it reads the row's two
-//    accumulators of 32 fp32 sums back from tensor memory, adds them,
-//    multiplies by 2^(E - 137) and
-//    adds them to its fp32 accumulators; at the end of its share of a tile
-//    it writes y or folds the logits into per-token argmax keys.
+//    accumulators (one per pipeline, each only if the box has a unit of that
+//    pipeline), adds them, multiplies by 2^(E - 137) and adds the result to
+//    its fp32 accumulators; at the end of its share of a tile it writes y, or
+//    for the head hands the tile's logits to the reducer.
+//  * warp 15, reducer (head only): lane t keeps the largest (logit, lowest
+//    id) key of token t over the CTA's finished tiles, read from a
+//    double-buffered shared-memory tile, then runs the grid argmax and the
+//    verify.
 #pragma once
 
 #include "w4a16_stream.cuh"

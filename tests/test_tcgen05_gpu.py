@@ -59,6 +59,39 @@ def test_one_hot_pins_tensor_memory_layout(sv, oracle):
     assert sv.last_device_error() == 0
 
 
+def test_scales_spanning_a_box(sv, oracle):
+    """Group scales 2^e with e spread over 2^+-20 inside each row's box of
+    eight groups, and rows whose smallest group scale is 2^-40 of the
+    largest.  One-hot activations give y = (nibble - 8) * s for one column of
+    each group.  The tcgen05 kernel forms level * s * 2^(137 - E) in fp16 per
+    box of eight groups (E the row's largest scale exponent in the box): the
+    product is exact whenever s is at least 2^-27 of the box's largest scale,
+    and otherwise off by less than 2^-30 of the largest.  The mma.sync kernel
+    scales in fp32 and is exact everywhere."""
+    K, N, T = 1024, 256, 32
+    W = K // 8
+    rng = np.random.default_rng(77)
+    Wq = rng.integers(0, 2**32, size=(N, W), dtype=np.uint32)
+    lv = ((Wq[:, :, None] >> (4 * np.arange(8, dtype=np.uint32))) & 0xF).reshape(N, K).astype(np.int64) - 8
+    e = rng.integers(-20, 21, size=(N, K // 128))
+    e[N // 2:, 0] = e[N // 2:, 1:].max(axis=1) - 40     # far below the box's largest
+    s = gen.f32_to_bf16_bits((2.0 ** e).astype(np.float32))
+    sval = gen.bf16_bits_to_f32(s).astype(np.float64)
+    one = gen.f32_to_bf16_bits(np.float32(1.0))
+    ks = 32 * np.arange(T)                               # four columns of every group
+    x = np.zeros((T, K), np.uint16)
+    x[np.arange(T), ks] = one
+    y = sv.w4a16_gemm(dev_bits16(x), dev_words(Wq), dev_bits16(s))
+    torch.cuda.synchronize()
+    got = to_f32(y).astype(np.float64)
+    expect = (lv[:, ks] * sval[:, ks // 128]).T           # [T][N]
+    smax = sval.max(axis=1)                              # one box per row (K = 1024)
+    exact = sval[:, ks // 128].T >= smax[None, :] * 2.0 ** -27
+    assert np.array_equal(got[exact], expect[exact])
+    assert np.all(np.abs(got - expect) <= smax[None, :] * 2.0 ** -30)
+    assert sv.last_device_error() == 0
+
+
 @pytest.mark.parametrize("T,K", [(32, 1024), (24, 5120)])
 def test_activation_dynamic_range(sv, oracle, T, K):
     """The wide-range rows (2^100, 2^-100, spread over 2^+-40, outliers),
