@@ -233,8 +233,8 @@ int plan_layout(Params &p, int smem_optin, int *smem_total)
     const int ids_bytes = up(2 * ROWS * 4, 128);
     const int red_bytes = up(C::RED_FLOATS * 4, 128);
     const int bk_bytes = HEAD ? up(32 * BK_STRIDE * 8, 128) : 0;
-    const int fixed = xres_bytes + 2 * p.sbuf_bytes + ids_bytes + red_bytes + 128 + ROWS * 8 * 4 + bk_bytes + 256 +
-                      6 * 8 + 16;
+    const int pre_bytes = NT == 1 ? PRE_PARTS * ROWS * 8 * 4 : 0;
+    const int fixed = xres_bytes + 2 * p.sbuf_bytes + ids_bytes + red_bytes + 128 + pre_bytes + bk_bytes + 256 + 6 * 8 + 16;
     int nst = (smem_optin - fixed - 1024) / (p.stage_bytes + 16);
     if (nst > 8) nst = 8;
     if (nst < 2) return SV_ERR_SHAPE;
@@ -251,7 +251,7 @@ int plan_layout(Params &p, int smem_optin, int *smem_total)
     p.off_xsc = off;
     off += 128;
     p.off_pre = off;
-    off += ROWS * 8 * 4;
+    off += pre_bytes;
     p.off_bk = off;
     off += bk_bytes;
     p.off_xzero = off;

@@ -60,6 +60,7 @@ __host__ __device__ constexpr int consumer_warps(int NT, bool XRES, bool GATHER)
 }
 constexpr int TMAX = 32;                        // largest T
 constexpr int PART_FLOATS = TMAX * ROWS;        // one split-tile partial
+constexpr int PRE_PARTS = 2;                     // partials a finishing CTA copies ahead (one token tile)
 constexpr int XBOX = 144;                       // bf16 activation box width (elements), one token tile
 constexpr int XROW_BYTES = XBOX * 2;            // = 32 (mod 128): conflict-free B loads
 constexpr int XSTR = 272;                       // bytes per token row of a converted group block
@@ -106,7 +107,7 @@ struct Params {
     int off_sbuf, off_ids, off_red, off_bars;
     int off_xres, xres_stride;  // resident activations (XRES kernels only)
     int off_xsc;                // XRES: per-token largest |x| (bf16 bits), [8] u32
-    int off_pre;                // prefetched partial of a split last tile, [ROWS][8] floats
+    int off_pre;                // NT = 1: other contributors' partials of the tile this CTA finishes, [PRE_PARTS][ROWS][8] floats
     int off_bk;                 // HEAD: running best key per lane and token, [32][BK_STRIDE] u64
     int off_xzero;              // XBF: 256 zero bytes, the activation row of absent tokens
     // GEMM output
@@ -632,56 +633,55 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
         if (p.stall_ns != 0u && b == 0) wait_or_flag_for(p, flag, smem_addr(stall_bar), 0u, p.stall_ns);
         for (int k = 0, tile = tile_first; tile <= tile_last; ++k, ++tile) {
             const int kb = k & 1;
-            // The CTA's last tile, when it is shared with exactly one later
-            // CTA: that CTA works on it first and has normally published its
-            // partial long before.  Confirm that (acquire load of the tile's
-            // counter) and copy the partial to shared memory while the
-            // consumers are still on this tile, so that the end of the kernel
-            // only adds and stores.  Polling stops when this CTA's own sums
-            // arrive; the regular path below then takes over.
             const bool first = tile == tile_first;
             const int tbf = first ? bfA : bfZ, tnc = first ? ncA : ncZ;
-            bool pre_ok = false;
-            if (NT == 1 && tile == tile_last) {
-                if (tbf == b && tnc == 2) {
-                    const uint64_t t0 = global_timer_ns();
-                    while (true) {
-                        const unsigned seen = ld_acquire_gpu_u32(&p.ctr[b]);
-                        if (__all_sync(0xFFFFFFFFu, seen == 1u)) {
-                            pre_ok = true;
-                            break;
-                        }
-                        if (mbar_try_wait(smem_addr(red_full), static_cast<uint32_t>(k & 1))) break;
-                        if (global_timer_ns() - t0 > WAIT_LIMIT_NS) break;
+            // The tile this CTA finishes (its own part is the end of its
+            // range): while the consumers are still on it, poll the tile's
+            // counter and, once the other contributors are all in, copy their
+            // partials to shared memory, so that the end of the kernel only
+            // adds and stores.  Polling stops when this CTA's own sums are
+            // ready; the finish below then waits and loads the rest itself.
+            int npre = 0;
+            const long long ts = static_cast<long long>(tile) * G, te = ts + G;
+            const bool split = !(u0 <= ts && u1 >= te);
+            if (NT == 1 && tile == tile_last && split && tbf == b && tnc > 1 && tnc - 1 <= PRE_PARTS) {
+                const uint64_t t0 = global_timer_ns();
+                while (true) {
+                    if (__all_sync(0xFFFFFFFFu, ld_acquire_gpu_u32(&p.ctr[b]) == static_cast<unsigned>(tnc - 1))) {
+                        npre = tnc - 1;
+                        break;
                     }
-                    if (pre_ok) {
-                        const float *src = p.part + static_cast<size_t>(b + 1) * 2 * PART_FLOATS;
-                        float *dst = reinterpret_cast<float *>(smem + p.off_pre);
+                    if (mbar_try_wait(smem_addr(red_full), static_cast<uint32_t>(k & 1))) break;
+                    if (global_timer_ns() - t0 > WAIT_LIMIT_NS) break;
+                    __nanosleep(256);
+                }
+                float *dst = reinterpret_cast<float *>(smem + p.off_pre);
+                for (int j = 0; j < npre; ++j) {
+                    const float *src = p.part + static_cast<size_t>(b + 1 + j) * 2 * PART_FLOATS;
 #pragma unroll
-                        for (int h = 0; h < 2; ++h)
+                    for (int h = 0; h < 2; ++h)
 #pragma unroll
-                            for (int q = 0; q < 2; ++q)
-                                if (4 * q < T)
-                                    *reinterpret_cast<float4 *>(dst + (lane + 32 * h) * 8 + 4 * q) =
-                                        ldcg_f4(src + (lane + 32 * h) * TMAX + 4 * q);
-                    }
+                        for (int q = 0; q < 2; ++q)
+                            if (4 * q < T)
+                                *reinterpret_cast<float4 *>(dst + (j * ROWS + lane + 32 * h) * 8 + 4 * q) =
+                                    ldcg_f4(src + (lane + 32 * h) * TMAX + 4 * q);
                 }
             }
             wait_or_flag(p, flag, smem_addr(red_full), static_cast<uint32_t>(k & 1));
-            const long long ts = static_cast<long long>(tile) * G, te = ts + G;
-            const bool complete = (u0 <= ts) && (u1 >= te);
+            const bool complete = !split;
             // This CTA's sums of the group slots (fixed slot order) for rows
             // lane and lane+32 of every token, kept as v[t][h] in registers
             // for the tokens being processed (chunks of 4).
-            // Split tiles: the tile's contributors are CTAs bf..bf+nc-1.  A
-            // CTA that finds (acquire load of the tile's counter) that all
-            // the others have already published their partials finishes the
-            // tile at once.  Otherwise it publishes its own partial in the
-            // scratch area as [row][TMAX] floats and counts itself in; the
-            // CTA whose count completes the tile finishes it.  The finisher
-            // adds the contributions in CTA order -- its own from shared
-            // memory, the others' with vectorised loads issued together --
-            // so results do not depend on who finishes.
+            // Split tiles: the tile's contributors are CTAs bf..bf+nc-1, and
+            // bf finishes the tile.  bf's part is the end of its range, so it
+            // comes to the tile last of its work; the others' parts are the
+            // start of their ranges (or all of them), done early.  The others
+            // publish their partials in the scratch area as [row][TMAX]
+            // floats and count themselves in with a release add they do not
+            // wait for; bf waits (acquire loads, bounded) until all nc - 1
+            // are in, adds the contributions in CTA order -- its own from
+            // shared memory, the others' with vectorised loads issued
+            // together -- and resets the counter for the next launch.
             int bf = 0, nc = 1, me = 0;
             bool finish = true;
             const float *others[4] = {nullptr, nullptr, nullptr, nullptr};
@@ -689,12 +689,7 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
                 bf = tbf;
                 nc = tnc;
                 me = b - bf;
-                if (pre_ok) {
-                    finish = true;          // the other contributor is counted in
-                } else {
-                    const unsigned seen = ld_acquire_gpu_u32(&p.ctr[bf]);
-                    finish = __all_sync(0xFFFFFFFFu, seen == static_cast<unsigned>(nc - 1));
-                }
+                finish = me == 0;
                 if (!finish) {
                     float *mine = p.part + (static_cast<size_t>(b) * 2 + (tile == tile_first ? 0 : 1)) * PART_FLOATS;
                     for (int t0 = 0; t0 < T; t0 += 4) {
@@ -704,15 +699,17 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
                             *reinterpret_cast<float4 *>(mine + row * TMAX + t0) = slot_sums4<NT, C::GPS>(red, t0, row, T);
                         }
                     }
-                    __threadfence();
                     __syncwarp();
-                    unsigned last = 0;
-                    if (lane == 0) {
-                        const unsigned old = atomic_add_acq_rel_gpu(&p.ctr[bf], 1u);
-                        last = (old == static_cast<unsigned>(nc - 1));
+                    if (lane == 0) red_add_release_gpu(&p.ctr[bf], 1u);
+                } else if (npre == 0) {
+                    const uint64_t t0 = global_timer_ns();
+                    while (!__all_sync(0xFFFFFFFFu, ld_acquire_gpu_u32(&p.ctr[bf]) == static_cast<unsigned>(nc - 1))) {
+                        if (global_timer_ns() - t0 > (*flag ? WAIT_LIMIT_AFTER_ERR_NS : WAIT_LIMIT_NS)) {
+                            *flag = 1;
+                            if (lane == 0) atomicOr(p.err, 2);
+                            break;
+                        }
                     }
-                    finish = __shfl_sync(0xFFFFFFFFu, last, 0) != 0;
-                    if (finish) __threadfence();
                 }
                 if (finish) {
                     if (lane == 0) p.ctr[bf] = 0u;        // ready for the next launch
@@ -746,11 +743,11 @@ w4a16_stream_kernel(const __grid_constant__ Params p, const __grid_constant__ CU
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
                             if (j < nc) {
-                                const float4 e =
-                                    j == me ? mine4
-                                    : (NT == 1 && pre_ok) ? *reinterpret_cast<const float4 *>(
-                                                   reinterpret_cast<const float *>(smem + p.off_pre) + row * 8 + t0)
-                                             : ldcg_f4(others[j] + row * TMAX + t0);
+                                const float4 e = j == me ? mine4
+                                                 : (NT == 1 && npre > 0) ? *reinterpret_cast<const float4 *>(
+                                                       reinterpret_cast<const float *>(smem + p.off_pre) +
+                                                       ((j - 1) * ROWS + row) * 8 + t0)
+                                                 : ldcg_f4(others[j] + row * TMAX + t0);
                                 if (j == 0) {
                                     acc4 = e;
                                 } else {
