@@ -178,7 +178,6 @@ w4a16_tc_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
     uint64_t *mma_done = tb_empty + 2;       //         MMA commits after the last unit
     uint64_t *stall_bar = mma_done + 1;      //         never completed (test hook)
     volatile int *flag = reinterpret_cast<volatile int *>(stall_bar + 1);   // a wait timed out
-    volatile int *decision = flag + 1;       // split-tile protocol
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(flag + 2);
     volatile int *tb_tile = flag + 3;        // [2] head: the tile in each buffer, -1 = no more
 
@@ -407,13 +406,11 @@ w4a16_tc_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
         // contributors of the first and the last tile, as in the other kernels
         const int tile_last = static_cast<int>((u1 - 1) / G);
         int bfA = b, ncA = 1, ncZ = 1;
-        bool bf_firstA = true;
         {
             const long long ts = static_cast<long long>(tile_first) * G, te = ts + G;
             if (u0 > ts || u1 < te) {
                 bfA = cta_of(ts, U, B);
                 ncA = cta_of(te - 1, U, B) - bfA + 1;
-                bf_firstA = cta_start(bfA, U, B) == ts;
             }
             const long long tz = static_cast<long long>(tile_last) * G;
             if (tile_last != tile_first && u1 < tz + G) ncZ = cta_of(tz + G - 1, U, B) - b + 1;
@@ -469,43 +466,49 @@ w4a16_tc_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
             const bool complete = (u0 <= ts) && (u1 >= te);
             bool finish = true;
             if (!complete) {
-                // every contributor publishes its row sums and counts itself in;
-                // the last to arrive adds them all in CTA order
+                // The tile's first contributor bf finishes it: for bf the
+                // tile is the end of its range and comes last, for the
+                // others it is the start of theirs.  The others publish their
+                // row sums and count themselves in with a release add they
+                // do not wait for; bf waits (bounded) until all nc - 1 are
+                // in, adds them after its own in CTA order and resets the
+                // counter for the next launch.
                 const bool first = tile == tile_first;
                 const int bf = first ? bfA : b;
                 const int nc = first ? ncA : ncZ;
-                const int slot_bf = (first ? bf_firstA : (u0 == ts)) ? 0 : 1;
-                float *mine = p.part + (static_cast<size_t>(b) * 2 + (first ? 0 : 1)) * WIDE_PART_FLOATS + row * TMAX;
+                finish = bf == b;
+                if (!finish) {
+                    float *mine = p.part + static_cast<size_t>(b) * 2 * WIDE_PART_FLOATS + row * TMAX;
 #pragma unroll
-                for (int t = 0; t < 32; t += 4)
-                    __stcg(reinterpret_cast<float4 *>(mine + t), make_float4(acc[t], acc[t + 1], acc[t + 2], acc[t + 3]));
-                __threadfence();
-                named_bar_sync(1, NTHR_E);
-                if (ew == 0 && lane == 0) {
-                    const unsigned old = atomic_add_acq_rel_gpu(&p.ctr[bf], 1u);
-                    const bool last = old == static_cast<unsigned>(nc - 1);
-                    if (last) p.ctr[bf] = 0u;          // everyone is in: ready for the next launch
-                    *decision = last ? WIDE_FINISH : WIDE_DONE;
-                }
-                named_bar_sync(1, NTHR_E);
-                finish = *decision == WIDE_FINISH;
-                named_bar_sync(1, NTHR_E);         // the decision word is read before it is reused
-                if (finish) {
-                    __threadfence();
-                    for (int jc = 0; jc < nc; ++jc) {
-                        const float *src = p.part + (static_cast<size_t>(bf + jc) * 2 + (jc == 0 ? slot_bf : 0)) *
-                                                        WIDE_PART_FLOATS + row * TMAX;
-                        float4 e4[8];
+                    for (int t = 0; t < 32; t += 4)
+                        __stcg(reinterpret_cast<float4 *>(mine + t), make_float4(acc[t], acc[t + 1], acc[t + 2], acc[t + 3]));
+                    named_bar_sync(1, NTHR_E);
+                    if (ew == 0 && lane == 0) red_add_release_gpu(&p.ctr[bf], 1u);
+                } else {
+                    if (ew == 0) {
+                        const uint64_t t0 = global_timer_ns();
+                        while (!__all_sync(0xFFFFFFFFu, ld_acquire_gpu_u32(&p.ctr[bf]) == static_cast<unsigned>(nc - 1))) {
+                            if (global_timer_ns() - t0 > (*flag ? WAIT_LIMIT_AFTER_ERR_NS : WAIT_LIMIT_NS)) {
+                                *flag = 1;
+                                if (lane == 0) atomicOr(p.err, 2);
+                                break;
+                            }
+                        }
+                    }
+                    named_bar_sync(1, NTHR_E);
+                    if (ew == 0 && lane == 0) p.ctr[bf] = 0u;
+#pragma unroll 1
+                    for (int jc = 1; jc < nc; ++jc) {
+                        const float *src = p.part + static_cast<size_t>(bf + jc) * 2 * WIDE_PART_FLOATS + row * TMAX;
 #pragma unroll
-                        for (int t = 0; t < 8; ++t) e4[t] = __ldcg(reinterpret_cast<const float4 *>(src) + t);
+                        for (int hh = 0; hh < 2; ++hh) {
+                            float4 e4[4];
 #pragma unroll
-                        for (int t = 0; t < 8; ++t) {
-                            if (jc == 0) {
-                                acc[4 * t] = e4[t].x; acc[4 * t + 1] = e4[t].y;
-                                acc[4 * t + 2] = e4[t].z; acc[4 * t + 3] = e4[t].w;
-                            } else {
-                                acc[4 * t] += e4[t].x; acc[4 * t + 1] += e4[t].y;
-                                acc[4 * t + 2] += e4[t].z; acc[4 * t + 3] += e4[t].w;
+                            for (int t = 0; t < 4; ++t) e4[t] = __ldcg(reinterpret_cast<const float4 *>(src) + 4 * hh + t);
+#pragma unroll
+                            for (int t = 0; t < 4; ++t) {
+                                const int c = 16 * hh + 4 * t;
+                                acc[c] += e4[t].x; acc[c + 1] += e4[t].y; acc[c + 2] += e4[t].z; acc[c + 3] += e4[t].w;
                             }
                         }
                     }
