@@ -440,9 +440,10 @@ int launch_wide(Params p, const DeviceState &st, cudaStream_t stream)
 // Shared-memory layout of a tcgen05 launch (offsets in bytes): nst stages
 // of TC_GU x 16 KB (8 KB of packed weights and 8 KB of activations per
 // group) from 0 -- 1024-byte aligned, as the swizzled weight boxes need |
-// the head's two finished-tile buffers | mbarriers, flag, decision word,
-// tensor-memory address, the buffers' tile numbers.  (The scales go from global memory to the dequant and epilogue
-// threads' registers, one 16-byte load per row and box.)
+// the head's two finished-tile buffers | the tokens' xinv, 32 floats |
+// mbarriers, flag, tensor-memory address, the buffers' tile numbers.  (The
+// scales go from global memory to the dequant and epilogue threads'
+// registers, one 16-byte load per row and box.)
 template <bool HEAD>
 int plan_layout_tc(Params &p, int smem_optin, int *smem_total)
 {
@@ -462,6 +463,8 @@ int plan_layout_tc(Params &p, int smem_optin, int *smem_total)
     p.off_sbuf = off;
     p.off_bk = off;                          // finished-tile buffers
     off += tb_bytes;
+    p.off_xinv = off;
+    off += 128;
     p.off_bars = off;
     off += (2 * nst + 2 * TC_NDQ * TC_NSLOT + 2 * TC_NB + 4 + 2) * 8 + 32;
     *smem_total = off;

@@ -108,6 +108,7 @@ struct Params {
     int off_xres, xres_stride;  // resident activations (XRES kernels only)
     int off_xsc;                // XRES: per-token largest |x| (bf16 bits), [8] u32
     int off_pre;                // NT = 1: other contributors' partials of the tile this CTA finishes, [PRE_PARTS][ROWS][8] floats
+    int off_xinv;               // tcgen05: xinv staged in shared memory, [32] floats
     int off_bk;                 // HEAD: running best key per lane and token, [32][BK_STRIDE] u64
     int off_xzero;              // XBF: 256 zero bytes, the activation row of absent tokens
     // GEMM output

@@ -84,7 +84,10 @@ constexpr int TC_MMA2 = TC_EP0 + 4;              // second MMA-issuing warp
 constexpr int TC_RED = TC_MMA2 + 1;              // head: the warp that reduces finished tiles to per-token maxima
 constexpr int TC_WARPS = TC_RED + 1;
 constexpr int TC_TB_BYTES = TC_RT * 32 * 4;      // head: one finished tile's logits, [row][32 tokens] fp32
-constexpr int TC_MAX_STAGES = 8;
+// Four stages (128 KB).  Measured at T = 32: the same lm_head time as six,
+// and GEMMs 0.4-1.3 us faster; a GEMM launch holding more than about 196 KB
+// of shared memory (six stages plus 16-32 KB) ran 1.3-2.5 us slower.
+constexpr int TC_MAX_STAGES = 4;
 constexpr int TC_SHIFT = 137;                    // a box's largest scale x 2^(TC_SHIFT - E) is in [2^10, 2^11)
 static_assert(TC_ACC_COL + TC_NB * TC_NDQ * 32 <= TC_TMEM_COLS, "tensor memory budget");
 static_assert(TC_NDQ == 2, "two pipelines: dequant warpgroup w with MMA warp w");
@@ -402,6 +405,8 @@ w4a16_tc_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
         const int row = 32 * q + lane;
         constexpr uint32_t NTHR_E = 128;
         pdl_wait_prior();                   // xinv, scratch area, outputs and drafts from here on
+        float *xinv_s = reinterpret_cast<float *>(smem + p.off_xinv);
+        if (ew == 0) xinv_s[lane] = __ldg(p.xinv + lane);
         if (p.stall_ns != 0u && b == 0 && ew == 0) wait_or_flag_for(p, flag, smem_addr(stall_bar), 0u, p.stall_ns);
         // contributors of the first and the last tile, as in the other kernels
         const int tile_last = static_cast<int>((u1 - 1) / G);
@@ -415,6 +420,7 @@ w4a16_tc_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
             const long long tz = static_cast<long long>(tile_last) * G;
             if (tile_last != tile_first && u1 < tz + G) ncZ = cta_of(tz + G - 1, U, B) - b + 1;
         }
+        named_bar_sync(1, NTHR_E);          // xinv staged
         const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + TC_ACC_COL;
         const int nbox = G / TC_BOX_UNITS;
         int ntb = 0;                                  // head: tiles handed to the reducer
@@ -461,7 +467,7 @@ w4a16_tc_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
             if (!tile_end) continue;
             // ------------------------------------------- end of this CTA's share of `tile`
 #pragma unroll
-            for (int t = 0; t < 32; ++t) acc[t] *= __ldg(p.xinv + t);
+            for (int t = 0; t < 32; ++t) acc[t] *= xinv_s[t];
             const long long ts = static_cast<long long>(tile) * G, te = ts + G;
             const bool complete = (u0 <= ts) && (u1 >= te);
             bool finish = true;
@@ -495,7 +501,7 @@ w4a16_tc_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
                             }
                         }
                     }
-                    named_bar_sync(1, NTHR_E);
+                    named_bar_sync(1, NTHR_E);      // all nc - 1 are in
                     if (ew == 0 && lane == 0) p.ctr[bf] = 0u;
 #pragma unroll 1
                     for (int jc = 1; jc < nc; ++jc) {
