@@ -181,8 +181,6 @@ __device__ __forceinline__ unsigned atomic_add_acq_rel_gpu(unsigned *p, unsigned
     return old;
 }
 
-// Load with acquire semantics at GPU scope: later reads of this thread see
-// every write released before the value it returns.
 // Release add without a result: the thread does not wait for it.  Writes
 // made before it by this thread, and by the threads of its warp ordered
 // before it by __syncwarp(), are visible to an acquire load that sees it.
@@ -191,6 +189,8 @@ __device__ __forceinline__ void red_add_release_gpu(unsigned *p, unsigned v)
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// Load with acquire semantics at GPU scope: later reads of this thread see
+// every write released before the value it returns.
 __device__ __forceinline__ unsigned ld_acquire_gpu_u32(const unsigned *p)
 {
     unsigned v;

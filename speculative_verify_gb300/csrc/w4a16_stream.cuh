@@ -385,13 +385,17 @@ __device__ __forceinline__ void stage_tile_meta(const Params &p, int tile, uint8
 __device__ __forceinline__ void head_grid_tail(const Params &p, unsigned long long best, int lane, int B)
 {
     const int T = p.T;
+    // The warp's maxima, then one acquire-release count per CTA: the warp
+    // barrier orders every lane's maximum before lane 0's release, and lane
+    // 0's acquire (the count that completes the grid) before the last CTA's
+    // reads of the keys.
     if (lane < T && best != 0ull) atomicMax(&p.keys[lane], best);
-    __threadfence();
     __syncwarp();
     unsigned last = 0;
-    if (lane == 0) last = (atomicAdd(p.done, 1u) == static_cast<unsigned>(B - 1));
-    if (__shfl_sync(0xFFFFFFFFu, last, 0)) {
-        __threadfence();
+    if (lane == 0) last = (atomic_add_acq_rel_gpu(p.done, 1u) == static_cast<unsigned>(B - 1));
+    last = __shfl_sync(0xFFFFFFFFu, last, 0);
+    __syncwarp();
+    if (last) {
         int32_t a = -1;
         unsigned long long kk = 0ull;
         if (lane < T) {
