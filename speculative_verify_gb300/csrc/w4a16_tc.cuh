@@ -28,7 +28,7 @@
 // (fewer at the ends of a CTA's share); boxes never straddle tiles (the
 // kernel needs K a multiple of 1024).  Units alternate between two
 // pipelines, each a dequant warpgroup and an MMA warp with a private ring of
-// three one-group A slots (64 tensor-memory columns each) and a private
+// two one-group A slots (64 tensor-memory columns each) and a private
 // accumulator per box: no barrier is shared between the pipelines, and every
 // waiter walks its barriers' phases in order, so no parity wait can alias a
 // phase two ahead.
@@ -74,7 +74,9 @@ constexpr int TC_W_BYTES = TC_RT * 64;           // one group of a tile's packed
 constexpr int TC_X_BYTES = 32 * 128 * 2;         // one group of 32 tokens, fp16
 constexpr int TC_STAGE = TC_GU * (TC_W_BYTES + TC_X_BYTES);   // weights of the unit's groups, then their activations
 constexpr int TC_NDQ = 2;                        // dequant warpgroups, taking units in turn
-constexpr int TC_NSLOT = 3;                      // A slots of one group (64 columns) per pipeline
+// A slots of one group (64 columns) per pipeline.  Measured on the T = 32
+// lm_head: one slot 200 us, two 170, three 174.
+constexpr int TC_NSLOT = 2;
 constexpr int TC_NB = 2;                         // box accumulator sets (one 32-column accumulator per pipeline)
 constexpr uint32_t TC_TMEM_COLS = 512;
 constexpr uint32_t TC_ACC_COL = TC_NDQ * TC_NSLOT * 64;   // the accumulators after the A slots

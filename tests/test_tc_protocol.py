@@ -12,13 +12,16 @@ barrier moved two phases past it (parity aliasing), or if no role can move
 (deadlock).  The launch shapes are those of the GPU tests and the benchmark
 step (units of two 128-column groups over 128-row tiles, stream-K shares of
 152 CTAs)."""
+import os
 import random
+import re
 
 import pytest
 
-NST = 6          # stages (the kernel's count for heads; GEMMs round 7 down to 6)
-NSLOT = 3        # A slots per pipeline
 BOXU = 4         # units per box of eight groups
+# (stages, A slots per pipeline) replayed; the kernel's own values are
+# checked to be among them
+CONFIGS = [(4, 2), (2, 2), (4, 1), (6, 3), (4, 3)]
 
 
 class Aliasing(Exception):
@@ -45,7 +48,7 @@ class Bar:
         return real
 
 
-def roles(n_units, grp_first, G):
+def roles(n_units, grp_first, G, NST, NSLOT):
     full = [Bar("full%d" % i, 1) for i in range(NST)]
     empty = [Bar("empty%d" % i, 1) for i in range(NST)]
     a_full = [[Bar("a_full%d.%d" % (w, i), 4) for i in range(NSLOT)] for w in range(2)]
@@ -115,9 +118,9 @@ def roles(n_units, grp_first, G):
     return main, pending
 
 
-def replay(n_units, grp_first, G, seed):
+def replay(n_units, grp_first, G, seed, nst, nslot):
     rnd = random.Random(seed)
-    gens, pending = roles(n_units, grp_first, G)
+    gens, pending = roles(n_units, grp_first, G, nst, nslot)
     waiting = dict.fromkeys(gens)
     live = set(gens)
     while live or pending[0] or pending[1]:
@@ -143,15 +146,31 @@ SHAPES = [(70, 1024), (300, 1024), (2500, 1024), (20000, 1024), (5000, 3072), (1
           (2000, 5120), (10240, 5120), (34816, 5120), (248320, 5120), (70, 17408), (5120, 17408)]
 
 
+def kernel_constants():
+    """TC_NSLOT and the stage count of a launch (TC_MAX_STAGES; shared memory
+    holds more for every shape) from the kernel's source."""
+    src = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                            "speculative_verify_gb300", "csrc", "w4a16_tc.cuh")).read()
+    nslot = int(re.search(r"constexpr int TC_NSLOT = (\d+);", src).group(1))
+    nst = int(re.search(r"constexpr int TC_MAX_STAGES = (\d+);", src).group(1))
+    return nst, nslot
+
+
+def test_the_kernels_configuration_is_replayed():
+    assert kernel_constants() in CONFIGS
+
+
+@pytest.mark.parametrize("nst,nslot", CONFIGS)
 @pytest.mark.parametrize("V,K", SHAPES)
-def test_protocol_has_no_deadlock_and_no_aliasing(V, K):
+def test_protocol_has_no_deadlock_and_no_aliasing(V, K, nst, nslot):
     G = K // 128 // 2                       # units per tile
     U = ((V + 127) // 128) * G
     B = min(152, U)
+    seeds = 3 if (nst, nslot) == kernel_constants() else 1
     for b in range(B):
         u0, u1 = b * U // B, (b + 1) * U // B
-        for seed in range(3):
-            r = replay(u1 - u0, u0 % G, G, seed)
+        for seed in range(seeds):
+            r = replay(u1 - u0, u0 % G, G, seed, nst, nslot)
             assert r is None, (V, K, b, r)
 
 
@@ -162,7 +181,7 @@ def test_replay_catches_a_shared_slot_ring():
     global roles
     orig = roles
 
-    def shared_roles(n_units, grp_first, G):
+    def shared_roles(n_units, grp_first, G, NST, NSLOT):
         full = [Bar("full%d" % i, 1) for i in range(NST)]
         empty = [Bar("empty%d" % i, 1) for i in range(NST)]
         a_full = [Bar("a_full%d" % i, 4) for i in range(NSLOT)]
@@ -200,7 +219,7 @@ def test_replay_catches_a_shared_slot_ring():
         found = False
         for seed in range(40):
             try:
-                if replay(24, 0, 20, seed) is not None:
+                if replay(24, 0, 20, seed, 6, 3) is not None:
                     found = True
             except Aliasing:
                 found = True
