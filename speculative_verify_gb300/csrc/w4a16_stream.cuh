@@ -7,9 +7,10 @@
 // (4 KB of packed weights).  Units are numbered tile-major and the grid's B
 // CTAs (B <= SM count, one CTA per SM) take equal contiguous ranges, so every
 // SM streams the same number of bytes whatever N and K are.  A tile whose
-// units straddle two CTAs is finished by the last CTA to arrive (per-tile
-// counter in the scratch area), which adds the fp32 partial sums of all the
-// tile's CTAs in a fixed order: results do not depend on arrival order.
+// units straddle CTAs is finished by its first CTA, for which it is the end
+// of its range: the others publish their fp32 partial sums and count
+// themselves in (per-tile counter in the scratch area), and the finisher
+// adds all of them in CTA order: results do not depend on arrival order.
 //
 // Warp roles inside a CTA (all hand-offs are mbarriers; no CTA-wide barrier
 // after set-up):

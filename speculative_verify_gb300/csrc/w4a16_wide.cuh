@@ -14,8 +14,8 @@
 //
 // Work decomposition: a unit is one tile x one 128-column group; units are
 // numbered tile-major and split evenly over the grid (stream-K), as in
-// w4a16_stream_kernel.  A tile shared by several CTAs is finished by the
-// last to arrive, adding the partial sums of all its CTAs in CTA order.
+// w4a16_stream_kernel.  A tile shared by several CTAs is finished by its
+// first CTA, adding the partial sums of all its CTAs in CTA order.
 //
 // Warp roles: warps 0..NCW-1 are consumers; warp NCW is the producer.
 //  * producer: per unit, the tile's packed weights of the group (TMA boxes
@@ -50,9 +50,6 @@ __host__ __device__ constexpr int wide_rt(int ncw) { return ncw * WIDE_WROWS; }
 // [8 * floor(grp / 8), + 8) of the tile's rows.
 __device__ __forceinline__ bool wide_new_box(bool first, int grp) { return first || (grp & 7) == 0; }
 
-// Shared decision word of the split-tile protocol.
-enum : int { WIDE_FINISH = 1, WIDE_DONE = 2 };
-
 template <int NT, bool HEAD, int NCW>
 __global__ void __launch_bounds__((NCW + 1) * 32, 1)
 w4a16_wide_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tmW,
@@ -74,7 +71,6 @@ w4a16_wide_kernel(const __grid_constant__ Params p, const __grid_constant__ CUte
     uint64_t *empty = bars + nst;           // [nst] consumers -> producer
     uint64_t *stall_bar = bars + 2 * nst;   // never completed (test hook)
     volatile int *flag = reinterpret_cast<volatile int *>(bars + 2 * nst + 1);   // a wait timed out
-    volatile int *decision = flag + 1;      // split-tile protocol, written by consumer thread 0
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int B = gridDim.x, b = blockIdx.x;
@@ -177,16 +173,14 @@ w4a16_wide_kernel(const __grid_constant__ Params p, const __grid_constant__ CUte
         for (int e = 0; e < 2; ++e) xinv[nt][e] = __ldg(p.xinv + nt * 8 + 2 * c + e);
 
     // Contributors of the first and the last tile (the only ones that can be
-    // shared): CTAs bf .. bf + nc - 1; whether bf's range starts at the tile.
+    // shared): CTAs bf .. bf + nc - 1.
     const int tile_last = static_cast<int>((u1 - 1) / G);
     int bfA = b, ncA = 1, bfZ = b, ncZ = 1;
-    bool bf_firstA = true;
     {
         const long long ts = static_cast<long long>(tile_first) * G, te = ts + G;
         if (u0 > ts || u1 < te) {
             bfA = cta_of(ts, U, B);
             ncA = cta_of(te - 1, U, B) - bfA + 1;
-            bf_firstA = cta_start(bfA, U, B) == ts;
         }
         const long long tz = static_cast<long long>(tile_last) * G;
         if (tile_last != tile_first && u1 < tz + G) ncZ = cta_of(tz + G - 1, U, B) - b + 1;
@@ -283,41 +277,47 @@ w4a16_wide_kernel(const __grid_constant__ Params p, const __grid_constant__ CUte
         const bool complete = (u0 <= ts) && (u1 >= te);
         bool finish = true;
         if (!complete) {
-            // Split tile: every contributor publishes its partial sums and
-            // counts itself in; the last to arrive adds all of them in CTA
-            // order (its own read back like the others'), so the result does
-            // not depend on who finishes.
+            // Split tile: finished by its first contributor bf, for which it
+            // is the end of its range (the others' parts are the start of
+            // theirs).  The others publish their partial sums and count
+            // themselves in with a release add they do not wait for; bf
+            // waits (bounded) until all nc - 1 are in, adds them after its
+            // own in CTA order and resets the counter for the next launch.
             const bool first = tile == tile_first;
             const int bf = first ? bfA : bfZ;
             const int nc = first ? ncA : ncZ;
-            // partial slot of contributor bf: 0 when the tile is bf's first
-            const int slot_bf = (first ? bf_firstA : (u0 == ts)) ? 0 : 1;
-            float *mine = p.part + (static_cast<size_t>(b) * 2 + (first ? 0 : 1)) * WIDE_PART_FLOATS;
+            finish = bf == b;
+            if (!finish) {
+                // the tile is this CTA's first: partial slot 0
+                float *mine = p.part + static_cast<size_t>(b) * 2 * WIDE_PART_FLOATS;
 #pragma unroll
-            for (int r = 0; r < WIDE_R; ++r)
+                for (int r = 0; r < WIDE_R; ++r)
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh)
+                    for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        const int row = warp * WIDE_WROWS + r * 16 + g + 8 * hh;
-                        __stcg(reinterpret_cast<float2 *>(mine + row * TMAX + nt * 8 + 2 * c),
-                               make_float2(acc[r][nt][2 * hh], acc[r][nt][2 * hh + 1]));
+                        for (int nt = 0; nt < NT; ++nt) {
+                            const int row = warp * WIDE_WROWS + r * 16 + g + 8 * hh;
+                            __stcg(reinterpret_cast<float2 *>(mine + row * TMAX + nt * 8 + 2 * c),
+                                   make_float2(acc[r][nt][2 * hh], acc[r][nt][2 * hh + 1]));
+                        }
+                named_bar_sync(1, NTHR_C);
+                if (threadIdx.x == 0) red_add_release_gpu(&p.ctr[bf], 1u);
+            } else {
+                if (warp == 0) {
+                    const uint64_t t0 = global_timer_ns();
+                    while (!__all_sync(0xFFFFFFFFu, ld_acquire_gpu_u32(&p.ctr[bf]) == static_cast<unsigned>(nc - 1))) {
+                        if (global_timer_ns() - t0 > (*flag ? WAIT_LIMIT_AFTER_ERR_NS : WAIT_LIMIT_NS)) {
+                            *flag = 1;
+                            if (lane == 0) atomicOr(p.err, 2);
+                            break;
+                        }
                     }
-            __threadfence();
-            named_bar_sync(1, NTHR_C);
-            if (threadIdx.x == 0) {
-                const unsigned old = atomic_add_acq_rel_gpu(&p.ctr[bf], 1u);
-                const bool last = old == static_cast<unsigned>(nc - 1);
-                if (last) p.ctr[bf] = 0u;          // everyone is in: ready for the next launch
-                *decision = last ? WIDE_FINISH : WIDE_DONE;
-            }
-            named_bar_sync(1, NTHR_C);
-            finish = *decision == WIDE_FINISH;
-            if (finish) {
-                __threadfence();
-                for (int j = 0; j < nc; ++j) {
-                    const float *src = p.part + (static_cast<size_t>(bf + j) * 2 + (j == 0 ? slot_bf : 0)) *
-                                                    WIDE_PART_FLOATS;
+                }
+                named_bar_sync(1, NTHR_C);      // all nc - 1 are in
+                if (threadIdx.x == 0) p.ctr[bf] = 0u;
+#pragma unroll 1
+                for (int j = 1; j < nc; ++j) {
+                    const float *src = p.part + static_cast<size_t>(bf + j) * 2 * WIDE_PART_FLOATS;
                     float2 e2[WIDE_R][2][NT];     // one contributor's values, loads all in flight
 #pragma unroll
                     for (int r = 0; r < WIDE_R; ++r)
@@ -334,13 +334,8 @@ w4a16_wide_kernel(const __grid_constant__ Params p, const __grid_constant__ CUte
                         for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
                             for (int nt = 0; nt < NT; ++nt) {
-                                if (j == 0) {
-                                    acc[r][nt][2 * hh] = e2[r][hh][nt].x;
-                                    acc[r][nt][2 * hh + 1] = e2[r][hh][nt].y;
-                                } else {
-                                    acc[r][nt][2 * hh] += e2[r][hh][nt].x;
-                                    acc[r][nt][2 * hh + 1] += e2[r][hh][nt].y;
-                                }
+                                acc[r][nt][2 * hh] += e2[r][hh][nt].x;
+                                acc[r][nt][2 * hh + 1] += e2[r][hh][nt].y;
                             }
                 }
             }
