@@ -23,8 +23,9 @@
 // ((16 + n) * s' - 24 s' = (n - 8) * s', with 24 s' exact in fp16).
 //
 // Work: a unit is one 128-row tile x two 128-column groups (TC_GU); units
-// are numbered tile-major and split evenly over the grid (stream-K), split
-// tiles finished in CTA order as in the other kernels.  A box is four units
+// are numbered tile-major and split evenly over the grid (stream-K); a split
+// tile is finished by its first CTA, which adds the others' published
+// partial sums after its own in CTA order.  A box is four units
 // (fewer at the ends of a CTA's share); boxes never straddle tiles (the
 // kernel needs K a multiple of 1024).  Units alternate between two
 // pipelines, each a dequant warpgroup and an MMA warp with a private ring of
@@ -54,8 +55,10 @@
 //  * warps 10..13, epilogue: thread = row; per box it reads the row's two
 //    accumulators (one per pipeline, each only if the box has a unit of that
 //    pipeline), adds them, multiplies by 2^(E - 137) and adds the result to
-//    its fp32 accumulators; at the end of its share of a tile it writes y, or
-//    for the head hands the tile's logits to the reducer.
+//    its fp32 accumulators; at the end of its share of a tile it multiplies
+//    by the tokens' 2^-s (staged in shared memory), finishes or publishes a
+//    split tile, and writes y, or for the head hands the tile's logits to
+//    the reducer.
 //  * warp 15, reducer (head only): lane t keeps the largest (logit, lowest
 //    id) key of token t over the CTA's finished tiles, read from a
 //    double-buffered shared-memory tile, then runs the grid argmax and the
