@@ -24,8 +24,9 @@
  *    been synchronised.
  *  * A call returns SV_OK or a negative status.  On any error nothing is
  *    launched and no output is touched.
- *  * The library keeps one small scratch area per device (split-tile fp32
- *    partial sums, completion counters, the argmax keys; under 6 MB),
+ *  * The library keeps one scratch area per device (split-tile fp32
+ *    partial sums, the converted activations of calls with T > 8,
+ *    completion counters, the argmax keys; about 32 MB on a 152-SM GPU),
  *    created with cudaMalloc by the first call on that device (so make that
  *    first call outside CUDA-graph capture) and reused afterwards.  Calls
  *    on one device must therefore be ordered with respect to each other
