@@ -411,8 +411,9 @@ int sv_debug_set_fma_consumers(int on);
  * (four n8 token tiles), contiguous rows and K a multiple of 1024 run by
  * default on the 5th-generation tensor cores (tcgen05.mma, M = 128 weight
  * rows x N = 32 tokens x K = 16; the A operand in tensor memory holds the
- * exact fp16 products level x scale x 2^(137 - E), E the largest scale
- * exponent of the row's box of eight groups; each box's fp32 sums are
+ * fp16 products level x scale x 2^(137 - E), E the largest scale exponent
+ * of the row's box of eight groups (exact for every scale of at least
+ * 2^-27 times the box's largest); each box's fp32 sums are
  * accumulated in tensor memory and multiplied by 2^(E - 137) in
  * registers); on = 0 makes them run on mma.sync
  * instead (same results within fp32 rounding order), 1 restores the
